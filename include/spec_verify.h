@@ -1,0 +1,151 @@
+/*
+ * spec_verify.h — C ABI of libspecverify.so: the verify step of speculative sampling on one GPU.
+ *
+ * What the step computes (cited as host + section of the page that defines it):
+ *   - cf-1.com/news/5155685 §2.2 and 2kiu.com/news/5895634 §2.2: a draft token x drawn from the
+ *     draft distribution q is accepted with probability min(1, p(x)/q(x)); on rejection a token is
+ *     drawn from norm(max(0, p - q)), so the emitted token is distributed as p;
+ *   - cf-1.com/news/5155685 §2.1 and gsyq.cn/news/428210 §3.1: positions are judged in order and
+ *     the output is cut at the first rejected position;
+ *   - gsyq.cn/news/428210 §3.2 and 2kiu.com/news/5895634 §3.1: one target forward yields
+ *     1 + a + ... + a^K tokens on average, i.e. when every draft is accepted one more token is
+ *     drawn from p at position K (the bonus token);
+ *   - gsyq.cn/news/428210 §3.3: temperature and top-k are shared sampling parameters of both sides.
+ * Readings where the pages are silent: temperature divides both logit sets; top-k keeps every
+ * logit >= the k-th largest (ties kept and flagged); accept iff u * q(x) < p(x); the inverse CDF
+ * runs in ascending token id with the strict rule u * R < C_v; temperature 0 is the greedy limit
+ * (accept iff x == argmax p, lowest index on ties; the emitted token is that argmax).
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are caller-owned device memory; the library never allocates, frees or
+ *     synchronises (spec_verify_host is the one exception: it synchronises its stream).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream) and is
+ *     asynchronous with respect to the host.
+ *   - The return code covers what the host can check.  Data-dependent problems (a draft token
+ *     outside [0, V), k_per_row outside [0, K_max], NaN / +inf logits, rounding fallbacks) are
+ *     reported per request in stats.flags and never trap.
+ *   - The library keeps no per-call global state and is safe to call from several host threads
+ *     on distinct workspaces.
+ */
+#ifndef SPEC_VERIFY_H_
+#define SPEC_VERIFY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SPEC_DTYPE_F32 = 0, SPEC_DTYPE_BF16 = 1 } spec_dtype_t;
+
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_ERR_INVALID_ARG = 1, /* a null required pointer, a negative size, T < 0, top_k < 0, ...  */
+  SPEC_ERR_UNSUPPORTED = 2, /* sizes beyond the limits below, or an unknown dtype              */
+  SPEC_ERR_CUDA = 3,        /* a CUDA runtime call failed (launch, copy, attribute query)       */
+  SPEC_ERR_WORKSPACE = 4,   /* workspace NULL, misaligned (< 256 B) or smaller than required    */
+  SPEC_ERR_TIMEOUT = 5      /* reserved: no kernel of this library waits on another block       */
+} spec_status_t;
+
+/* Per-request flag bits of spec_verify_stats_t.flags. */
+#define SPEC_FLAG_RESIDUAL_ZERO 1 /* max(0, p - q) summed to 0 after rounding: drew from p   */
+#define SPEC_FLAG_CDF_CLAMP 2     /* u * R fell past the last cumulative sum: took the last v  */
+#define SPEC_FLAG_BAD_TOKEN 4     /* a draft token outside [0, V): treated as p = q = 0        */
+#define SPEC_FLAG_BAD_K 8         /* k_per_row outside [0, K_max]: clamped into range          */
+#define SPEC_FLAG_NONFINITE 16    /* a NaN / +inf logit or an all -inf row: result unspecified */
+#define SPEC_FLAG_TOPK_TIE 32     /* top-k kept more than k logits of some row (ties)          */
+
+/* Limits (SPEC_ERR_UNSUPPORTED beyond them). */
+#define SPEC_MAX_K 16        /* K_max                                                        */
+#define SPEC_MAX_V 2097152   /* vocabulary size                                              */
+#define SPEC_MAX_TOPK 256    /* top_k values in (0, V) above this take SPEC_ERR_UNSUPPORTED   */
+
+/*
+ * Optional diagnostics.  Every pointer is device memory and may be NULL (= not written).
+ *   p_draft, q_draft [B * K_max] float: normalised p_j(x_j), q_j(x_j) at the examined positions
+ *       (j <= first rejection), NaN elsewhere and in greedy mode;
+ *   accept_margin [B * K_max] float: |u_j - p_j(x_j)/q_j(x_j)| (inf when q_j(x_j) == 0), NaN where
+ *       p_draft is NaN; a decision with margin < 1e-5 may legitimately differ from an fp64 oracle;
+ *   sample_margin [B] float: distance of u_resample to the nearer edge of the drawn token's CDF
+ *       interval (inf in greedy mode);
+ *   residual_mass [B] float: sum_v max(0, p - q) at the first rejected position, 0 for a bonus draw;
+ *   row_lognorm [B * (2*K_max + 1)] float: per row, max(z)/T + ln sum_v exp((z_v - max z)/T) over
+ *       the kept set; p rows 0..K_max then q rows 0..K_max-1; NaN for rows past K_b and in greedy mode;
+ *   flags [B] int32: SPEC_FLAG_* bits.
+ */
+typedef struct {
+  float* p_draft;
+  float* q_draft;
+  float* accept_margin;
+  float* sample_margin;
+  float* residual_mass;
+  float* row_lognorm;
+  int32_t* flags;
+} spec_verify_stats_t;
+
+/*
+ * Bytes of device workspace spec_verify needs for these sizes (0 is never returned for valid
+ * sizes; returns 0 for invalid ones).  The workspace must be zero-filled before its first use and
+ * must not be written by the caller between calls: every call leaves its counters at zero again.
+ * One workspace must not be used by two calls that may run at the same time.
+ */
+size_t spec_verify_workspace_bytes(int32_t B, int32_t K_max, int32_t V, spec_dtype_t dtype,
+                                   int32_t top_k);
+
+/*
+ * The verify step for a batch of B independent requests (all pointers device memory):
+ *   p_logits      [B, K_max+1, V] dtype: target logits, position K_b is the bonus position;
+ *   q_logits      [B, K_max, V] dtype: draft logits (may be NULL iff temperature == 0);
+ *   draft_tokens  [B, K_max] int32: x_0..x_{K_b-1} (entries past K_b are not read);
+ *   k_per_row     [B] int32 or NULL: K_b in [0, K_max] drafts of request b (NULL: all K_max);
+ *                 rows past K_b are never read, so ragged batches use the padded layout;
+ *   u_accept      [B, K_max] float in [0, 1): one uniform per (request, position) (NULL iff T == 0);
+ *   u_resample    [B] float in [0, 1): one uniform per request for the resample or bonus draw
+ *                 (NULL iff T == 0);
+ *   temperature   > 0, or 0 for greedy argmax-match;
+ *   top_k         0 = off, >= V = off, else keep the top_k largest logits of every row (<= 256);
+ *   out_tokens    [B, K_max+1] int32: x_0..x_{n-1}, then the resampled / bonus / argmax token,
+ *                 then -1 padding;
+ *   out_num_accepted [B] int32: n = accepted drafts, in [0, K_b];
+ *   out_stats     host struct of device pointers, or NULL;
+ *   workspace     device memory of at least spec_verify_workspace_bytes(...) bytes, 256-B aligned.
+ * Launches one kernel.  Returns SPEC_OK once the work is enqueued.
+ */
+spec_status_t spec_verify(const void* p_logits, const void* q_logits, const int32_t* draft_tokens,
+                          const int32_t* k_per_row, const float* u_accept, const float* u_resample,
+                          float temperature, int32_t top_k, int32_t* out_tokens,
+                          int32_t* out_num_accepted, const spec_verify_stats_t* out_stats, int32_t B,
+                          int32_t K_max, int32_t V, spec_dtype_t dtype, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/*
+ * Device bytes spec_verify_host needs as staging for these sizes (inputs, outputs and the
+ * spec_verify workspace, each 256-B aligned), or 0 for invalid sizes.
+ */
+size_t spec_verify_host_staging_bytes(int32_t B, int32_t K_max, int32_t V, spec_dtype_t dtype,
+                                      int32_t top_k, int32_t has_k_per_row);
+
+/*
+ * The same step on HOST buffers: copies the inputs into `staging` (device memory of at least
+ * spec_verify_host_staging_bytes(...) bytes, zero-filled before its first use and otherwise
+ * owned by this function between calls), runs spec_verify there, copies out_tokens and
+ * out_num_accepted back, and synchronises `stream` before returning.  Host pointers follow the
+ * layouts of spec_verify; q_logits / u_accept / u_resample may be NULL iff temperature == 0 and
+ * k_per_row may be NULL.  Pinned (page-locked) host memory makes the copies asynchronous DMA.
+ */
+spec_status_t spec_verify_host(const void* p_logits, const void* q_logits,
+                               const int32_t* draft_tokens, const int32_t* k_per_row,
+                               const float* u_accept, const float* u_resample, float temperature,
+                               int32_t top_k, int32_t* out_tokens, int32_t* out_num_accepted,
+                               int32_t B, int32_t K_max, int32_t V, spec_dtype_t dtype,
+                               void* staging, size_t staging_bytes, void* stream);
+
+/* A static, human-readable name for a status code. */
+const char* spec_verify_status_string(spec_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H_ */

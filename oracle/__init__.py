@@ -1,0 +1,187 @@
+"""fp64 CPU oracle for the speculative-sampling verify step — TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline / reference legs of
+``bench.py`` may import this package.  The CUDA library never links or calls it, and the two
+share no code: this wrapper loads ``liboracle.so`` built from ``oracle.c`` (plain C, double
+precision) with ``gcc``.
+
+What it computes is stated in ``oracle.c`` with the page passages it follows (cf-1.com §2.1-§2.2,
+2kiu.com §2.2, gsyq.cn §3.1-§3.3).  Logits are passed as float32 arrays or as bf16 raw bits in
+uint16 arrays; every value is widened exactly to double.
+
+Parity unpinned (conventions, fixed by reading only): the top-k tie rule, the ascending-token-id
+CDF order, and the 2^-24 uniform grid.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+DTYPE_F32 = 0
+DTYPE_BF16 = 1
+
+FLAG_RESIDUAL_ZERO = 1
+FLAG_CDF_CLAMP = 2
+FLAG_BAD_TOKEN = 4
+FLAG_BAD_K = 8
+FLAG_NONFINITE = 16
+FLAG_TOPK_TIE = 32
+
+# Flags the build uses: no fast-math and no FMA contraction, so x86 and Arm hosts agree.
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off", "-fno-fast-math"]
+
+
+def build(out: str = _LIB, extra_flags: Optional[list] = None) -> str:
+    """Compile oracle.c into a shared library (``extra_flags`` lets a test build a variant)."""
+    cmd = ["gcc", *CFLAGS, *(extra_flags or []), _SRC, "-o", out, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+def _stale() -> bool:
+    return (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+
+
+_P = ctypes.c_void_p
+
+
+def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
+    i32, f32, f64 = ctypes.c_int, ctypes.c_float, ctypes.c_double
+    lib.oracle_row_dist.argtypes = [_P, i32, i32, f64, i32, _P, _P]
+    lib.oracle_row_dist.restype = i32
+    lib.oracle_decide.argtypes = [_P, _P, i32, i32, _P, _P, f64, _P, _P, _P, _P, _P, _P, _P, _P]
+    lib.oracle_decide.restype = i32
+    lib.oracle_verify.argtypes = [_P, _P, _P, _P, _P, _P, f32, i32, _P, _P, _P, _P, _P, _P, _P,
+                                  _P, _P, i32, i32, i32, i32, i32]
+    lib.oracle_verify.restype = i32
+    lib.oracle_decide_trials.argtypes = [_P, _P, i32, i32, i32, _P, _P, _P, _P, _P, _P, i32]
+    lib.oracle_decide_trials.restype = i32
+    return lib
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load (building first if needed) the oracle library, or a variant at ``path``."""
+    global _lib
+    if path is not None:
+        return _bind(ctypes.CDLL(path))
+    if _lib is None:
+        if _stale():
+            build()
+        _lib = _bind(ctypes.CDLL(_LIB))
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _logits(a: np.ndarray):
+    """(array, dtype code) for float32 logits or bf16 bits held in uint16."""
+    if a.dtype == np.float32:
+        return np.ascontiguousarray(a), DTYPE_F32
+    if a.dtype == np.uint16:
+        return np.ascontiguousarray(a), DTYPE_BF16
+    raise TypeError(f"logits must be float32 or bf16 bits (uint16), got {a.dtype}")
+
+
+def row_dist(z: np.ndarray, temperature: float, top_k: int = 0, lib=None):
+    """Normalised distribution of one logit row.
+
+    Returns (P float64[V], info dict {m, lognorm, threshold, kept}, flags)."""
+    lib = lib or load()
+    z, dt = _logits(z)
+    V = z.shape[-1]
+    P = np.empty(V, np.float64)
+    info = np.empty(4, np.float64)
+    fl = lib.oracle_row_dist(_ptr(z), dt, V, float(temperature), int(top_k), _ptr(P), _ptr(info))
+    return P, dict(m=info[0], lognorm=info[1], threshold=info[2], kept=info[3]), int(fl)
+
+
+def decide(P: np.ndarray, Q: np.ndarray, x, ua, ur: float, lib=None):
+    """The verify decision of one request on fp64 distributions P [(K+1),V], Q [K,V].
+
+    The uniforms are taken as float64 (the batch entry points take the float32 grid values)."""
+    lib = lib or load()
+    P = np.ascontiguousarray(P, np.float64)
+    K = P.shape[0] - 1
+    V = P.shape[1]
+    Q = np.ascontiguousarray(Q, np.float64).reshape(K, V) if K > 0 else np.zeros((1, V))
+    x = np.ascontiguousarray(x, np.int32).reshape(K)
+    ua = np.ascontiguousarray(ua, np.float64).reshape(K)
+    tok = np.empty(K + 1, np.int32)
+    n = np.empty(1, np.int32)
+    pd, qd, am = (np.empty(max(K, 1)) for _ in range(3))
+    sm = np.empty(1)
+    rm = np.empty(1)
+    work = np.empty(V)
+    fl = lib.oracle_decide(_ptr(P), _ptr(Q), V, K, _ptr(x), _ptr(ua), float(ur), _ptr(tok), _ptr(n),
+                           _ptr(pd), _ptr(qd), _ptr(am), _ptr(sm), _ptr(rm), _ptr(work))
+    return dict(tokens=tok, n_acc=int(n[0]), p_draft=pd[:K], q_draft=qd[:K], accept_margin=am[:K],
+                sample_margin=float(sm[0]), residual_mass=float(rm[0]), flags=int(fl))
+
+
+def decide_trials(P: np.ndarray, Q: np.ndarray, x: np.ndarray, ua: np.ndarray, ur: np.ndarray,
+                  nthreads: int = 0, lib=None):
+    """N independent decisions on one shared pair of distributions.
+
+    x, ua: [N, K]; ur: [N].  Returns (tokens [N, K+1], n_acc [N], flags [N])."""
+    lib = lib or load()
+    P = np.ascontiguousarray(P, np.float64)
+    K = P.shape[0] - 1
+    V = P.shape[1]
+    Q = np.ascontiguousarray(Q, np.float64) if K > 0 else np.zeros((1, V))
+    N = ur.shape[0]
+    x = np.ascontiguousarray(x, np.int32).reshape(N, K)
+    ua = np.ascontiguousarray(ua, np.float32).reshape(N, K)
+    ur = np.ascontiguousarray(ur, np.float32)
+    tok = np.empty((N, K + 1), np.int32)
+    n = np.empty(N, np.int32)
+    fl = np.empty(N, np.int32)
+    lib.oracle_decide_trials(_ptr(P), _ptr(Q), V, K, N, _ptr(x), _ptr(ua), _ptr(ur), _ptr(tok),
+                             _ptr(n), _ptr(fl), nthreads or (os.cpu_count() or 1))
+    return tok, n, fl
+
+
+def verify(p: np.ndarray, q: Optional[np.ndarray], draft: np.ndarray, k_per_row: Optional[np.ndarray],
+           ua: Optional[np.ndarray], ur: Optional[np.ndarray], temperature: float, top_k: int = 0,
+           nthreads: int = 1, lib=None) -> dict:
+    """The whole verify step on host arrays, same argument meaning as the CUDA ``spec_verify``.
+
+    p: [B, K_max+1, V], q: [B, K_max, V] (float32 or bf16-as-uint16; q may be None when
+    temperature == 0), draft: [B, K_max] int32, k_per_row: [B] int32 or None, ua: [B, K_max],
+    ur: [B] float32.  Returns a dict of numpy outputs (tokens, n_acc, stats..., flags)."""
+    lib = lib or load()
+    p, dt = _logits(p)
+    B, K1, V = p.shape
+    K_max = K1 - 1
+    if q is not None:
+        q, dtq = _logits(q)
+        assert dtq == dt and q.shape == (B, K_max, V)
+    draft = np.ascontiguousarray(draft, np.int32).reshape(B, K_max)
+    kpr = None if k_per_row is None else np.ascontiguousarray(k_per_row, np.int32)
+    ua = np.zeros((B, K_max), np.float32) if ua is None else np.ascontiguousarray(ua, np.float32)
+    ur = np.zeros(B, np.float32) if ur is None else np.ascontiguousarray(ur, np.float32)
+    out = dict(
+        tokens=np.empty((B, K_max + 1), np.int32), n_acc=np.empty(B, np.int32),
+        p_draft=np.empty((B, K_max)), q_draft=np.empty((B, K_max)), accept_margin=np.empty((B, K_max)),
+        sample_margin=np.empty(B), residual_mass=np.empty(B), row_lognorm=np.empty((B, 2 * K_max + 1)),
+        flags=np.empty(B, np.int32))
+    rc = lib.oracle_verify(_ptr(p), _ptr(q), _ptr(draft), _ptr(kpr), _ptr(ua), _ptr(ur),
+                           float(temperature), int(top_k), _ptr(out["tokens"]), _ptr(out["n_acc"]),
+                           _ptr(out["p_draft"]), _ptr(out["q_draft"]), _ptr(out["accept_margin"]),
+                           _ptr(out["sample_margin"]), _ptr(out["residual_mass"]), _ptr(out["row_lognorm"]),
+                           _ptr(out["flags"]), B, K_max, V, dt, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_verify rejected its arguments")
+    return out

@@ -1,0 +1,384 @@
+/*
+ * oracle.c — plain, slow, fp64 CPU oracle for the speculative-sampling verify step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may link, load or call this file;
+ * only the tests, the smoke check and the benchmark's CPU-baseline leg do.  It shares no
+ * code, header, table or constant with the CUDA library: it restates the method from the
+ * pages, in their order, one request at a time, in double precision.
+ *
+ * Sources (cited as host + section of the page):
+ *   cf-1.com/news/5155685  §2.1  the draft guesses, the target checks, roll back to the first wrong position
+ *   cf-1.com/news/5155685  §2.2  accept x with probability min(1, p(x)/q(x)); on rejection resample
+ *                                from norm(max(0, p(x) - q(x))); the result is distributed as p
+ *   2kiu.com/news/5895634  §2.2  the same rule, written with (p(x) - q(x))_+
+ *   gsyq.cn/news/428210    §3.1  one target forward gives the K positions' logits; judge position by
+ *                                position; keep the accepted part and start drafting again
+ *   gsyq.cn/news/428210    §3.2  E = 1 + a + ... + a^K: the target emits one token beyond the accepted
+ *                                drafts, which is the bonus token when all K are accepted
+ *   gsyq.cn/news/428210    §3.3  temperature and top-k are sampling parameters shared by draft and target
+ *
+ * Readings taken where the pages are silent (each is also listed in the design notes):
+ *   - temperature divides the logits of both p and q; top-k keeps every logit >= the k-th largest
+ *     (ties kept, flagged); the kept set is applied to the raw logits;
+ *   - accept iff u * q(x) < p(x)  (strict; q(x) = 0 accepts iff p(x) > 0);
+ *   - the inverse CDF runs in ascending token id with the strict rule u * R < C_v;
+ *   - n_acc counts accepted drafts; one more token (resampled or bonus) is always emitted;
+ *   - T == 0 is the greedy limit: accept iff x == argmax p (lowest index on ties).
+ *
+ * Pins (tests, not in this file): exhaustive breakpoint enumeration of the decision at V = 4,
+ * K <= 3 (exact output law == p); chi-square over 1e6 seeded trials; the mean emitted count
+ * against (1 - a^(K+1)) / (1 - a) on inputs with exactly known a; softmax against a library
+ * softmax; top-k against a library top-k; greedy against a library argmax.
+ * Parity unpinned (conventions fixed by reading, not by the pages): the top-k tie rule, the CDF
+ * order, the uniform grid.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define OR_DTYPE_F32 0
+#define OR_DTYPE_BF16 1
+
+#define OR_FLAG_RESIDUAL_ZERO 1   /* R == 0 after rounding: resampled from p instead   */
+#define OR_FLAG_CDF_CLAMP 2       /* u * R beyond the last cumulative value (rounding) */
+#define OR_FLAG_BAD_TOKEN 4       /* a draft token outside [0, V)                      */
+#define OR_FLAG_BAD_K 8           /* k_per_row outside [0, K_max]                      */
+#define OR_FLAG_NONFINITE 16      /* NaN / +inf logit, or nothing left to sample from  */
+#define OR_FLAG_TOPK_TIE 32       /* top-k kept more than k logits because of ties     */
+
+/* One logit as an exact double.  bf16 is the upper half of an IEEE binary32. */
+static double logit_at(const void* base, int dtype, size_t i) {
+  if (dtype == OR_DTYPE_F32) return (double)((const float*)base)[i];
+  uint32_t bits = (uint32_t)((const uint16_t*)base)[i] << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+static int cmp_desc(const void* a, const void* b) {
+  double x = *(const double*)a, y = *(const double*)b;
+  return (x < y) - (x > y);
+}
+
+/*
+ * Distribution of one row (gsyq.cn §3.3: temperature and top-k).
+ *   z: V logits; T > 0; top_k: 0 or >= V means no truncation.
+ *   P_out: V doubles, the normalised probabilities.
+ *   info_out (nullable): [0] m = max kept logit, [1] log-normaliser m/T + ln sum_v w_v,
+ *                        [2] top-k threshold t (-inf when off), [3] kept count.
+ * Returns OR_FLAG_NONFINITE if the row holds NaN or +inf or keeps nothing finite,
+ * OR_FLAG_TOPK_TIE if ties made the kept set larger than k.
+ */
+int oracle_row_dist(const void* z, int dtype, int V, double T, int top_k, double* P_out,
+                    double* info_out) {
+  int flags = 0;
+  double t = -INFINITY;
+  for (int v = 0; v < V; ++v) {
+    double x = logit_at(z, dtype, (size_t)v);
+    if (isnan(x) || (isinf(x) && x > 0)) flags |= OR_FLAG_NONFINITE;
+  }
+  if (flags) {
+    for (int v = 0; v < V; ++v) P_out[v] = NAN;
+    if (info_out) info_out[0] = info_out[1] = info_out[2] = info_out[3] = NAN;
+    return flags;
+  }
+  if (top_k > 0 && top_k < V) {
+    /* t = the k-th largest logit, counted with multiplicity (a library sort as the step). */
+    double* s = (double*)malloc(sizeof(double) * (size_t)V);
+    for (int v = 0; v < V; ++v) s[v] = logit_at(z, dtype, (size_t)v);
+    qsort(s, (size_t)V, sizeof(double), cmp_desc);
+    t = s[top_k - 1];
+    free(s);
+  }
+  double m = -INFINITY;
+  int kept = 0;
+  for (int v = 0; v < V; ++v) {
+    double x = logit_at(z, dtype, (size_t)v);
+    if (x >= t) {
+      ++kept;
+      if (x > m) m = x;
+    }
+  }
+  if (top_k > 0 && top_k < V && kept > top_k) flags |= OR_FLAG_TOPK_TIE;
+  if (!(m > -INFINITY)) { /* every kept logit is -inf: nothing to sample from */
+    for (int v = 0; v < V; ++v) P_out[v] = NAN;
+    if (info_out) {
+      info_out[0] = m;
+      info_out[1] = NAN;
+      info_out[2] = t;
+      info_out[3] = kept;
+    }
+    return flags | OR_FLAG_NONFINITE;
+  }
+  double sum = 0.0;
+  for (int v = 0; v < V; ++v) {
+    double x = logit_at(z, dtype, (size_t)v);
+    double w = (x >= t) ? exp((x - m) / T) : 0.0;
+    P_out[v] = w;
+    sum += w;
+  }
+  for (int v = 0; v < V; ++v) P_out[v] /= sum;
+  if (info_out) {
+    info_out[0] = m;
+    info_out[1] = m / T + log(sum);
+    info_out[2] = t;
+    info_out[3] = kept;
+  }
+  return flags;
+}
+
+/*
+ * Inverse-CDF draw from the non-negative weights r[0..V) with total R, in ascending token id:
+ * y = the smallest v with u * R < C_v, C_v = r_0 + ... + r_v.  If rounding leaves no such v,
+ * y = the last v with r_v > 0 and OR_FLAG_CDF_CLAMP is returned.  *margin = the distance of u
+ * to the nearer edge of y's interval, min(u - C_{y-1}/R, C_y/R - u).
+ */
+static int inverse_cdf(const double* r, int V, double R, double u, int32_t* y, double* margin) {
+  double target = u * R, C = 0.0;
+  for (int v = 0; v < V; ++v) {
+    double prev = C;
+    C += r[v];
+    if (target < C) {
+      double lo = u - prev / R, hi = C / R - u;
+      *y = v;
+      *margin = lo < hi ? lo : hi;
+      return 0;
+    }
+  }
+  *y = -1;
+  for (int v = V - 1; v >= 0; --v)
+    if (r[v] > 0.0) {
+      *y = v;
+      break;
+    }
+  *margin = 0.0;
+  return OR_FLAG_CDF_CLAMP;
+}
+
+/*
+ * The decision for one request, on its normalised distributions (cf-1.com §2.2, 2kiu.com §2.2,
+ * cf-1.com §2.1, gsyq.cn §3.1-§3.2).
+ *   P: (K+1) rows of V doubles, p at positions 0..K (row K is the bonus position);
+ *   Q: K rows of V doubles;  x: K draft tokens;  ua: K accept uniforms;  ur: resample uniform
+ *   (uniforms in [0, 1), taken as doubles so a test can place them anywhere on the real line).
+ *   out_tokens: K+1 entries (x_0..x_{n-1}, y, then -1);  *n_acc: accepted drafts.
+ *   p_draft, q_draft, accept_margin: K entries each (NaN past the first rejection);
+ *   sample_margin, residual_mass: scalars.  work: V doubles of scratch.
+ * Returns the request's flags.
+ */
+int oracle_decide(const double* P, const double* Q, int V, int K, const int32_t* x,
+                  const double* ua, double ur, int32_t* out_tokens, int32_t* n_acc, double* p_draft,
+                  double* q_draft, double* accept_margin, double* sample_margin,
+                  double* residual_mass, double* work) {
+  int flags = 0;
+  for (int j = 0; j <= K; ++j) out_tokens[j] = -1;
+  for (int j = 0; j < K; ++j) p_draft[j] = q_draft[j] = accept_margin[j] = NAN;
+
+  /* Acceptance, position by position, stopping at the first rejection. */
+  int jstar = K;
+  for (int j = 0; j < K; ++j) {
+    double a = 0.0, c = 0.0;
+    if (x[j] < 0 || x[j] >= V)
+      flags |= OR_FLAG_BAD_TOKEN; /* p(x) = q(x) = 0: never accepted */
+    else {
+      a = P[(size_t)j * V + x[j]];
+      c = Q[(size_t)j * V + x[j]];
+    }
+    double u = ua[j];
+    p_draft[j] = a;
+    q_draft[j] = c;
+    accept_margin[j] = (c > 0.0) ? fabs(u - a / c) : INFINITY;
+    if (u * c < a) { /* u < p/q, with q = 0 accepting iff p > 0 */
+      out_tokens[j] = x[j];
+      continue;
+    }
+    jstar = j;
+    break;
+  }
+  *n_acc = jstar;
+
+  const double* Pj = P + (size_t)jstar * V;
+  double R = 0.0;
+  if (jstar < K) {
+    /* Residual max(0, p - q) at the first rejected position. */
+    const double* Qj = Q + (size_t)jstar * V;
+    for (int v = 0; v < V; ++v) {
+      double d = Pj[v] - Qj[v];
+      work[v] = d > 0.0 ? d : 0.0;
+      R += work[v];
+    }
+    *residual_mass = R;
+    if (!(R > 0.0)) { /* only reachable through rounding: fall back to p */
+      flags |= OR_FLAG_RESIDUAL_ZERO;
+      R = 0.0;
+      for (int v = 0; v < V; ++v) {
+        work[v] = Pj[v];
+        R += work[v];
+      }
+    }
+  } else {
+    /* Every draft accepted: the bonus token from p at position K. */
+    for (int v = 0; v < V; ++v) {
+      work[v] = Pj[v];
+      R += work[v];
+    }
+    *residual_mass = 0.0;
+  }
+  flags |= inverse_cdf(work, V, R, ur, &out_tokens[jstar], sample_margin);
+  return flags;
+}
+
+/* Greedy limit (T == 0): g = argmax with the lowest index on ties.  -1 if the row has NaN. */
+static int32_t argmax_row(const void* z, int dtype, int V, int* flags) {
+  int32_t g = -1;
+  double best = -INFINITY;
+  for (int v = 0; v < V; ++v) {
+    double x = logit_at(z, dtype, (size_t)v);
+    if (isnan(x)) {
+      *flags |= OR_FLAG_NONFINITE;
+      return -1;
+    }
+    if (g < 0 || x > best) {
+      best = x;
+      g = v;
+    }
+  }
+  return g;
+}
+
+/*
+ * The whole verify step over a batch, with the same argument meaning as the CUDA library's
+ * spec_verify, on host arrays.  Layout: p [B, K_max+1, V], q [B, K_max, V] (dtype), draft [B, K_max],
+ * k_per_row [B] (NULL = K_max for all), ua [B, K_max], ur [B].
+ * Outputs (all host, all required): out_tokens [B, K_max+1], out_n_acc [B], p_draft / q_draft /
+ * accept_margin [B, K_max], sample_margin / residual_mass [B], row_lognorm [B, 2*K_max+1]
+ * (p rows 0..K_max, then q rows 0..K_max-1; NaN where unused), flags [B].
+ * A request whose rows are non-finite gets n_acc = 0 and tokens -1 (its result is unspecified).
+ * nthreads > 1 runs requests in parallel (OpenMP); the result does not depend on it.
+ */
+int oracle_verify(const void* p, const void* q, const int32_t* draft, const int32_t* k_per_row,
+                  const float* ua, const float* ur, float temperature, int top_k, int32_t* out_tokens,
+                  int32_t* out_n_acc, double* p_draft, double* q_draft, double* accept_margin,
+                  double* sample_margin, double* residual_mass, double* row_lognorm,
+                  int32_t* out_flags, int B, int K_max, int V, int dtype, int nthreads) {
+  if (B < 0 || K_max < 0 || K_max > 64 || V <= 0 || !(temperature >= 0.0f) || top_k < 0) return 1;
+  if (nthreads < 1) nthreads = 1;
+  const int rows_lognorm = 2 * K_max + 1;
+  const size_t es = dtype == OR_DTYPE_F32 ? 4 : 2;
+  const double T = (double)temperature;
+
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+  for (int b = 0; b < B; ++b) {
+    int flags = 0;
+    int K = k_per_row ? k_per_row[b] : K_max;
+    if (K < 0 || K > K_max) {
+      flags |= OR_FLAG_BAD_K;
+      K = K < 0 ? 0 : K_max;
+    }
+    const char* pb = (const char*)p + (size_t)b * (K_max + 1) * V * es;
+    const char* qb = q ? (const char*)q + (size_t)b * K_max * V * es : NULL;
+    const int32_t* xb = draft + (size_t)b * K_max;
+    const float* uab = ua ? ua + (size_t)b * K_max : NULL;
+    int32_t* tok = out_tokens + (size_t)b * (K_max + 1);
+    double* pd = p_draft + (size_t)b * K_max;
+    double* qd = q_draft + (size_t)b * K_max;
+    double* am = accept_margin + (size_t)b * K_max;
+    double* ln = row_lognorm + (size_t)b * rows_lognorm;
+    for (int j = 0; j <= K_max; ++j) tok[j] = -1;
+    for (int j = 0; j < K_max; ++j) pd[j] = qd[j] = am[j] = NAN;
+    for (int r = 0; r < rows_lognorm; ++r) ln[r] = NAN;
+    sample_margin[b] = NAN;
+    residual_mass[b] = NAN;
+
+    if (temperature == 0.0f) {
+      /* Greedy: accept while the draft equals the target's argmax.  Every row 0..K is examined
+         (so a NaN anywhere in the request is flagged), then the decision is taken. */
+      int32_t g[64 + 1];
+      for (int j = 0; j <= K; ++j) g[j] = argmax_row(pb + (size_t)j * V * es, dtype, V, &flags);
+      int n = K;
+      for (int j = 0; j <= K; ++j) {
+        if (j == K) {
+          tok[j] = g[j];
+          break;
+        }
+        if (xb[j] < 0 || xb[j] >= V) flags |= OR_FLAG_BAD_TOKEN;
+        if (xb[j] == g[j]) {
+          tok[j] = xb[j];
+          continue;
+        }
+        tok[j] = g[j];
+        n = j;
+        break;
+      }
+      sample_margin[b] = INFINITY;
+      residual_mass[b] = 0.0;
+      if (flags & OR_FLAG_NONFINITE) {
+        for (int j = 0; j <= K_max; ++j) tok[j] = -1;
+        n = 0;
+      }
+      out_n_acc[b] = n;
+      out_flags[b] = flags;
+      continue;
+    }
+
+    double uad[64];
+    for (int j = 0; j < K; ++j) uad[j] = uab ? (double)uab[j] : 0.0;
+    double* Pr = (double*)malloc(sizeof(double) * (size_t)(K + 1) * V);
+    double* Qr = (double*)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1) * V);
+    double* work = (double*)malloc(sizeof(double) * (size_t)V);
+    double info[4];
+    for (int j = 0; j <= K; ++j) {
+      flags |= oracle_row_dist(pb + (size_t)j * V * es, dtype, V, T, top_k, Pr + (size_t)j * V, info);
+      ln[j] = info[1];
+    }
+    for (int j = 0; j < K; ++j) {
+      flags |= oracle_row_dist(qb + (size_t)j * V * es, dtype, V, T, top_k, Qr + (size_t)j * V, info);
+      ln[K_max + 1 + j] = info[1];
+    }
+    int32_t n = 0;
+    if (flags & OR_FLAG_NONFINITE) {
+      for (int j = 0; j <= K_max; ++j) tok[j] = -1;
+    } else {
+      flags |= oracle_decide(Pr, Qr, V, K, xb, uad, (double)ur[b], tok, &n, pd, qd, am, &sample_margin[b],
+                             &residual_mass[b], work);
+    }
+    out_n_acc[b] = n;
+    out_flags[b] = flags;
+    free(Pr);
+    free(Qr);
+    free(work);
+  }
+  return 0;
+}
+
+/*
+ * Many independent trials of oracle_decide on one shared pair of distributions (the pins'
+ * chi-square and Monte-Carlo checks): P [(K+1), V], Q [K, V]; x, ua [N, K]; ur [N].
+ * Outputs out_tokens [N, K+1], out_n_acc [N], out_flags [N].
+ */
+int oracle_decide_trials(const double* P, const double* Q, int V, int K, int N, const int32_t* x,
+                         const float* ua, const float* ur, int32_t* out_tokens, int32_t* out_n_acc,
+                         int32_t* out_flags, int nthreads) {
+  if (nthreads < 1) nthreads = 1;
+#pragma omp parallel num_threads(nthreads)
+  {
+    double* work = (double*)malloc(sizeof(double) * (size_t)V);
+    double* scratch = (double*)malloc(sizeof(double) * (size_t)(4 * (K > 0 ? K : 1)));
+    double sm, rm;
+#pragma omp for schedule(static)
+    for (int i = 0; i < N; ++i) {
+      double* uad = scratch + 3 * K;
+      for (int j = 0; j < K; ++j) uad[j] = (double)ua[(size_t)i * K + j];
+      out_flags[i] = oracle_decide(P, Q, V, K, x + (size_t)i * K, uad, (double)ur[i],
+                                   out_tokens + (size_t)i * (K + 1), &out_n_acc[i], scratch,
+                                   scratch + K, scratch + 2 * K, &sm, &rm, work);
+    }
+    free(work);
+    free(scratch);
+  }
+  return 0;
+}
