@@ -1,0 +1,382 @@
+"""Benchmark of the speculative-sampling verify step (one JSON line on rank 0).
+
+A step is one spec_verify call over one batch of synthetic requests whose logits are already
+resident in HBM.  The default workload is the largest batch, B=1024 requests x K=4 drafts over a
+128256-token vocabulary in bf16 (alpha ~ 0.8, T = 1): 2.36 GB of logits per step, well above the
+129 MB L2, and two copies of the inputs alternate between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c5_a0.8] [--impl reference]
+
+value     = verified draft positions per second over all ranks (sum_b K_b / step time)
+roofline  = logits bytes per launch / mean kernel time, against the measured HBM copy peak
+e2e       = the same metric through spec_verify_host (pinned host buffers, copies included)
+cpu_baseline = the fp64 oracle on the host cores, on a bounded sample of the same workload
+Multi-GPU (torchrun): every rank verifies its own batch of distinct requests (weak scaling, no
+collective on the data path); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "verified draft positions/s and logits GB/s (fraction of GB300 HBM peak)"
+UNIT = "positions/s"
+KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_rejection_verify_gb300", "csrc", "spec_verify.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+# ------------------------------------------------------------------------------------------------
+# distributed plumbing (host logic; tested with gloo on CPU)
+# ------------------------------------------------------------------------------------------------
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def shard_requests(B: int, rank: int) -> range:
+    """The requests rank `rank` verifies: its own B distinct requests (weak scaling)."""
+    return range(rank * B, (rank + 1) * B)
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for _, _, fl in rows for n, v in zip(names, fl) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------------------------------
+# helpers
+# ------------------------------------------------------------------------------------------------
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_for(workload_key: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on this kernel."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        t = json.load(f)
+    if t.get("kernel_sha256_16") != kernel_hash():
+        return None
+    e = t.get("workloads", {}).get(workload_key)
+    return None if e is None else e.get("dram_bytes_per_launch")
+
+
+def describe(w: W.Workload) -> str:
+    kk = f"K_b~U{{{w.ragged[0]}..{w.ragged[1]}}}" if w.ragged else f"K={w.K}"
+    extra = " greedy" if w.temperature == 0 else f" T={w.temperature:g}" + (f" top_k={w.top_k}" if w.top_k else "")
+    return f"{w.key if not w.greedy else 'c5_greedy'}: B={w.B} {kk} V={w.V} {w.dtype}{extra}" + \
+        (f" alpha~{w.alpha:g}" if w.alpha is not None and not w.greedy else "")
+
+
+def cpu_baseline(w: W.Workload, budget_requests: int):
+    """The oracle, as it stands, on the host cores over a bounded sample of the workload."""
+    import oracle
+    n = min(budget_requests, w.B)
+    d = W.generate(w, requests=range(n))
+    cores = os.cpu_count() or 1
+    kpr = d["k_per_row"] if w.ragged else None
+    t0 = time.perf_counter()
+    oracle.verify(d["p"], None if w.temperature == 0 else d["q"], d["draft"], kpr, d["ua"], d["ur"],
+                  w.temperature, w.top_k, nthreads=cores)
+    dt = time.perf_counter() - t0
+    pos = int(d["k_per_row"].sum())
+    return {"value": pos / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"first {n} of the {w.B} requests, one oracle call, OpenMP over requests ({dt:.2f} s)"}, pos, dt
+
+
+# ------------------------------------------------------------------------------------------------
+# arms
+# ------------------------------------------------------------------------------------------------
+def run_reference(args, w: W.Workload):
+    """The oracle timed on the host cores: --warmup + --steps oracle calls, each over a sample of
+    the workload's requests sized so the whole run stays within about two minutes."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    cores = os.cpu_count() or 1
+    q_of = lambda d: None if w.temperature == 0 else d["q"]  # noqa: E731
+    kpr_of = lambda d: d["k_per_row"] if w.ragged else None  # noqa: E731
+    probe = W.generate(w, requests=range(min(8, w.B)))
+    t0 = time.perf_counter()
+    oracle.verify(probe["p"], q_of(probe), probe["draft"], kpr_of(probe), probe["ua"], probe["ur"], w.temperature,
+                  w.top_k, nthreads=cores)
+    per_req = (time.perf_counter() - t0) / probe["p"].shape[0]
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)
+    n = int(max(1, min(args.ref_requests, w.B, budget / max(per_req, 1e-9))))
+    d = W.generate(w, requests=range(n))
+
+    def one():
+        oracle.verify(d["p"], q_of(d), d["draft"], kpr_of(d), d["ua"], d["ur"], w.temperature, w.top_k,
+                      nthreads=cores)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    dt = (time.perf_counter() - t0) / args.steps
+    pos = int(d["k_per_row"].sum())
+    v = pos / dt
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generator; no dataset)",
+            "config": {"workload": describe(w), "sample_requests": n},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"first {n} of the {w.B} requests per step, OpenMP over requests"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args, w: W.Workload):
+    import torch
+    import speculative_decoding_rejection_verify_gb300 as sv
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sv.load()
+
+    reqs = shard_requests(w.B, rank)
+    d = W.generate(w, requests=reqs)
+    ragged = w.ragged is not None
+    greedy = w.temperature == 0
+    kb = d["k_per_row"]
+    positions = int(kb.sum())
+    logits_bytes = W.algorithmic_bytes(w, kb)
+
+    def up(a):
+        if a is None:
+            return None
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == np.uint16 else torch.from_numpy(a)
+        return t.to(dev)
+
+    # two copies of the inputs alternate, so no step finds the previous step's logits in L2
+    copies = []
+    for _ in range(2):
+        copies.append(dict(p=up(d["p"]), q=None if greedy else up(d["q"]), x=up(d["draft"]),
+                           k=up(kb) if ragged else None, ua=None if greedy else up(d["ua"]),
+                           ur=None if greedy else up(d["ur"])))
+    B, K, V = len(reqs), w.K, w.V
+    dt_code = sv.DTYPE_BF16 if w.dtype == "bf16" else sv.DTYPE_F32
+    ws = torch.zeros(sv.workspace_bytes(B, K, V, dt_code, w.top_k), dtype=torch.uint8, device=dev)
+    tok = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    nacc = torch.empty((B,), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        c = copies[i & 1]
+        sv.verify(c["p"], c["q"], c["x"], c["k"], c["ua"], c["ur"], w.temperature, w.top_k,
+                  workspace_tensor=ws, stream=stream, out=(tok, nacc))
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    gpu_id = "0"
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    with ClockSampler(gpu_id) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step(i)
+            ev[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    total_ms = t_start.elapsed_time(t_end)
+    per_launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    step_ms = max_over_ranks(total_ms / args.steps, world, dev)
+    all_positions = sum_over_ranks(positions, world, dev)
+    value = all_positions / (step_ms * 1e-3)
+
+    # end to end: host buffers through spec_verify_host (H2D + verify + D2H, synchronous)
+    e2e = None
+    if args.e2e_steps > 0:
+        pin = lambda a: None if a is None else torch.from_numpy(a).pin_memory().numpy()  # noqa: E731
+        hp = dict(p=pin(d["p"]), q=None if greedy else pin(d["q"]), x=pin(d["draft"]), k=pin(kb) if ragged else None,
+                  ua=None if greedy else pin(d["ua"]), ur=None if greedy else pin(d["ur"]))
+        htok = torch.empty((B, K + 1), dtype=torch.int32).pin_memory().numpy()
+        hn = torch.empty((B,), dtype=torch.int32).pin_memory().numpy()
+
+        def hstep():
+            sv.verify_host(hp["p"], hp["q"], hp["x"], hp["k"], hp["ua"], hp["ur"], w.temperature, w.top_k,
+                           device=dev, stream=stream, out=(htok, hn))
+
+        for _ in range(2):
+            hstep()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            hstep()
+        e2e_s = max_over_ranks((time.perf_counter() - t0) / args.e2e_steps, world, dev)
+        h2d = sum(a.nbytes for a in hp.values() if a is not None)
+        e2e = {"value": all_positions / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(htok.nbytes + hn.nbytes), "ms_per_step": e2e_s * 1e3,
+               "steps": args.e2e_steps}
+
+    if rank != 0:
+        return 0
+    peak, peak_kind = measured_peak()
+    achieved = logits_bytes / (per_launch_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded generator; no dataset)",
+        "config": {"workload": describe(w), "B_per_gpu": B, "K": K, "V": V, "temperature": w.temperature,
+                   "top_k": w.top_k, "logits_bytes_per_step": logits_bytes,
+                   "l2": "inputs larger than L2 (129 MB); two input copies alternate between steps",
+                   "parallelism": f"{world} independent batches (no collective)"},
+        "logits_gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": traffic_for(w.key if not w.greedy else "c5_greedy"),
+                     "kernel": "verify_kernel", "per_launch_ms": per_launch_ms},
+        "gpu_launches": args.steps * (2 if ragged else 1),
+        "clocks": clk.summary(),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        cb, _, _ = cpu_baseline(w, args.cpu_requests)
+        line["cpu_baseline"] = cb
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="c5_a0.8", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-requests", type=int, default=1024)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-requests", type=int, default=64, help="reference arm: max requests per step")
+    ap.add_argument("--ref-seconds", type=float, default=120.0, help="reference arm: time budget")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = W.get(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,265 @@
+"""Python binding of libspecverify.so — the speculative-sampling verify step on one GB300 GPU.
+
+Argument marshalling only: every step of the verify computation runs in the library's CUDA
+kernels (``csrc/spec_verify.cu``); PyTorch supplies device memory and the current stream.  There is
+no CPU fallback: without the compiled library every call raises.
+
+The C ABI is declared in ``include/spec_verify.h``; the names here mirror it:
+
+* ``verify(p, q, draft, k_per_row, u_accept, u_resample, temperature, top_k, stats=False)``
+  -> ``(tokens [B, K+1] int32, num_accepted [B] int32, stats dict | None)`` on device tensors;
+* ``verify_host(...)`` the same on host (numpy / CPU torch) arrays through ``spec_verify_host``;
+* ``workspace_bytes(B, K, V, dtype, top_k)``.
+
+Logits are ``torch.float32`` or ``torch.bfloat16`` tensors ``p [B, K+1, V]`` and ``q [B, K, V]``
+(q may be None at temperature 0).  The verify rule (cf-1.com/news/5155685 §2.2,
+2kiu.com/news/5895634 §2.2, gsyq.cn/news/428210 §3.1-§3.3) is restated in the header.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Dict, Optional, Tuple
+
+import numpy as np
+
+from . import _build
+
+SPEC_OK = 0
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: "workspace", 5: "timeout"}
+DTYPE_F32, DTYPE_BF16 = 0, 1
+
+FLAG_RESIDUAL_ZERO = 1
+FLAG_CDF_CLAMP = 2
+FLAG_BAD_TOKEN = 4
+FLAG_BAD_K = 8
+FLAG_NONFINITE = 16
+FLAG_TOPK_TIE = 32
+
+MAX_K = 16
+MAX_V = 2097152
+MAX_TOPK = 256
+
+EXPORTS = ("spec_verify_workspace_bytes", "spec_verify", "spec_verify_host_staging_bytes",
+           "spec_verify_host", "spec_verify_status_string")
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: status {code} ({STATUS.get(code, '?')})")
+        self.code = code
+
+
+class StatsStruct(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("p_draft", "q_draft", "accept_margin", "sample_margin", "residual_mass", "row_lognorm", "flags")]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """The loaded library.  Raises if it has not been built (there is no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if build_if_missing and _build.stale():
+                _build.build()
+            if not os.path.exists(_build.LIB):
+                raise RuntimeError(f"libspecverify.so is not built ({_build.LIB}); run "
+                                   "`python -m speculative_decoding_rejection_verify_gb300._build`")
+            lib = ctypes.CDLL(_build.LIB)
+            P, I, F, Z = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+            lib.spec_verify_workspace_bytes.argtypes = [I, I, I, I, I]
+            lib.spec_verify_workspace_bytes.restype = Z
+            lib.spec_verify.argtypes = [P, P, P, P, P, P, F, I, P, P, ctypes.POINTER(StatsStruct),
+                                        I, I, I, I, P, Z, P]
+            lib.spec_verify.restype = I
+            lib.spec_verify_host_staging_bytes.argtypes = [I, I, I, I, I, I]
+            lib.spec_verify_host_staging_bytes.restype = Z
+            lib.spec_verify_host.argtypes = [P, P, P, P, P, P, F, I, P, P, I, I, I, I, P, Z, P]
+            lib.spec_verify_host.restype = I
+            lib.spec_verify_status_string.argtypes = [I]
+            lib.spec_verify_status_string.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def workspace_bytes(B: int, K: int, V: int, dtype: int, top_k: int = 0) -> int:
+    n = load().spec_verify_workspace_bytes(B, K, V, dtype, top_k)
+    if n == 0:
+        raise SpecVerifyError(1, "spec_verify_workspace_bytes")
+    return n
+
+
+# Workspaces are cached per (device, stream): the kernel leaves them zeroed for the next call.
+_ws_cache: Dict[Tuple[int, int], object] = {}
+
+
+def workspace(nbytes: int, device, stream_handle: int):
+    torch = _torch()
+    key = (device.index if device.index is not None else torch.cuda.current_device(), stream_handle)
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _check(t, name, shape, dtype, device):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)} != {tuple(shape)}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype} != {dtype}")
+    if t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+def verify(p, q, draft, k_per_row=None, u_accept=None, u_resample=None, temperature: float = 1.0,
+           top_k: int = 0, stats: bool = False, workspace_tensor=None, stream=None, out=None):
+    """Run spec_verify on device tensors; returns (tokens, num_accepted, stats | None).
+
+    ``out``: optional (tokens, num_accepted) tensors to write into.  ``stream``: a
+    torch.cuda.Stream (default: the current stream).  The call is asynchronous."""
+    torch = _torch()
+    lib = load()
+    if p.dim() != 3:
+        raise ValueError("p must be [B, K+1, V]")
+    B, K1, V = p.shape
+    K = K1 - 1
+    dev = p.device
+    if dev.type != "cuda":
+        raise ValueError("verify() takes CUDA tensors; use verify_host() for host arrays")
+    dt = _dtype_code(p)
+    _check(p, "p", (B, K + 1, V), p.dtype, dev)
+    if q is not None:
+        _check(q, "q", (B, K, V), p.dtype, dev)
+    if draft is not None:
+        _check(draft, "draft", (B, K), torch.int32, dev)
+    if k_per_row is not None:
+        _check(k_per_row, "k_per_row", (B,), torch.int32, dev)
+    if u_accept is not None:
+        _check(u_accept, "u_accept", (B, K), torch.float32, dev)
+    if u_resample is not None:
+        _check(u_resample, "u_resample", (B,), torch.float32, dev)
+    st = stream if stream is not None else torch.cuda.current_stream(dev)
+    handle = st.cuda_stream
+    if out is None:
+        tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+        nacc = torch.empty((B,), dtype=torch.int32, device=dev)
+    else:
+        tokens, nacc = out
+    sd = None
+    sp = None
+    if stats:
+        f32 = dict(dtype=torch.float32, device=dev)
+        sd = dict(p_draft=torch.empty((B, K), **f32), q_draft=torch.empty((B, K), **f32),
+                  accept_margin=torch.empty((B, K), **f32), sample_margin=torch.empty((B,), **f32),
+                  residual_mass=torch.empty((B,), **f32), row_lognorm=torch.empty((B, 2 * K + 1), **f32),
+                  flags=torch.empty((B,), dtype=torch.int32, device=dev))
+        sp = StatsStruct(**{k: v.data_ptr() for k, v in sd.items()})
+    nbytes = workspace_bytes(B, K, V, dt, top_k)
+    ws = workspace_tensor if workspace_tensor is not None else workspace(nbytes, dev, handle)
+    rc = lib.spec_verify(_ptr(p), _ptr(q), _ptr(draft), _ptr(k_per_row), _ptr(u_accept), _ptr(u_resample),
+                         float(temperature), int(top_k), tokens.data_ptr(), nacc.data_ptr(),
+                         ctypes.byref(sp) if sp is not None else None, B, K, V, dt, ws.data_ptr(),
+                         ws.numel(), handle)
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_verify")
+    return tokens, nacc, sd
+
+
+_stage_cache: Dict[int, object] = {}
+
+
+def staging_bytes(B: int, K: int, V: int, dtype: int, top_k: int, ragged: bool) -> int:
+    n = load().spec_verify_host_staging_bytes(B, K, V, dtype, top_k, int(ragged))
+    if n == 0:
+        raise SpecVerifyError(1, "spec_verify_host_staging_bytes")
+    return n
+
+
+def verify_host(p, q, draft, k_per_row=None, u_accept=None, u_resample=None, temperature: float = 1.0,
+                top_k: int = 0, staging=None, device=None, stream=None, out=None):
+    """spec_verify_host on host arrays (numpy, or CPU torch tensors; pinned memory recommended).
+
+    ``p``/``q``: float32 arrays or bf16 bits as uint16 (numpy) / torch.bfloat16 (CPU tensors).
+    Returns (tokens [B, K+1] int32, num_accepted [B] int32) as numpy arrays (or writes ``out``).
+    The call blocks until the results are on the host."""
+    torch = _torch()
+    lib = load()
+
+    def host(a, dtype=None):
+        if a is None:
+            return None, None
+        if isinstance(a, np.ndarray):
+            a = np.ascontiguousarray(a if dtype is None else a.astype(dtype, copy=False))
+            return a, a.ctypes.data
+        if a.device.type != "cpu" or not a.is_contiguous():
+            raise ValueError("verify_host takes contiguous host arrays")
+        return a, a.data_ptr()
+
+    if isinstance(p, np.ndarray):
+        dt = DTYPE_BF16 if p.dtype == np.uint16 else DTYPE_F32
+        if p.dtype not in (np.uint16, np.float32):
+            raise TypeError("p must be float32 or bf16 bits (uint16)")
+    else:
+        dt = _dtype_code(p)
+    B, K1, V = p.shape
+    K = K1 - 1
+    p, pp = host(p)
+    q, qp = host(q)
+    draft, dp = host(draft, np.int32)
+    k_per_row, kp = host(k_per_row, np.int32)
+    u_accept, ap = host(u_accept, np.float32)
+    u_resample, rp = host(u_resample, np.float32)
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    nbytes = staging_bytes(B, K, V, dt, top_k, k_per_row is not None)
+    if staging is None:
+        key = dev.index if dev.index is not None else torch.cuda.current_device()
+        staging = _stage_cache.get(key)
+        if staging is None or staging.numel() < nbytes:
+            staging = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+            _stage_cache[key] = staging
+    if out is None:
+        tokens = np.empty((B, K + 1), np.int32)
+        nacc = np.empty(B, np.int32)
+        tp, npp = tokens.ctypes.data, nacc.ctypes.data
+    else:
+        tokens, nacc = out
+        tp, npp = (tokens.ctypes.data, nacc.ctypes.data) if isinstance(tokens, np.ndarray) else \
+            (tokens.data_ptr(), nacc.data_ptr())
+    st = stream if stream is not None else torch.cuda.current_stream(dev)
+    rc = lib.spec_verify_host(pp, qp, dp, kp, ap, rp, float(temperature), int(top_k), tp, npp, B, K, V, dt,
+                              staging.data_ptr(), staging.numel(), st.cuda_stream)
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_verify_host")
+    return tokens, nacc

@@ -1,0 +1,1431 @@
+// spec_verify.cu — the verify step of speculative sampling as one fused sm_103a kernel.
+//
+// What is computed (host + section of the page that defines it):
+//   cf-1.com/news/5155685 §2.2, 2kiu.com/news/5895634 §2.2  accept x ~ q with probability
+//       min(1, p(x)/q(x)); on rejection draw from norm(max(0, p - q));
+//   cf-1.com/news/5155685 §2.1, gsyq.cn/news/428210 §3.1     cut the output at the first rejection;
+//   gsyq.cn/news/428210 §3.2                                  all K accepted: one more token from p;
+//   gsyq.cn/news/428210 §3.3                                  temperature / top-k on both sides.
+//
+// Design.  The work is a stream over every logit of every valid row (HBM bound), plus a small
+// per-request tail.  One persistent kernel does all of it:
+//   * the item space is (request, row, 8192-logit chunk) in request-major order; CTAs take items
+//     from an atomic counter (one 16-32 KB chunk per item, read with 128-bit non-allocating loads);
+//   * each item leaves a per-chunk summary in the workspace: (max, sum of exp) for sampling,
+//     (max, lowest argmax) for greedy, the chunk's top-k candidates for top-k;
+//   * the CTA that completes the last item of a request (a counter per request; no block ever
+//     waits for another) combines the summaries into each row's normaliser, runs the ratio test
+//     and the first-rejection scan, and draws the resampled / bonus token by inverse CDF over the
+//     one or two rows it needs, which were streamed microseconds earlier and are still in L2;
+//   * all counters return to zero by the end of the kernel, so the workspace is reusable.
+// A request-major item order keeps only a few requests in flight, which is what keeps the rows of
+// the final draw L2-resident.  There is no tensor-core work: nothing here is a contraction.
+
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "spec_verify.h"
+
+namespace sv {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kChunk = 8192;             // logits per work item
+constexpr int kPer = kChunk / kThreads;  // logits per thread per item
+constexpr int kTile = 256;               // inverse-CDF tile: 32 lanes x 8 logits
+constexpr int kCandCap = 256;            // top-k candidates stored per chunk
+constexpr int kSurvCap = 1024;           // survivors examined per chunk
+constexpr int kRowCap = 256;             // candidates >= the row's lower bound, per row
+constexpr int kMaxRows = 2 * SPEC_MAX_K + 1;
+constexpr int kUnrollA = 4;              // tiles in flight per warp in the CDF passes
+
+enum Mode { kSample = 0, kTopK = 1, kGreedy = 2 };
+
+// Per-chunk top-k metadata word: count | flags.
+constexpr uint32_t kMetaOverflow = 1u << 30;
+constexpr uint32_t kMetaNaN = 1u << 31;
+constexpr uint32_t kMetaCount = (1u << 30) - 1;
+
+struct Params {
+  const void* p;
+  const void* q;
+  const int32_t* draft;
+  const int32_t* kpr;
+  const float* ua;
+  const float* ur;
+  int32_t* out_tokens;
+  int32_t* out_nacc;
+  float* p_draft;
+  float* q_draft;
+  float* acc_margin;
+  float* samp_margin;
+  float* resid_mass;
+  float* lognorm;
+  int32_t* flags;
+  int B, K, V, top_k, nchunk, R;  // R = padded rows per request (2K+1, or K+1 in greedy)
+  float c2;                       // log2(e) / T
+  float invT;                     // 1 / T
+  uint32_t* sched;                // [0] next item, [1] finished CTAs
+  uint32_t* req_cnt;              // [B] items completed per request
+  float2* partial;                // [B, R, nchunk]
+  uint2* cmeta;                   // [B, R, nchunk] top-k: (k-th largest key of the chunk, count|flags)
+  uint2* cand;                    // [B, R, nchunk, kCandCap] top-k: (key, token)
+  const uint32_t* rowmap;         // ragged: [rows] (b << 6 | padded row); null = uniform layout
+  const uint32_t* total_rows;     // ragged: number of valid rows
+  uint32_t uniform_items;         // uniform layout: B * R * nchunk
+};
+
+// ------------------------------------------------------------------------------------------------
+// small helpers
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+template <typename T>
+__device__ __forceinline__ float to_f(T x);
+template <>
+__device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f<uint16_t>(uint16_t x) { return __uint_as_float((uint32_t)x << 16); }
+
+template <typename T>
+__device__ __forceinline__ float load1(const T* p) { return to_f<T>(__ldg(p)); }
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// Total order on floats as unsigned keys (-0 is folded into +0; NaN handled by callers).
+__device__ __forceinline__ uint32_t fkey(float f) {
+  uint32_t u = __float_as_uint(f + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float keyf(uint32_t k) {
+  uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+  return __uint_as_float(u);
+}
+
+// Merge two (max, sum of exp2((z - max) * c2)) pairs.  A pair with sum 0 carries no mass.
+__device__ __forceinline__ void lse_merge(float& m, float& s, float mo, float so, float c2) {
+  float mn = fmaxf(m, mo);
+  float a = (s == 0.0f) ? 0.0f : s * exp2f((m - mn) * c2);
+  float b = (so == 0.0f) ? 0.0f : so * exp2f((mo - mn) * c2);
+  m = mn;
+  s = a + b;
+}
+
+__device__ __forceinline__ void lse_warp(float& m, float& s, float c2) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float mo = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+    float so = __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    lse_merge(m, s, mo, so, c2);
+  }
+}
+
+// argmax with the lowest index on ties
+__device__ __forceinline__ void amax_merge(float& v, int& i, float vo, int io) {
+  if (vo > v || (vo == v && io < i)) {
+    v = vo;
+    i = io;
+  }
+}
+
+// max that returns NaN if either input is NaN (so a NaN logit poisons its row's sum)
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+  return x;
+}
+
+// Row pointers in the padded layouts p [B, K+1, V] and q [B, K, V].
+template <typename T>
+__device__ __forceinline__ const T* prow(const Params& P, int b, int j) {
+  return static_cast<const T*>(P.p) + ((size_t)b * (P.K + 1) + j) * (size_t)P.V;
+}
+template <typename T>
+__device__ __forceinline__ const T* qrow(const Params& P, int b, int j) {
+  return static_cast<const T*>(P.q) + ((size_t)b * P.K + j) * (size_t)P.V;
+}
+// Padded row index rp: p rows 0..K, q rows K+1..2K.
+template <typename T>
+__device__ __forceinline__ const T* row_ptr(const Params& P, int b, int rp) {
+  return rp <= P.K ? prow<T>(P, b, rp) : qrow<T>(P, b, rp - P.K - 1);
+}
+
+__device__ __forceinline__ int clamp_k(const Params& P, int b, int* bad) {
+  int k = P.kpr ? __ldg(P.kpr + b) : P.K;
+  if (k < 0 || k > P.K) {
+    if (bad) *bad = 1;
+    k = k < 0 ? 0 : P.K;
+  }
+  return k;
+}
+
+// ------------------------------------------------------------------------------------------------
+// chunk loading: 32 logits per thread; slot i of thread t holds chunk-local logit elem(i, t)
+// ------------------------------------------------------------------------------------------------
+template <typename T, bool VEC>
+__device__ __forceinline__ int elem_of(int i, int t) {
+  if (VEC) {
+    constexpr int VW = 16 / sizeof(T);
+    return ((i / VW) * kThreads + t) * VW + (i % VW);
+  }
+  return i * kThreads + t;
+}
+
+// Loads logits [0, n) of the chunk starting at `base`; invalid slots get -inf.
+template <typename T, bool VEC>
+__device__ __forceinline__ void load_chunk(const T* __restrict__ base, int n, float (&v)[kPer]) {
+  const int t = threadIdx.x;
+  if (VEC) {
+    constexpr int VW = 16 / sizeof(T);
+    constexpr int L = kPer / VW;
+    uint4 raw[L];
+#pragma unroll
+    for (int l = 0; l < L; ++l) {
+      int e0 = (l * kThreads + t) * VW;
+      if (e0 < n)
+        raw[l] = ldg_stream(base + e0);
+      else
+        raw[l] = make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+    }
+#pragma unroll
+    for (int l = 0; l < L; ++l) {
+      const uint32_t w[4] = {raw[l].x, raw[l].y, raw[l].z, raw[l].w};
+      int e0 = (l * kThreads + t) * VW;
+      bool ok = e0 < n;
+      if (sizeof(T) == 2) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          v[l * 8 + 2 * k] = ok ? bf16_lo(w[k]) : -INFINITY;
+          v[l * 8 + 2 * k + 1] = ok ? bf16_hi(w[k]) : -INFINITY;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[l * 4 + k] = __uint_as_float(w[k]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      int e = i * kThreads + t;
+      v[i] = e < n ? load1<T>(base + e) : -INFINITY;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// shared memory
+// ------------------------------------------------------------------------------------------------
+struct Smem {
+  int item;
+  int last;
+  float red_m[kWarps];
+  float red_s[kWarps];
+  int red_i[kWarps];
+  uint32_t red_k[kWarps];
+  int red_c[kWarps];
+  int nsurv;
+  int nkept;
+  uint32_t meta;
+  // finisher
+  float rowM[kMaxRows];
+  float rowS[kMaxRows];
+  float rowT[kMaxRows];  // top-k threshold (-inf when off)
+  int rowG[kMaxRows];    // greedy argmax
+  int rowFlag[kMaxRows];
+  int Kb, jstar, flags, nonfinite;
+  int tile, seg_first, found;
+  float tile_base, total;
+  float incl[kThreads];
+  int y;
+  float margin;
+};
+
+// ------------------------------------------------------------------------------------------------
+// per-item work
+// ------------------------------------------------------------------------------------------------
+template <typename T, bool VEC>
+__device__ void item_sample(const Params& P, const T* base, int n, float2* out, Smem& sm) {
+  float v[kPer];
+  load_chunk<T, VEC>(base, n, v);
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) m = fmax_nan(m, v[i]);
+  float s = 0.0f;
+  if (m != -INFINITY) {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) s += exp2f((v[i] - m) * P.c2);
+  }
+  lse_warp(m, s, P.c2);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    sm.red_m[warp] = m;
+    sm.red_s[warp] = s;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    m = lane < kWarps ? sm.red_m[lane] : -INFINITY;
+    s = lane < kWarps ? sm.red_s[lane] : 0.0f;
+    lse_warp(m, s, P.c2);
+    if (lane == 0) *out = make_float2(m, s);
+  }
+}
+
+template <typename T, bool VEC>
+__device__ void item_greedy(const Params& P, const T* base, int n, float2* out, Smem& sm) {
+  float v[kPer];
+  load_chunk<T, VEC>(base, n, v);
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  float best = -INFINITY;
+  int bi = 0x7FFFFFFF;
+  bool nan = false;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    int e = elem_of<T, VEC>(i, t);
+    if (e < n) {
+      nan |= v[i] != v[i];
+      amax_merge(best, bi, v[i], e);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float vo = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+    int io = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+    amax_merge(best, bi, vo, io);
+  }
+  bool anynan = __syncthreads_or(nan);
+  if (lane == 0) {
+    sm.red_m[warp] = best;
+    sm.red_i[warp] = bi;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    best = lane < kWarps ? sm.red_m[lane] : -INFINITY;
+    bi = lane < kWarps ? sm.red_i[lane] : 0x7FFFFFFF;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      float vo = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+      int io = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+      amax_merge(best, bi, vo, io);
+    }
+    if (lane == 0) *out = make_float2(best, __int_as_float(anynan ? -1 : bi));
+  }
+}
+
+// Descending bitonic sort of one key per lane across a warp.
+__device__ __forceinline__ uint32_t warp_sort_desc(uint32_t x) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, x, j);
+      bool up = ((lane & k) == 0);      // this pair's block sorts descending when up
+      bool lower = ((lane & j) == 0);   // this lane holds the lower index of the pair
+      uint32_t hi = max(x, y), lo = min(x, y);
+      x = (up == lower) ? hi : lo;
+    }
+  }
+  return x;
+}
+
+// Top-k candidates of one chunk: every logit >= the chunk's k-th largest (ties kept).  Stored as
+// (key, token) pairs plus a meta word (count | overflow | NaN) and the chunk's k-th largest key
+// (0 when the chunk holds fewer than k logits).
+template <typename T, bool VEC>
+__device__ void item_topk(const Params& P, const T* base, int n, int v0, uint2* cand, uint2* meta,
+                          Smem& sm, uint2* surv) {
+  float v[kPer];
+  load_chunk<T, VEC>(base, n, v);
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int k = P.top_k;
+  uint32_t key[kPer];
+  uint32_t tmax = 0;
+  bool nan = false;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    int e = elem_of<T, VEC>(i, t);
+    bool ok = e < n && v[i] == v[i];
+    nan |= (e < n) && (v[i] != v[i]);
+    key[i] = ok ? fkey(v[i]) : 0u;  // 0 = no logit (every real key is > 0)
+    tmax = max(tmax, key[i]);
+  }
+  // Lower bound theta0 on the chunk's k-th largest: in each warp with data, the c_w-th largest of
+  // its per-thread maxima, c_w = min(ceil(k / warps with data), threads with data).  Those maxima
+  // are distinct logits, so at least sum_w c_w logits are >= min_w theta_w.
+  unsigned has = __ballot_sync(0xFFFFFFFFu, tmax != 0u);
+  if (lane == 0) sm.red_c[warp] = __popc(has);
+  __syncthreads();
+  int nw = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) nw += sm.red_c[w] > 0;
+  const int kp = (k + nw - 1) / max(nw, 1);
+  uint32_t sorted = warp_sort_desc(tmax);
+  int cw = min(kp, __popc(has));
+  uint32_t thw = cw > 0 ? __shfl_sync(0xFFFFFFFFu, sorted, cw - 1) : 0xFFFFFFFFu;
+  __syncthreads();  // red_c reads done
+  if (lane == 0) {
+    sm.red_k[warp] = thw;
+    sm.red_c[warp] = cw;
+  }
+  if (t == 0) sm.nsurv = 0;
+  __syncthreads();
+  uint32_t theta = 0xFFFFFFFFu;
+  int certified = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    if (sm.red_c[w] > 0) theta = min(theta, sm.red_k[w]);
+    certified += sm.red_c[w];
+  }
+  if (kp > 32 || certified < k) theta = 1u;  // no usable bound: every logit survives
+  // survivors -> shared buffer
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    bool s = key[i] >= theta && key[i] != 0u;
+    unsigned bal = __ballot_sync(0xFFFFFFFFu, s);
+    if (bal) {
+      int base_slot = 0;
+      if (lane == 0) base_slot = atomicAdd(&sm.nsurv, __popc(bal));
+      base_slot = __shfl_sync(0xFFFFFFFFu, base_slot, 0);
+      if (s) {
+        int slot = base_slot + __popc(bal & ((1u << lane) - 1u));
+        if (slot < kSurvCap) surv[slot] = make_uint2(key[i], (uint32_t)(v0 + elem_of<T, VEC>(i, t)));
+      }
+    }
+  }
+  bool anynan = __syncthreads_or(nan);
+  const int ns = sm.nsurv;
+  if (t == 0) sm.nkept = 0;
+  __syncthreads();
+  if (ns > kSurvCap) {
+    if (t == 0) {
+      *meta = make_uint2(0u, kMetaOverflow | (anynan ? kMetaNaN : 0u));
+    }
+    return;
+  }
+  // exact selection among the survivors: keep those with fewer than k survivors strictly greater
+  uint32_t kth = 0xFFFFFFFFu;
+  for (int i = t; i < ns; i += kThreads) {
+    uint32_t ki = surv[i].x;
+    int greater = 0;
+    for (int j = 0; j < ns; ++j) greater += surv[j].x > ki;
+    if (greater < k) {
+      int slot = atomicAdd(&sm.nkept, 1);
+      if (slot < kCandCap) cand[slot] = surv[i];
+      kth = min(kth, ki);
+    }
+  }
+  // the chunk's k-th largest is the smallest kept key when the chunk holds >= k logits
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) kth = min(kth, __shfl_xor_sync(0xFFFFFFFFu, kth, o));
+  if (lane == 0) sm.red_k[warp] = kth;
+  __syncthreads();
+  if (t == 0) {
+    uint32_t mk = 0xFFFFFFFFu;
+    for (int w = 0; w < kWarps; ++w) mk = min(mk, sm.red_k[w]);
+    int nk = sm.nkept;
+    uint32_t fl = (anynan ? kMetaNaN : 0u) | (nk > kCandCap ? kMetaOverflow : 0u);
+    *meta = make_uint2(ns >= k ? mk : 0u, (uint32_t)min(nk, kCandCap) | fl);
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// finisher pieces
+// ------------------------------------------------------------------------------------------------
+// Loads the 8 logits [e0, e0+8) of a row (e0 a multiple of 8); logits at or past V read -inf.
+template <typename T, bool VEC>
+__device__ __forceinline__ void load8(const T* __restrict__ row, int e0, int V, float (&z)[8]) {
+  if (VEC) {
+    if (sizeof(T) == 2) {
+      if (e0 < V) {
+        uint4 r = ldg_stream(row + e0);
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          z[2 * k] = bf16_lo(w[k]);
+          z[2 * k + 1] = bf16_hi(w[k]);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) z[k] = -INFINITY;
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        int e = e0 + 4 * h;
+        if (e < V) {
+          uint4 r = ldg_stream(row + e);
+          z[4 * h] = __uint_as_float(r.x);
+          z[4 * h + 1] = __uint_as_float(r.y);
+          z[4 * h + 2] = __uint_as_float(r.z);
+          z[4 * h + 3] = __uint_as_float(r.w);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) z[4 * h + k] = -INFINITY;
+        }
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) z[k] = (e0 + k < V) ? load1<T>(row + e0 + k) : -INFINITY;
+  }
+}
+
+// Weights of the inverse-CDF draw for 8 logits: the residual max(0, P - Q) when `resid`, else the
+// (unnormalised) target weights exp((z_p - M_p)/T) on the kept set.
+struct DrawRows {
+  float Mp, invSp, Tp;  // target row: max, 1/sum, top-k threshold
+  float Mq, invSq, Tq;  // draft row
+  bool resid;
+};
+
+template <typename T, bool VEC>
+__device__ __forceinline__ void weights8(const T* pr, const T* qr, int e0, int V, const DrawRows& d,
+                                         float c2, float (&w)[8]) {
+  float zp[8];
+  load8<T, VEC>(pr, e0, V, zp);
+  if (d.resid) {
+    float zq[8];
+    load8<T, VEC>(qr, e0, V, zq);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      float a = zp[k] >= d.Tp ? __fmul_rn(exp2f(__fmul_rn(__fsub_rn(zp[k], d.Mp), c2)), d.invSp) : 0.0f;
+      float b = zq[k] >= d.Tq ? __fmul_rn(exp2f(__fmul_rn(__fsub_rn(zq[k], d.Mq), c2)), d.invSq) : 0.0f;
+      w[k] = fmaxf(__fsub_rn(a, b), 0.0f);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w[k] = zp[k] >= d.Tp ? exp2f(__fmul_rn(__fsub_rn(zp[k], d.Mp), c2)) : 0.0f;
+  }
+}
+
+// Inverse-CDF draw over a whole row: y = the smallest v with u * R < C_v, C_v cumulative in
+// ascending token id, computed hierarchically (8 logits per lane, 256 per warp tile, tiles by
+// segments per thread).  Returns R; sets sm.y, sm.margin and the clamp flag.
+template <typename T, bool VEC>
+__device__ float draw_row(const Params& P, const T* pr, const T* qr, const DrawRows& d, float u,
+                          float* wt, Smem& sm, int* clamp) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int V = P.V;
+  const int ntile = (V + kTile - 1) / kTile;
+  // pass A: tile sums
+  for (int i0 = warp; i0 < ntile; i0 += kWarps * kUnrollA) {
+    float w[kUnrollA][8];
+#pragma unroll
+    for (int u4 = 0; u4 < kUnrollA; ++u4) {
+      int i = i0 + u4 * kWarps;
+      if (i < ntile)
+        weights8<T, VEC>(pr, qr, i * kTile + lane * 8, V, d, P.c2, w[u4]);
+      else
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[u4][k] = 0.0f;
+    }
+#pragma unroll
+    for (int u4 = 0; u4 < kUnrollA; ++u4) {
+      int i = i0 + u4 * kWarps;
+      float s = 0.0f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) s += w[u4][k];
+      s = warp_sum(s);
+      if (lane == 0 && i < ntile) wt[i] = s;
+    }
+  }
+  __syncthreads();
+  // segments of tiles per thread, then a block inclusive scan of the segment sums
+  const int L = (ntile + kThreads - 1) / kThreads;
+  const int s0 = t * L, s1 = min(s0 + L, ntile);
+  float seg = 0.0f;
+  for (int i = s0; i < s1; ++i) seg += wt[i];
+  float x = seg;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    float y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sm.red_s[warp] = x;
+  if (t == 0) sm.seg_first = kThreads;
+  __syncthreads();
+  float off = 0.0f;
+  for (int w = 0; w < warp; ++w) off += sm.red_s[w];
+  const float incl = x + off;
+  sm.incl[t] = incl;
+  if (t == kThreads - 1) sm.total = incl;
+  __syncthreads();
+  const float R = sm.total;
+  if (!(R > 0.0f)) return R;  // caller handles an empty residual
+  const float target = u * R;
+  if (target < incl) atomicMin(&sm.seg_first, t);
+  if (t == 0) sm.found = 0;
+  __syncthreads();
+  const int tf = sm.seg_first;
+  if (t == (tf == kThreads ? 0 : tf)) {
+    int found = -1;
+    float run = 0.0f;
+    if (tf < kThreads) {
+      run = t == 0 ? 0.0f : sm.incl[t - 1];
+      for (int i = s0; i < s1; ++i) {
+        if (target < run + wt[i]) {
+          found = i;
+          break;
+        }
+        run += wt[i];
+      }
+    }
+    if (found >= 0) {
+      sm.tile = found;
+      sm.tile_base = run;
+      sm.found = 1;
+    } else {
+      // rounding left the target past the sums: the last tile with mass before the limit
+      const int lim = tf < kThreads ? s1 : ntile;
+      int i = lim - 1;
+      while (i >= 0 && !(wt[i] > 0.0f)) --i;
+      if (i < 0) {
+        i = lim;
+        while (i < ntile - 1 && !(wt[i] > 0.0f)) ++i;
+      }
+      float base = 0.0f;
+      for (int j = 0; j < i; ++j) base += wt[j];
+      sm.tile = i;
+      sm.tile_base = base;
+      sm.found = 2;
+    }
+  }
+  __syncthreads();
+  // inside the tile: one warp, 8 logits per lane
+  if (warp == 0) {
+    const int tile = sm.tile;
+    const float tbase = sm.tile_base;
+    bool clamped = sm.found == 2;
+    float w[8];
+    weights8<T, VEC>(pr, qr, tile * kTile + lane * 8, V, d, P.c2, w);
+    float ls = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) ls += w[k];
+    float li = ls;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      float y = __shfl_up_sync(0xFFFFFFFFu, li, o);
+      if (lane >= o) li += y;
+    }
+    float le = __shfl_up_sync(0xFFFFFFFFu, li, 1);
+    if (lane == 0) le = 0.0f;
+    const float tl = target - tbase;
+    unsigned hit = clamped ? 0u : __ballot_sync(0xFFFFFFFFu, tl < li);
+    int yl, ye = -1;
+    float run, margin = 0.0f;
+    if (hit) {
+      yl = __ffs(hit) - 1;
+      if (lane == yl) {
+        run = le;
+        for (int k = 0; k < 8; ++k) {
+          if (tl < run + w[k]) {
+            ye = k;
+            margin = fminf(tl - run, run + w[k] - tl) / R;
+            break;
+          }
+          run += w[k];
+        }
+        if (ye < 0) {  // sub-ulp disagreement between levels: last logit with mass in the lane
+          for (int k = 7; k >= 0; --k)
+            if (w[k] > 0.0f) {
+              ye = k;
+              break;
+            }
+          margin = 0.0f;
+          clamped = true;
+        }
+      }
+    } else {
+      unsigned pos = __ballot_sync(0xFFFFFFFFu, ls > 0.0f);
+      yl = pos ? 31 - __clz(pos) : 0;
+      if (lane == yl) {
+        for (int k = 7; k >= 0; --k)
+          if (w[k] > 0.0f) {
+            ye = k;
+            break;
+          }
+        if (ye < 0) ye = 0;
+      }
+      clamped = true;
+    }
+    if (lane == yl) {
+      sm.y = tile * kTile + yl * 8 + ye;
+      sm.margin = clamped ? 0.0f : margin;
+      if (clamped) *clamp = 1;
+    }
+  }
+  __syncthreads();
+  return R;
+}
+
+// Row threshold, max and sum for top-k from the chunks' candidates.  One warp per row.
+// Returns false if the row needs the exact full-row path (candidate overflow).
+template <typename T>
+__device__ bool topk_row_fast(const Params& P, int b, int rp, uint2* buf, float& M, float& S,
+                              float& thr, int& flags) {
+  const int lane = threadIdx.x & 31;
+  const int nch = P.nchunk;
+  const uint2* meta = P.cmeta + ((size_t)b * P.R + rp) * nch;
+  const uint2* cand = P.cand + ((size_t)b * P.R + rp) * nch * (size_t)kCandCap;
+  // lower bound L = the largest chunk-local k-th largest
+  uint32_t Lk = 0;
+  bool ovf = false, nan = false;
+  for (int c = lane; c < nch; c += 32) {
+    uint2 mt = __ldcg(meta + c);
+    Lk = max(Lk, mt.x);
+    ovf |= (mt.y & kMetaOverflow) != 0;
+    nan |= (mt.y & kMetaNaN) != 0;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) Lk = max(Lk, __shfl_xor_sync(0xFFFFFFFFu, Lk, o));
+  ovf = __any_sync(0xFFFFFFFFu, ovf);
+  nan = __any_sync(0xFFFFFFFFu, nan);
+  if (nan) flags |= SPEC_FLAG_NONFINITE;
+  if (ovf) return false;
+  // gather candidates >= L into the warp's buffer
+  int n = 0;
+  for (int c = 0; c < nch; ++c) {
+    const int cnt = (int)(__ldcg(&meta[c].y) & kMetaCount);
+    for (int i0 = 0; i0 < cnt; i0 += 32) {
+      const int i = i0 + lane;
+      uint2 e = make_uint2(0u, 0u);
+      if (i < cnt) e = __ldcg(cand + (size_t)c * kCandCap + i);
+      const bool s = i < cnt && e.x >= Lk;
+      const unsigned bal = __ballot_sync(0xFFFFFFFFu, s);
+      const int slot = n + __popc(bal & ((1u << lane) - 1u));
+      if (s && slot < kRowCap) buf[slot] = e;
+      n += __popc(bal);
+    }
+  }
+  if (n > kRowCap) return false;
+  __syncwarp();
+  // exact k-th largest among the gathered candidates
+  const int k = P.top_k;
+  uint32_t kth = 0xFFFFFFFFu, mx = 0;
+  for (int i = lane; i < n; i += 32) {
+    uint32_t ki = buf[i].x;
+    int greater = 0;
+    for (int j = 0; j < n; ++j) greater += buf[j].x > ki;
+    if (greater < k) kth = min(kth, ki);
+    mx = max(mx, ki);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    kth = min(kth, __shfl_xor_sync(0xFFFFFFFFu, kth, o));
+    mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  }
+  if (n == 0) return false;
+  M = keyf(mx);
+  thr = keyf(kth);
+  float s = 0.0f;
+  int kept = 0;
+  for (int i = lane; i < n; i += 32) {
+    if (buf[i].x >= kth) {
+      s += exp2f((keyf(buf[i].x) - M) * P.c2);
+      ++kept;
+    }
+  }
+  S = warp_sum(s);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) kept += __shfl_xor_sync(0xFFFFFFFFu, kept, o);
+  if (kept > k) flags |= SPEC_FLAG_TOPK_TIE;
+  return true;
+}
+
+// Exact top-k statistics of a whole row by radix selection over the row (whole CTA).
+template <typename T, bool VEC>
+__device__ void topk_row_exact(const Params& P, const T* row, uint32_t* hist, Smem& sm, float& M,
+                               float& S, float& thr, int& flags) {
+  const int t = threadIdx.x;
+  const int V = P.V, k = P.top_k;
+  uint32_t prefix = 0, mask = 0;
+  int kk = k;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = t; i < 256; i += kThreads) hist[i] = 0;
+    __syncthreads();
+    for (int e = t; e < V; e += kThreads) {
+      float z = load1<T>(row + e);
+      if (z != z) continue;
+      uint32_t key = fkey(z);
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (t == 0) {
+      int acc = 0, d = 255;
+      for (; d > 0; --d) {
+        if (acc + (int)hist[d] >= kk) break;
+        acc += (int)hist[d];
+      }
+      sm.red_c[0] = d;
+      sm.red_c[1] = kk - acc;
+    }
+    __syncthreads();
+    prefix |= (uint32_t)sm.red_c[0] << shift;
+    mask |= 255u << shift;
+    kk = sm.red_c[1];
+    __syncthreads();
+  }
+  thr = keyf(prefix);
+  // max and sum over the kept set
+  float m = -INFINITY;
+  for (int e = t; e < V; e += kThreads) {
+    float z = load1<T>(row + e);
+    if (z >= thr) m = fmaxf(m, z);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if ((t & 31) == 0) sm.red_m[t >> 5] = m;
+  __syncthreads();
+  m = -INFINITY;
+  for (int w = 0; w < kWarps; ++w) m = fmaxf(m, sm.red_m[w]);
+  float s = 0.0f;
+  int kept = 0;
+  for (int e = t; e < V; e += kThreads) {
+    float z = load1<T>(row + e);
+    if (z >= thr) {
+      s += exp2f((z - m) * P.c2);
+      ++kept;
+    }
+  }
+  s = warp_sum(s);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) kept += __shfl_xor_sync(0xFFFFFFFFu, kept, o);
+  __syncthreads();
+  if ((t & 31) == 0) {
+    sm.red_s[t >> 5] = s;
+    sm.red_c[t >> 5] = kept;
+  }
+  __syncthreads();
+  s = 0.0f;
+  kept = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    s += sm.red_s[w];
+    kept += sm.red_c[w];
+  }
+  M = m;
+  S = s;
+  if (kept > k) flags |= SPEC_FLAG_TOPK_TIE;
+  __syncthreads();
+}
+
+// The per-request tail, run by the CTA that completed the request's last item.
+template <typename T, int MODE, bool VEC>
+__device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* dyn) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int K = P.K;
+  if (t == 0) {
+    int bad = 0;
+    sm.Kb = clamp_k(P, b, &bad);
+    sm.flags = bad ? SPEC_FLAG_BAD_K : 0;
+    sm.nonfinite = 0;
+  }
+  __syncthreads();
+  const int Kb = sm.Kb;
+  const int nrows = MODE == kGreedy ? Kb + 1 : 2 * Kb + 1;
+  // ---- row statistics ----
+  if (MODE == kSample) {
+    for (int r = warp; r < nrows; r += kWarps) {
+      const int rp = r <= Kb ? r : K + 1 + (r - Kb - 1);
+      const float2* part = P.partial + ((size_t)b * P.R + rp) * P.nchunk;
+      float m = -INFINITY, s = 0.0f;
+      for (int c = lane; c < P.nchunk; c += 32) {
+        float2 pc = __ldcg(part + c);
+        lse_merge(m, s, pc.x, pc.y, P.c2);
+      }
+      lse_warp(m, s, P.c2);
+      if (lane == 0) {
+        sm.rowM[r] = m;
+        sm.rowS[r] = s;
+        sm.rowT[r] = -INFINITY;
+        sm.rowFlag[r] = (!(s > 0.0f) || isinf(m) || isnan(s)) ? SPEC_FLAG_NONFINITE : 0;
+      }
+    }
+  } else if (MODE == kGreedy) {
+    for (int r = warp; r < nrows; r += kWarps) {
+      const float2* part = P.partial + ((size_t)b * P.R + r) * P.nchunk;
+      float best = -INFINITY;
+      int bi = 0x7FFFFFFF;
+      bool nan = false;
+      for (int c = lane; c < P.nchunk; c += 32) {
+        float2 pc = __ldcg(part + c);
+        int idx = __float_as_int(pc.y);
+        if (idx < 0) nan = true;
+        amax_merge(best, bi, pc.x, idx);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        float vo = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+        int io = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+        amax_merge(best, bi, vo, io);
+      }
+      nan = __any_sync(0xFFFFFFFFu, nan);
+      if (lane == 0) {
+        sm.rowG[r] = bi;
+        sm.rowFlag[r] = nan ? SPEC_FLAG_NONFINITE : 0;
+      }
+    }
+  } else {  // kTopK
+    uint2* buf = reinterpret_cast<uint2*>(dyn) + (size_t)warp * kRowCap;
+    for (int r = warp; r < nrows; r += kWarps) {
+      const int rp = r <= Kb ? r : K + 1 + (r - Kb - 1);
+      float M = NAN, S = NAN, thr = NAN;
+      int fl = 0;
+      bool ok = topk_row_fast<T>(P, b, rp, buf, M, S, thr, fl);
+      if (lane == 0) {
+        sm.rowM[r] = M;
+        sm.rowS[r] = S;
+        sm.rowT[r] = thr;
+        if (!ok && !(fl & SPEC_FLAG_NONFINITE)) fl |= 0x40000000;  // needs the exact path
+        if (ok && (!(S > 0.0f) || isinf(M) || isnan(S))) fl |= SPEC_FLAG_NONFINITE;
+        sm.rowFlag[r] = fl;
+      }
+      __syncwarp();
+    }
+    __syncthreads();
+    for (int r = 0; r < nrows; ++r) {
+      if (sm.rowFlag[r] & 0x40000000) {
+        const int rp = r <= Kb ? r : K + 1 + (r - Kb - 1);
+        float M, S, thr;
+        int fl = 0;
+        topk_row_exact<T, VEC>(P, row_ptr<T>(P, b, rp), reinterpret_cast<uint32_t*>(dyn), sm, M, S,
+                               thr, fl);
+        if (t == 0) {
+          sm.rowM[r] = M;
+          sm.rowS[r] = S;
+          sm.rowT[r] = thr;
+          sm.rowFlag[r] = fl | ((!(S > 0.0f) || isinf(M) || isnan(S)) ? SPEC_FLAG_NONFINITE : 0);
+        }
+        __syncthreads();
+      }
+    }
+  }
+  __syncthreads();
+  if (t == 0) {
+    int f = 0;
+    for (int r = 0; r < nrows; ++r) f |= sm.rowFlag[r];
+    sm.flags |= f;
+    sm.nonfinite = (f & SPEC_FLAG_NONFINITE) != 0;
+  }
+  __syncthreads();
+
+  // ---- ratio test and first rejection (warp 0; K <= 16) ----
+  int32_t* tok = P.out_tokens + (size_t)b * (K + 1);
+  if (warp == 0) {
+    bool examined_bad = false;
+    int jstar;
+    float a = NAN, cq = NAN, am = NAN;
+    int x = 0;
+    if (MODE == kGreedy) {
+      bool acc = true, bad = false;
+      if (lane < Kb) {
+        x = __ldg(P.draft + (size_t)b * K + lane);
+        bad = x < 0 || x >= P.V;
+        acc = x == sm.rowG[lane];
+      }
+      unsigned rej = __ballot_sync(0xFFFFFFFFu, lane < Kb && !acc);
+      jstar = rej ? __ffs(rej) - 1 : Kb;
+      unsigned badm = __ballot_sync(0xFFFFFFFFu, bad);
+      examined_bad = jstar < Kb && ((badm >> jstar) & 1u);
+      if (lane <= K) {
+        int v = -1;
+        if (lane < jstar) v = x;
+        else if (lane == jstar) v = sm.rowG[jstar];
+        tok[lane] = v;
+      }
+      if (lane == 0) {
+        sm.jstar = jstar;
+        sm.y = sm.rowG[jstar];
+        sm.margin = INFINITY;
+      }
+    } else {
+      bool acc = true, bad = false;
+      if (lane < Kb) {
+        x = __ldg(P.draft + (size_t)b * K + lane);
+        bad = x < 0 || x >= P.V;
+        a = 0.0f;
+        cq = 0.0f;
+        if (!bad) {
+          const float zp = load1<T>(prow<T>(P, b, lane) + x);
+          const float zq = load1<T>(qrow<T>(P, b, lane) + x);
+          const int rq = Kb + 1 + lane;
+          if (zp >= sm.rowT[lane]) a = exp2f((zp - sm.rowM[lane]) * P.c2) / sm.rowS[lane];
+          if (zq >= sm.rowT[rq]) cq = exp2f((zq - sm.rowM[rq]) * P.c2) / sm.rowS[rq];
+        }
+        const float u = __ldg(P.ua + (size_t)b * K + lane);
+        acc = u * cq < a;
+        am = cq > 0.0f ? fabsf(u - a / cq) : INFINITY;
+      }
+      unsigned rej = __ballot_sync(0xFFFFFFFFu, lane < Kb && !acc);
+      jstar = rej ? __ffs(rej) - 1 : Kb;
+      unsigned badm = __ballot_sync(0xFFFFFFFFu, bad);
+      examined_bad = jstar < Kb && ((badm >> jstar) & 1u);
+      if (lane < K) {
+        const bool ex = lane <= jstar && lane < Kb;
+        if (P.p_draft) P.p_draft[(size_t)b * K + lane] = ex ? a : NAN;
+        if (P.q_draft) P.q_draft[(size_t)b * K + lane] = ex ? cq : NAN;
+        if (P.acc_margin) P.acc_margin[(size_t)b * K + lane] = ex ? am : NAN;
+      }
+      if (lane <= K) tok[lane] = lane < jstar ? x : -1;
+      if (lane == 0) sm.jstar = jstar;
+    }
+    if (lane == 0 && examined_bad) sm.flags |= SPEC_FLAG_BAD_TOKEN;
+  }
+  __syncthreads();
+
+  // ---- resample at the first rejection, or the bonus draw ----
+  if (MODE != kGreedy && !sm.nonfinite) {
+    const int js = sm.jstar;
+    const float u = __ldg(P.ur + b);
+    DrawRows d;
+    const int rq = Kb + 1 + js;
+    d.Mp = sm.rowM[js];
+    d.invSp = 1.0f / sm.rowS[js];
+    d.Tp = sm.rowT[js];
+    d.resid = js < Kb;
+    d.Mq = d.resid ? sm.rowM[rq] : 0.0f;
+    d.invSq = d.resid ? 1.0f / sm.rowS[rq] : 0.0f;
+    d.Tq = d.resid ? sm.rowT[rq] : 0.0f;
+    const T* pr = prow<T>(P, b, js);
+    const T* qr = d.resid ? qrow<T>(P, b, js) : pr;
+    float* wt = reinterpret_cast<float*>(dyn + (MODE == kTopK ? (size_t)kWarps * kRowCap * sizeof(uint2) : 0));
+    int clamp = 0;
+    float R = draw_row<T, VEC>(P, pr, qr, d, u, wt, sm, &clamp);
+    float resid_mass = d.resid ? R : 0.0f;
+    if (!(R > 0.0f)) {
+      // max(0, p - q) vanished through rounding: draw from p instead
+      d.resid = false;
+      if (t == 0) sm.flags |= SPEC_FLAG_RESIDUAL_ZERO;
+      R = draw_row<T, VEC>(P, pr, pr, d, u, wt, sm, &clamp);
+    }
+    if (clamp) atomicOr(&sm.flags, SPEC_FLAG_CDF_CLAMP);
+    __syncthreads();
+    if (t == 0) {
+      tok[js] = sm.y;
+      if (P.resid_mass) P.resid_mass[b] = resid_mass;
+      if (P.samp_margin) P.samp_margin[b] = sm.margin;
+    }
+  } else if (MODE != kGreedy) {  // non-finite rows: no result
+    if (t <= K) tok[t] = -1;
+    if (t == 0) {
+      sm.jstar = 0;
+      if (P.resid_mass) P.resid_mass[b] = NAN;
+      if (P.samp_margin) P.samp_margin[b] = NAN;
+    }
+  } else {
+    if (sm.nonfinite && t <= K) tok[t] = -1;
+    if (t == 0) {
+      if (sm.nonfinite) sm.jstar = 0;
+      if (P.resid_mass) P.resid_mass[b] = 0.0f;
+      if (P.samp_margin) P.samp_margin[b] = INFINITY;
+    }
+  }
+  __syncthreads();
+  if (t == 0) {
+    P.out_nacc[b] = sm.jstar;
+    if (P.flags) P.flags[b] = sm.flags;
+    P.req_cnt[b] = 0;  // ready for the next call
+  }
+  if (P.lognorm) {
+    const int R = 2 * K + 1;
+    for (int r = t; r < R; r += kThreads) {
+      float v = NAN;
+      if (MODE != kGreedy) {
+        int rr = -1;  // compact row index of padded row r
+        if (r <= K) rr = r <= Kb ? r : -1;
+        else rr = (r - K - 1) < Kb ? Kb + 1 + (r - K - 1) : -1;
+        if (rr >= 0) v = sm.rowM[rr] * P.invT + logf(sm.rowS[rr]);
+      }
+      P.lognorm[(size_t)b * R + r] = v;
+    }
+  }
+  if (MODE == kGreedy && t < K) {
+    if (P.p_draft) P.p_draft[(size_t)b * K + t] = NAN;
+    if (P.q_draft) P.q_draft[(size_t)b * K + t] = NAN;
+    if (P.acc_margin) P.acc_margin[(size_t)b * K + t] = NAN;
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// the kernel
+// ------------------------------------------------------------------------------------------------
+template <typename T, int MODE, bool VEC>
+__global__ void __launch_bounds__(kThreads, 4) verify_kernel(const Params P) {
+  extern __shared__ __align__(16) unsigned char dyn[];
+  __shared__ Smem sm;
+  const int t = threadIdx.x;
+  const uint32_t total = P.rowmap ? __ldg(P.total_rows) * (uint32_t)P.nchunk : P.uniform_items;
+  if (t == 0) sm.item = (int)atomicAdd(&P.sched[0], 1u);
+  __syncthreads();
+  uint32_t item = (uint32_t)sm.item;
+  while (item < total) {
+    uint32_t next = 0;
+    if (t == 0) next = atomicAdd(&P.sched[0], 1u);  // prefetch the next item
+    const uint32_t row = item / (uint32_t)P.nchunk;
+    const int c = (int)(item - row * (uint32_t)P.nchunk);
+    int b, rp;
+    if (P.rowmap) {
+      const uint32_t e = __ldg(P.rowmap + row);
+      b = (int)(e >> 6);
+      rp = (int)(e & 63u);
+    } else {
+      b = (int)(row / (uint32_t)P.R);
+      rp = (int)(row - (uint32_t)b * P.R);
+    }
+    const int v0 = c * kChunk;
+    const int n = min(kChunk, P.V - v0);
+    const T* base = row_ptr<T>(P, b, rp) + v0;
+    const size_t slot = ((size_t)b * P.R + rp) * P.nchunk + c;
+    if (MODE == kSample)
+      item_sample<T, VEC>(P, base, n, P.partial + slot, sm);
+    else if (MODE == kGreedy)
+      item_greedy<T, VEC>(P, base, n, P.partial + slot, sm);
+    else
+      item_topk<T, VEC>(P, base, n, v0, P.cand + slot * kCandCap, P.cmeta + slot, sm,
+                        reinterpret_cast<uint2*>(dyn));
+    __threadfence();
+    __syncthreads();
+    if (t == 0) {
+      const int kb = clamp_k(P, b, nullptr);
+      const uint32_t need = (uint32_t)(MODE == kGreedy ? kb + 1 : 2 * kb + 1) * (uint32_t)P.nchunk;
+      sm.last = atomicAdd(&P.req_cnt[b], 1u) == need - 1;
+      sm.item = (int)next;
+    }
+    __syncthreads();
+    if (sm.last) {
+      __threadfence();
+      finish_request<T, MODE, VEC>(P, b, sm, dyn);
+    }
+    item = (uint32_t)sm.item;
+    __syncthreads();
+  }
+  if (t == 0) {
+    if (atomicAdd(&P.sched[1], 1u) == gridDim.x - 1) {  // the last CTA out resets the scheduler
+      P.sched[0] = 0;
+      P.sched[1] = 0;
+    }
+  }
+}
+
+// Ragged batches: a table of valid rows in request-major order, so no item is spent on padding.
+__global__ void __launch_bounds__(1024) build_rowmap(const int32_t* __restrict__ kpr, int B, int K,
+                                                     int greedy, uint32_t* rowmap,
+                                                     uint32_t* total_rows) {
+  __shared__ uint32_t warp_tot[32];
+  __shared__ uint32_t carry;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  if (t == 0) carry = 0;
+  __syncthreads();
+  for (int b0 = 0; b0 < B; b0 += 1024) {
+    const int b = b0 + t;
+    uint32_t rows = 0;
+    int kb = 0;
+    if (b < B) {
+      kb = kpr[b];
+      kb = kb < 0 ? 0 : (kb > K ? K : kb);
+      rows = greedy ? kb + 1 : 2 * kb + 1;
+    }
+    uint32_t x = rows;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      uint32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    uint32_t off = carry;
+    for (int w = 0; w < warp; ++w) off += warp_tot[w];
+    off += x - rows;
+    for (uint32_t r = 0; r < rows; ++r) {
+      // compact row r of request b -> padded row: p rows 0..kb, then q rows K+1..K+kb
+      const uint32_t rp = r <= (uint32_t)kb ? r : (uint32_t)K + 1 + (r - kb - 1);
+      rowmap[off + r] = ((uint32_t)b << 6) | rp;
+    }
+    __syncthreads();
+    if (t == 1023) carry = off + rows;
+    __syncthreads();
+  }
+  if (t == 0) *total_rows = carry;
+}
+
+// ------------------------------------------------------------------------------------------------
+// host side
+// ------------------------------------------------------------------------------------------------
+struct Layout {
+  size_t sched, req_cnt, partial, cmeta, cand, rowmap, total_rows, bytes;
+  int R, nchunk;
+  uint64_t rows_padded;
+};
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+static bool make_layout(int B, int K, int V, int mode, bool ragged, Layout* L) {
+  L->R = mode == kGreedy ? K + 1 : 2 * K + 1;
+  L->nchunk = (V + kChunk - 1) / kChunk;
+  L->rows_padded = (uint64_t)B * L->R;
+  const uint64_t items = L->rows_padded * (uint64_t)L->nchunk;
+  if (items >= (1ull << 31) || (uint64_t)B >= (1ull << 25)) return false;
+  size_t o = 0;
+  L->sched = o;
+  o = align256(o + 2 * sizeof(uint32_t));
+  L->req_cnt = o;
+  o = align256(o + (size_t)B * sizeof(uint32_t));
+  L->partial = o;
+  o = align256(o + (size_t)items * sizeof(float2));
+  L->cmeta = o;
+  L->cand = o;
+  if (mode == kTopK) {
+    o = align256(o + (size_t)items * sizeof(uint2));
+    L->cand = o;
+    o = align256(o + (size_t)items * kCandCap * sizeof(uint2));
+  }
+  L->rowmap = o;
+  L->total_rows = o;
+  if (ragged) {
+    o = align256(o + (size_t)L->rows_padded * sizeof(uint32_t));
+    L->total_rows = o;
+    o = align256(o + sizeof(uint32_t));
+  }
+  L->bytes = o;
+  return true;
+}
+
+static int mode_of(float temperature, int top_k, int V) {
+  if (temperature == 0.0f) return kGreedy;
+  return (top_k > 0 && top_k < V) ? kTopK : kSample;
+}
+
+static size_t dyn_smem_bytes(int mode, int V) {
+  const int ntile = (V + kTile - 1) / kTile;
+  size_t wt = (size_t)ntile * sizeof(float);
+  if (mode == kGreedy) return 0;
+  if (mode == kTopK) {
+    size_t a = (size_t)kWarps * kRowCap * sizeof(uint2) + wt;
+    size_t b = (size_t)kSurvCap * sizeof(uint2);
+    return a > b ? a : b;
+  }
+  return wt;
+}
+
+template <typename T, int MODE, bool VEC>
+static cudaError_t launch_t(const Params& P, uint32_t items, size_t dsm, cudaStream_t st) {
+  auto kern = verify_kernel<T, MODE, VEC>;
+  if (dsm > 32 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm);
+    if (e != cudaSuccess) return e;
+  }
+  int dev = 0, sms = 0, occ = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, dsm);
+  if (e != cudaSuccess) return e;
+  if (occ < 1) occ = 1;
+  uint32_t grid = (uint32_t)sms * (uint32_t)occ;
+  if (items < grid) grid = items > 0 ? items : 1;
+  kern<<<grid, kThreads, dsm, st>>>(P);
+  return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_mode(int mode, bool vec, const Params& P, uint32_t items, size_t dsm,
+                               cudaStream_t st) {
+  switch (mode) {
+    case kSample:
+      return vec ? launch_t<T, kSample, true>(P, items, dsm, st) : launch_t<T, kSample, false>(P, items, dsm, st);
+    case kTopK:
+      return vec ? launch_t<T, kTopK, true>(P, items, dsm, st) : launch_t<T, kTopK, false>(P, items, dsm, st);
+    default:
+      return vec ? launch_t<T, kGreedy, true>(P, items, dsm, st) : launch_t<T, kGreedy, false>(P, items, dsm, st);
+  }
+}
+
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" {
+
+size_t spec_verify_workspace_bytes(int32_t B, int32_t K_max, int32_t V, spec_dtype_t dtype,
+                                   int32_t top_k) {
+  if (B < 0 || K_max < 0 || V <= 0 || K_max > SPEC_MAX_K || V > SPEC_MAX_V) return 0;
+  if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return 0;
+  if (top_k < 0) return 0;
+  // the largest layout over the three modes, so one workspace serves any temperature
+  Layout a, b;
+  const int heavy = (top_k > 0 && top_k < V) ? kTopK : kSample;
+  if (!make_layout(B, K_max, V, heavy, true, &a) || !make_layout(B, K_max, V, kGreedy, true, &b)) return 0;
+  return a.bytes > b.bytes ? a.bytes : b.bytes;
+}
+
+spec_status_t spec_verify(const void* p_logits, const void* q_logits, const int32_t* draft_tokens,
+                          const int32_t* k_per_row, const float* u_accept, const float* u_resample,
+                          float temperature, int32_t top_k, int32_t* out_tokens,
+                          int32_t* out_num_accepted, const spec_verify_stats_t* out_stats, int32_t B,
+                          int32_t K_max, int32_t V, spec_dtype_t dtype, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  if (B < 0 || K_max < 0 || V <= 0) return SPEC_ERR_INVALID_ARG;
+  if (!(temperature >= 0.0f) || isinf(temperature) || top_k < 0) return SPEC_ERR_INVALID_ARG;
+  if (K_max > SPEC_MAX_K || V > SPEC_MAX_V) return SPEC_ERR_UNSUPPORTED;
+  if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED;
+  const int mode = mode_of(temperature, top_k, V);
+  if (mode == kTopK && top_k > SPEC_MAX_TOPK) return SPEC_ERR_UNSUPPORTED;
+  if (!p_logits || !out_tokens || !out_num_accepted) return SPEC_ERR_INVALID_ARG;
+  if (K_max > 0 && !draft_tokens) return SPEC_ERR_INVALID_ARG;
+  if (mode != kGreedy && (!u_resample || (K_max > 0 && (!q_logits || !u_accept))))
+    return SPEC_ERR_INVALID_ARG;
+  if (B == 0) return SPEC_OK;
+  const bool ragged = k_per_row != nullptr;
+  Layout L;
+  if (!make_layout(B, K_max, V, mode, ragged, &L)) return SPEC_ERR_UNSUPPORTED;
+  if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
+
+  const size_t es = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
+  const bool vec = ((uintptr_t)p_logits % 16 == 0) && (!q_logits || (uintptr_t)q_logits % 16 == 0) &&
+                   ((size_t)V * es % 16 == 0);
+  char* ws = static_cast<char*>(workspace);
+  Params P;
+  P.p = p_logits;
+  P.q = mode == kGreedy ? nullptr : q_logits;
+  P.draft = draft_tokens;
+  P.kpr = k_per_row;
+  P.ua = u_accept;
+  P.ur = u_resample;
+  P.out_tokens = out_tokens;
+  P.out_nacc = out_num_accepted;
+  spec_verify_stats_t st = {};
+  if (out_stats) st = *out_stats;
+  P.p_draft = st.p_draft;
+  P.q_draft = st.q_draft;
+  P.acc_margin = st.accept_margin;
+  P.samp_margin = st.sample_margin;
+  P.resid_mass = st.residual_mass;
+  P.lognorm = st.row_lognorm;
+  P.flags = st.flags;
+  P.B = B;
+  P.K = K_max;
+  P.V = V;
+  P.top_k = top_k;
+  P.nchunk = L.nchunk;
+  P.R = L.R;
+  const double T = temperature;
+  P.c2 = mode == kGreedy ? 0.0f : (float)(1.4426950408889634 / T);
+  P.invT = mode == kGreedy ? 0.0f : (float)(1.0 / T);
+  P.sched = reinterpret_cast<uint32_t*>(ws + L.sched);
+  P.req_cnt = reinterpret_cast<uint32_t*>(ws + L.req_cnt);
+  P.partial = reinterpret_cast<float2*>(ws + L.partial);
+  P.cmeta = reinterpret_cast<uint2*>(ws + L.cmeta);
+  P.cand = reinterpret_cast<uint2*>(ws + L.cand);
+  P.rowmap = ragged ? reinterpret_cast<const uint32_t*>(ws + L.rowmap) : nullptr;
+  P.total_rows = ragged ? reinterpret_cast<const uint32_t*>(ws + L.total_rows) : nullptr;
+  P.uniform_items = (uint32_t)(L.rows_padded * (uint64_t)L.nchunk);
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (ragged) {
+    build_rowmap<<<1, 1024, 0, s>>>(k_per_row, B, K_max, mode == kGreedy,
+                                    reinterpret_cast<uint32_t*>(ws + L.rowmap),
+                                    reinterpret_cast<uint32_t*>(ws + L.total_rows));
+    if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+  }
+  const size_t dsm = dyn_smem_bytes(mode, V);
+  const uint32_t items = P.uniform_items;  // an upper bound on the grid's useful size
+  cudaError_t e = dtype == SPEC_DTYPE_BF16 ? launch_mode<uint16_t>(mode, vec, P, items, dsm, s)
+                                           : launch_mode<float>(mode, vec, P, items, dsm, s);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+size_t spec_verify_host_staging_bytes(int32_t B, int32_t K_max, int32_t V, spec_dtype_t dtype,
+                                      int32_t top_k, int32_t has_k_per_row) {
+  const size_t ws = spec_verify_workspace_bytes(B, K_max, V, dtype, top_k);
+  if (ws == 0) return 0;
+  const size_t es = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
+  size_t o = 0;
+  o = align256(o + (size_t)B * (K_max + 1) * V * es);  // p
+  o = align256(o + (size_t)B * K_max * V * es);        // q
+  o = align256(o + (size_t)B * K_max * 4);             // draft
+  o = align256(o + (size_t)(has_k_per_row ? B : 0) * 4);
+  o = align256(o + (size_t)B * K_max * 4);  // ua
+  o = align256(o + (size_t)B * 4);          // ur
+  o = align256(o + (size_t)B * (K_max + 1) * 4);  // tokens
+  o = align256(o + (size_t)B * 4);                // n_acc
+  return o + ws;
+}
+
+spec_status_t spec_verify_host(const void* p_logits, const void* q_logits,
+                               const int32_t* draft_tokens, const int32_t* k_per_row,
+                               const float* u_accept, const float* u_resample, float temperature,
+                               int32_t top_k, int32_t* out_tokens, int32_t* out_num_accepted,
+                               int32_t B, int32_t K_max, int32_t V, spec_dtype_t dtype,
+                               void* staging, size_t staging_bytes, void* stream) {
+  if (B < 0 || K_max < 0 || V <= 0 || K_max > SPEC_MAX_K || V > SPEC_MAX_V) return SPEC_ERR_INVALID_ARG;
+  if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED;
+  const size_t need = spec_verify_host_staging_bytes(B, K_max, V, dtype, top_k, k_per_row != nullptr);
+  if (need == 0) return SPEC_ERR_INVALID_ARG;
+  if (!staging || ((uintptr_t)staging & 255u) || staging_bytes < need) return SPEC_ERR_WORKSPACE;
+  if (!p_logits || !out_tokens || !out_num_accepted) return SPEC_ERR_INVALID_ARG;
+  if (B == 0) return SPEC_OK;
+  const bool greedy = temperature == 0.0f;
+  const size_t es = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
+  char* d = static_cast<char*>(staging);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    char* p = d + o;
+    o = align256(o + bytes);
+    return p;
+  };
+  const size_t np = (size_t)B * (K_max + 1) * V * es, nq = (size_t)B * K_max * V * es;
+  char* dp = take(np);
+  char* dq = take(nq);
+  char* dx = take((size_t)B * K_max * 4);
+  char* dk = take((size_t)(k_per_row ? B : 0) * 4);
+  char* dua = take((size_t)B * K_max * 4);
+  char* dur = take((size_t)B * 4);
+  char* dtok = take((size_t)B * (K_max + 1) * 4);
+  char* dn = take((size_t)B * 4);
+  char* dws = d + o;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(dp, p_logits, np, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && !greedy && q_logits && nq) e = cudaMemcpyAsync(dq, q_logits, nq, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && draft_tokens && K_max) e = cudaMemcpyAsync(dx, draft_tokens, (size_t)B * K_max * 4, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && k_per_row) e = cudaMemcpyAsync(dk, k_per_row, (size_t)B * 4, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && !greedy && u_accept && K_max) e = cudaMemcpyAsync(dua, u_accept, (size_t)B * K_max * 4, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && !greedy && u_resample) e = cudaMemcpyAsync(dur, u_resample, (size_t)B * 4, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return SPEC_ERR_CUDA;
+  spec_status_t r = spec_verify(dp, greedy ? nullptr : (q_logits ? dq : nullptr), draft_tokens ? (const int32_t*)dx : nullptr,
+                                k_per_row ? (const int32_t*)dk : nullptr, greedy ? nullptr : (u_accept ? (const float*)dua : nullptr),
+                                greedy ? nullptr : (u_resample ? (const float*)dur : nullptr), temperature, top_k,
+                                (int32_t*)dtok, (int32_t*)dn, nullptr, B, K_max, V, dtype, dws,
+                                staging_bytes - (size_t)(dws - d), stream);
+  if (r != SPEC_OK) return r;
+  e = cudaMemcpyAsync(out_tokens, dtok, (size_t)B * (K_max + 1) * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(out_num_accepted, dn, (size_t)B * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+const char* spec_verify_status_string(spec_status_t status) {
+  switch (status) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_INVALID_ARG: return "invalid argument";
+    case SPEC_ERR_UNSUPPORTED: return "unsupported size, dtype or option";
+    case SPEC_ERR_CUDA: return "CUDA runtime error";
+    case SPEC_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case SPEC_ERR_TIMEOUT: return "timeout";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,216 @@
+"""GPU parity: the CUDA verify step against the fp64 oracle on the same seeded inputs.
+
+Each of the five workloads is checked at a size the oracle finishes in seconds (full vocabulary,
+several chunks, ragged tails) and at its full size (the launch configuration the benchmark times),
+where the oracle runs on every request with all host cores.  Edge cases: empty batch, bonus-only
+requests, unaligned vocabularies and pointers, tiny vocabularies, NaN / -inf rows, bad tokens and
+bad k_per_row, top-k ties and the exact top-k path, p == q, extreme uniforms, workspace reuse,
+streams and the host-buffer entry point.
+"""
+import numpy as np
+import pytest
+
+import workloads as W
+from _parity import compare, run_gpu, run_oracle, to_dev
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def _check(d, **kw):
+    g = run_gpu(d, **kw)
+    o = run_oracle(d)
+    w = d["workload"]
+    res = compare(g, o, w.K, d["k_per_row"])
+    assert res["low_margin"] <= max(2, res["requests"] // 100), res
+    return res, g, o
+
+
+# ------------------------------------------------------------------------------------------------
+# the five workloads, small
+# ------------------------------------------------------------------------------------------------
+SMALL = [("c1", {}), ("c2", {}), ("c3", dict(B=8)), ("c4", dict(B=8)), ("c5_a0.4", dict(B=16)),
+         ("c5_a0.6", dict(B=16)), ("c5_a0.8", dict(B=16)), ("c5_a0.9", dict(B=16)), ("c5_greedy", dict(B=32))]
+
+
+@pytest.mark.parametrize("name,over", SMALL, ids=[s[0] for s in SMALL])
+def test_workload_small(name, over):
+    d = W.generate(W.get(name, **over))
+    _check(d)
+
+
+# ------------------------------------------------------------------------------------------------
+# full sizes (every request compared)
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("name", ["c3", "c4", "c5_a0.8", "c5_greedy"])
+def test_workload_full(name):
+    d = W.generate(W.get(name))
+    res, g, o = _check(d)
+    print(name, res)
+
+
+def test_alpha_sweep_mean_emitted():
+    """Mean emitted tokens per request near the closed form sum_n prod alpha (loose, statistical)."""
+    for name in ("c5_a0.4", "c5_a0.9"):
+        w = W.get(name, B=256)
+        d = W.generate(w)
+        g = run_gpu(d, stats=False)
+        m = (g["n_acc"] + 1).mean()
+        a = w.alpha
+        e = (1 - a ** (w.K + 1)) / (1 - a)
+        assert abs(m - e) < 0.25 * e, (name, m, e)
+
+
+# ------------------------------------------------------------------------------------------------
+# edge cases
+# ------------------------------------------------------------------------------------------------
+def _gen(name="c2", **over):
+    return W.generate(W.get(name, **over))
+
+
+def test_empty_batch():
+    import speculative_decoding_rejection_verify_gb300 as sv
+    dev = torch.device("cuda:0")
+    p = torch.zeros((0, 5, 100), device=dev)
+    tok, n, _ = sv.verify(p, torch.zeros((0, 4, 100), device=dev), torch.zeros((0, 4), dtype=torch.int32, device=dev),
+                          None, torch.zeros((0, 4), device=dev), torch.zeros((0,), device=dev), 1.0, 0)
+    assert tok.shape == (0, 5) and n.shape == (0,)
+
+
+def test_ragged_with_bonus_only_requests():
+    w = W.get("c3", B=12, V=50000, ragged=(0, 6), tau=1.0)
+    d = W.generate(w)
+    d["k_per_row"][:3] = 0
+    d["k_per_row"][3] = 6
+    _check(d, k_per_row=d["k_per_row"])
+
+
+@pytest.mark.parametrize("V,dtype", [(1001, "bf16"), (1003, "f32"), (7, "f32"), (1, "bf16"), (8200, "bf16"),
+                                     (8192 * 3 + 5, "f32")])
+def test_odd_vocabularies(V, dtype):
+    d = _gen("c2", B=5, V=V, dtype=dtype, tau=0.7)
+    _check(d)
+
+
+def test_unaligned_pointers():
+    d = _gen("c2", B=3, V=4096, tau=0.7)
+    dev = torch.device("cuda:0")
+    import speculative_decoding_rejection_verify_gb300 as sv
+    p = to_dev(d["p"], dev)
+    q = to_dev(d["q"], dev)
+    # shift both logit buffers by one element inside a larger allocation
+    pbig = torch.empty(p.numel() + 1, dtype=p.dtype, device=dev)
+    qbig = torch.empty(q.numel() + 1, dtype=q.dtype, device=dev)
+    pbig[1:].copy_(p.flatten())
+    qbig[1:].copy_(q.flatten())
+    tok, n, st = sv.verify(pbig[1:].view(p.shape), qbig[1:].view(q.shape), to_dev(d["draft"], dev), None,
+                           to_dev(d["ua"], dev), to_dev(d["ur"], dev), d["temperature"], 0, stats=True)
+    torch.cuda.synchronize()
+    g = dict(tokens=tok.cpu().numpy(), n_acc=n.cpu().numpy(), **{k: v.cpu().numpy() for k, v in st.items()})
+    compare(g, run_oracle(d), d["workload"].K)
+
+
+def test_nonfinite_rows_flagged():
+    d = _gen("c2", B=6, V=3000, dtype="f32", tau=0.7)
+    d["p"][0, 1, 17] = np.nan
+    d["q"][1, 0, 5] = np.inf
+    d["p"][2, :, :] = -np.inf
+    d["q"][3, 2, :100] = -np.inf  # -inf entries are allowed
+    d["p"][4, 0, :] = np.nan
+    g, o = run_gpu(d), run_oracle(d)
+    assert o["flags"][0] & 16 and o["flags"][1] & 16 and o["flags"][2] & 16 and o["flags"][4] & 16
+    assert not o["flags"][3] & 16
+    compare(g, o, d["workload"].K)
+
+
+def test_bad_tokens_and_bad_k():
+    w = W.get("c2", B=6, V=3000, tau=0.7, ragged=(1, 5))
+    d = W.generate(w)
+    d["draft"][0, 0] = -1
+    d["draft"][1, 2] = 3000
+    d["ua"][1, :2] = 0.0  # make sure the first two are accepted so position 2 is examined
+    d["k_per_row"][2] = -3
+    d["k_per_row"][3] = 9
+    g, o = run_gpu(d, k_per_row=d["k_per_row"]), run_oracle(d, k_per_row=d["k_per_row"])
+    assert o["flags"][0] & 4 and o["flags"][2] & 8 and o["flags"][3] & 8
+    compare(g, o, w.K, np.clip(d["k_per_row"], 0, w.K))
+
+
+def test_topk_variants():
+    # k = 1, k >= V (off), bf16 logits with many ties, and a small vocabulary (exact top-k path)
+    for over in (dict(top_k=1), dict(top_k=200000), dict(dtype="bf16", top_k=50), dict(V=900, top_k=50),
+                 dict(top_k=256, B=4), dict(V=20000, top_k=7, temperature=1.3)):
+        base = dict(B=6, V=40000, tau=0.6)
+        base.update(over)
+        d = W.generate(W.get("c4", **base))
+        if over.get("dtype") == "bf16":
+            for key in ("p", "q"):  # coarse logits: many exact ties around the k-th largest
+                f = W.bf16_bits_to_f32(d[key])
+                d[key] = W.to_bf16_bits(np.round(f * 2) / 2)
+        _check(d)
+
+
+def test_p_equals_q_accepts_everything():
+    d = _gen("c2", B=8, V=5000, tau=0.0)
+    d["p"][:, : d["q"].shape[1]] = d["q"]
+    g = run_gpu(d)
+    assert (g["n_acc"] == d["workload"].K).all()
+    compare(g, run_oracle(d), d["workload"].K)
+
+
+def test_extreme_uniforms():
+    d = _gen("c2", B=8, V=5000, tau=0.7)
+    d["ua"][:4] = 0.0
+    d["ua"][4:] = np.float32(1 - 2 ** -24)
+    d["ur"][::2] = 0.0
+    d["ur"][1::2] = np.float32(1 - 2 ** -24)
+    _check(d)
+
+
+def test_workspace_reuse_and_determinism():
+    d = _gen("c3", B=16, tau=1.0)
+    a = run_gpu(d)
+    b = run_gpu(d)
+    for k in a:
+        np.testing.assert_array_equal(a[k], b[k])
+
+
+def test_side_stream():
+    d = _gen("c2", B=8)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g = run_gpu(d, stream=s)
+    compare(g, run_oracle(d), d["workload"].K)
+
+
+def test_greedy_without_q():
+    d = _gen("c5_greedy", B=8, V=6000)
+    g = run_gpu(d)  # run_gpu passes q=None at temperature 0
+    compare(g, run_oracle(d), d["workload"].K)
+
+
+def test_host_entry_point_matches_device():
+    import speculative_decoding_rejection_verify_gb300 as sv
+    for name, over in (("c2", {}), ("c4", dict(B=4)), ("c5_greedy", dict(B=8))):
+        d = _gen(name, **over)
+        w = d["workload"]
+        kpr = d["k_per_row"] if w.ragged else None
+        greedy = w.temperature == 0
+        tok, n = sv.verify_host(d["p"], None if greedy else d["q"], d["draft"], kpr, None if greedy else d["ua"],
+                                None if greedy else d["ur"], w.temperature, w.top_k)
+        g = run_gpu(d, stats=False)
+        np.testing.assert_array_equal(tok, g["tokens"])
+        np.testing.assert_array_equal(n, g["n_acc"])
+
+
+def test_errors_are_reported():
+    import speculative_decoding_rejection_verify_gb300 as sv
+    d = _gen("c2", B=2, V=1000)
+    dev = torch.device("cuda:0")
+    with pytest.raises(sv.SpecVerifyError):
+        sv.verify(to_dev(d["p"], dev), to_dev(d["q"], dev), to_dev(d["draft"], dev), None, to_dev(d["ua"], dev),
+                  to_dev(d["ur"], dev), -1.0, 0)
+    with pytest.raises(sv.SpecVerifyError):
+        sv.verify(to_dev(d["p"], dev), to_dev(d["q"], dev), to_dev(d["draft"], dev), None, to_dev(d["ua"], dev),
+                  to_dev(d["ur"], dev), 1.0, 300)  # top-k above the supported bound
