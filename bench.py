@@ -342,7 +342,7 @@ def run_gpu(args, w: W.Workload):
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": traffic_for(w.key if not w.greedy else "c5_greedy"),
                      "kernel": "verify_kernel", "per_launch_ms": per_launch_ms},
-        "gpu_launches": args.steps * (2 if ragged else 1),
+        "gpu_launches": args.steps * (3 if ragged else 2),
         "clocks": clk.summary(),
     }
     if e2e is not None:
@@ -363,6 +363,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="c5_a0.8", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--batch", type=int, default=0, help="override B (profiling a smaller case)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-requests", type=int, default=1024)
@@ -373,6 +374,8 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = W.get(args.workload)
+    if args.batch:
+        w = w.with_(B=args.batch)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_gpu(args, w)

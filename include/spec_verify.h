@@ -85,10 +85,10 @@ typedef struct {
 } spec_verify_stats_t;
 
 /*
- * Bytes of device workspace spec_verify needs for these sizes (0 is never returned for valid
- * sizes; returns 0 for invalid ones).  The workspace must be zero-filled before its first use and
- * must not be written by the caller between calls: every call leaves its counters at zero again.
- * One workspace must not be used by two calls that may run at the same time.
+ * Bytes of device workspace spec_verify needs for these sizes, for any temperature (0 for invalid
+ * sizes).  The workspace holds per-call scratch only (per-chunk summaries, top-k candidates, the
+ * ragged row table): it needs no initialisation and keeps nothing between calls, but one
+ * workspace must not be used by two calls that may run at the same time.
  */
 size_t spec_verify_workspace_bytes(int32_t B, int32_t K_max, int32_t V, spec_dtype_t dtype,
                                    int32_t top_k);
@@ -110,7 +110,9 @@ size_t spec_verify_workspace_bytes(int32_t B, int32_t K_max, int32_t V, spec_dty
  *   out_num_accepted [B] int32: n = accepted drafts, in [0, K_b];
  *   out_stats     host struct of device pointers, or NULL;
  *   workspace     device memory of at least spec_verify_workspace_bytes(...) bytes, 256-B aligned.
- * Launches one kernel.  Returns SPEC_OK once the work is enqueued.
+ * Launches two kernels (three with k_per_row): a streaming pass over every valid logit row that
+ * leaves per-chunk summaries in the workspace, then one block per request for the decision and
+ * the draw.  Returns SPEC_OK once the work is enqueued.
  */
 spec_status_t spec_verify(const void* p_logits, const void* q_logits, const int32_t* draft_tokens,
                           const int32_t* k_per_row, const float* u_accept, const float* u_resample,
@@ -128,8 +130,8 @@ size_t spec_verify_host_staging_bytes(int32_t B, int32_t K_max, int32_t V, spec_
 
 /*
  * The same step on HOST buffers: copies the inputs into `staging` (device memory of at least
- * spec_verify_host_staging_bytes(...) bytes, zero-filled before its first use and otherwise
- * owned by this function between calls), runs spec_verify there, copies out_tokens and
+ * spec_verify_host_staging_bytes(...) bytes, no initialisation needed), runs spec_verify there,
+ * copies out_tokens and
  * out_num_accepted back, and synchronises `stream` before returning.  Host pointers follow the
  * layouts of spec_verify; q_logits / u_accept / u_resample may be NULL iff temperature == 0 and
  * k_per_row may be NULL.  Pinned (page-locked) host memory makes the copies asynchronous DMA.

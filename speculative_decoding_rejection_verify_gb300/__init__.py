@@ -114,7 +114,7 @@ def workspace_bytes(B: int, K: int, V: int, dtype: int, top_k: int = 0) -> int:
     return n
 
 
-# Workspaces are cached per (device, stream): the kernel leaves them zeroed for the next call.
+# Workspaces (per-call scratch) are cached per (device, stream) so repeated calls allocate nothing.
 _ws_cache: Dict[Tuple[int, int], object] = {}
 
 

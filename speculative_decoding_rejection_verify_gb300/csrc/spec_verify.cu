@@ -31,8 +31,8 @@ namespace sv {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kChunk = 8192;             // logits per work item
-constexpr int kPer = kChunk / kThreads;  // logits per thread per item
+constexpr int kChunkBytes = 16384;      // bytes of logits per work item (16 B per thread x 4)
+constexpr int kStages = 4;               // work items in flight per CTA (cp.async ring)
 constexpr int kTile = 256;               // inverse-CDF tile: 32 lanes x 8 logits
 constexpr int kCandCap = 256;            // top-k candidates stored per chunk
 constexpr int kSurvCap = 1024;           // survivors examined per chunk
@@ -41,6 +41,15 @@ constexpr int kMaxRows = 2 * SPEC_MAX_K + 1;
 constexpr int kUnrollA = 4;              // tiles in flight per warp in the CDF passes
 
 enum Mode { kSample = 0, kTopK = 1, kGreedy = 2 };
+
+// Per-dtype chunking: every item is 16 KB of logits, 4 x 16-byte vectors per thread.
+template <typename T>
+struct Cfg {
+  static constexpr int CH = kChunkBytes / (int)sizeof(T);  // logits per item
+  static constexpr int PER = CH / kThreads;                 // logits per thread
+  static constexpr int VW = 16 / (int)sizeof(T);            // logits per 16-byte vector
+  static constexpr int LOADS = PER / VW;                    // vectors per thread
+};
 
 // Per-chunk top-k metadata word: count | flags.
 constexpr uint32_t kMetaOverflow = 1u << 30;
@@ -66,9 +75,7 @@ struct Params {
   int B, K, V, top_k, nchunk, R;  // R = padded rows per request (2K+1, or K+1 in greedy)
   float c2;                       // log2(e) / T
   float invT;                     // 1 / T
-  uint32_t* sched;                // [0] next item, [1] finished CTAs
-  uint32_t* req_cnt;              // [B] items completed per request
-  float2* partial;                // [B, R, nchunk]
+  float2* partial;                // [B, R, nchunk, warps] (max, sum) or (max, argmax) per warp
   uint2* cmeta;                   // [B, R, nchunk] top-k: (k-th largest key of the chunk, count|flags)
   uint2* cand;                    // [B, R, nchunk, kCandCap] top-k: (key, token)
   const uint32_t* rowmap;         // ragged: [rows] (b << 6 | padded row); null = uniform layout
@@ -100,6 +107,14 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   return r;
 }
 
+// 2^x on the SFU (ex2.approx.ftz: relative error ~2^-22; results below 2^-126 flush to 0, which
+// is far below what a sum of at most 2^21 terms, each relative to the row maximum, can resolve)
+__device__ __forceinline__ float ex2(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // Total order on floats as unsigned keys (-0 is folded into +0; NaN handled by callers).
 __device__ __forceinline__ uint32_t fkey(float f) {
   uint32_t u = __float_as_uint(f + 0.0f);
@@ -113,8 +128,8 @@ __device__ __forceinline__ float keyf(uint32_t k) {
 // Merge two (max, sum of exp2((z - max) * c2)) pairs.  A pair with sum 0 carries no mass.
 __device__ __forceinline__ void lse_merge(float& m, float& s, float mo, float so, float c2) {
   float mn = fmaxf(m, mo);
-  float a = (s == 0.0f) ? 0.0f : s * exp2f((m - mn) * c2);
-  float b = (so == 0.0f) ? 0.0f : so * exp2f((mo - mn) * c2);
+  float a = (s == 0.0f) ? 0.0f : s * ex2((m - mn) * c2);
+  float b = (so == 0.0f) ? 0.0f : so * ex2((mo - mn) * c2);
   m = mn;
   s = a + b;
 }
@@ -179,52 +194,74 @@ __device__ __forceinline__ int clamp_k(const Params& P, int b, int* bad) {
 template <typename T, bool VEC>
 __device__ __forceinline__ int elem_of(int i, int t) {
   if (VEC) {
-    constexpr int VW = 16 / sizeof(T);
+    constexpr int VW = Cfg<T>::VW;
     return ((i / VW) * kThreads + t) * VW + (i % VW);
   }
   return i * kThreads + t;
 }
 
-// Loads logits [0, n) of the chunk starting at `base`; invalid slots get -inf.
+// Unpacks the thread's 16-byte vectors of a chunk into floats; vectors at or past n read -inf.
+template <typename T>
+__device__ __forceinline__ void unpack(const uint4 (&raw)[Cfg<T>::LOADS], int n, float (&v)[Cfg<T>::PER]) {
+  constexpr int VW = Cfg<T>::VW;
+  const int t = threadIdx.x;
+#pragma unroll
+  for (int l = 0; l < Cfg<T>::LOADS; ++l) {
+    const uint32_t w[4] = {raw[l].x, raw[l].y, raw[l].z, raw[l].w};
+    const bool ok = (l * kThreads + t) * VW < n;
+    if (sizeof(T) == 2) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        v[l * 8 + 2 * k] = ok ? bf16_lo(w[k]) : -INFINITY;
+        v[l * 8 + 2 * k + 1] = ok ? bf16_hi(w[k]) : -INFINITY;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[l * 4 + k] = ok ? __uint_as_float(w[k]) : -INFINITY;
+    }
+  }
+}
+
+// Loads logits [0, n) of the chunk at `base` straight from global memory (any alignment).
 template <typename T, bool VEC>
-__device__ __forceinline__ void load_chunk(const T* __restrict__ base, int n, float (&v)[kPer]) {
+__device__ __forceinline__ void load_chunk(const T* __restrict__ base, int n, float (&v)[Cfg<T>::PER]) {
   const int t = threadIdx.x;
   if (VEC) {
-    constexpr int VW = 16 / sizeof(T);
-    constexpr int L = kPer / VW;
-    uint4 raw[L];
+    constexpr int VW = Cfg<T>::VW;
+    uint4 raw[Cfg<T>::LOADS];
 #pragma unroll
-    for (int l = 0; l < L; ++l) {
-      int e0 = (l * kThreads + t) * VW;
-      if (e0 < n)
-        raw[l] = ldg_stream(base + e0);
-      else
-        raw[l] = make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+    for (int l = 0; l < Cfg<T>::LOADS; ++l) {
+      const int e0 = (l * kThreads + t) * VW;
+      raw[l] = e0 < n ? ldg_stream(base + e0) : make_uint4(0u, 0u, 0u, 0u);
     }
-#pragma unroll
-    for (int l = 0; l < L; ++l) {
-      const uint32_t w[4] = {raw[l].x, raw[l].y, raw[l].z, raw[l].w};
-      int e0 = (l * kThreads + t) * VW;
-      bool ok = e0 < n;
-      if (sizeof(T) == 2) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          v[l * 8 + 2 * k] = ok ? bf16_lo(w[k]) : -INFINITY;
-          v[l * 8 + 2 * k + 1] = ok ? bf16_hi(w[k]) : -INFINITY;
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) v[l * 4 + k] = __uint_as_float(w[k]);
-      }
-    }
+    unpack<T>(raw, n, v);
   } else {
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      int e = i * kThreads + t;
+    for (int i = 0; i < Cfg<T>::PER; ++i) {
+      const int e = i * kThreads + t;
       v[i] = e < n ? load1<T>(base + e) : -INFINITY;
     }
   }
 }
+
+// The thread's vectors of a chunk staged in shared memory by issue_chunk().
+template <typename T>
+__device__ __forceinline__ void load_stage(const uint4* stage, int n, float (&v)[Cfg<T>::PER]) {
+  uint4 raw[Cfg<T>::LOADS];
+#pragma unroll
+  for (int l = 0; l < Cfg<T>::LOADS; ++l) raw[l] = stage[l * kThreads + threadIdx.x];
+  unpack<T>(raw, n, v);
+}
+
+// cp.async ring: each thread copies its own 16-byte vectors of a chunk into a stage and later
+// reads exactly those bytes back, so only its own wait_group orders the copy and the read.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(gmem), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // ------------------------------------------------------------------------------------------------
 // shared memory
@@ -232,6 +269,7 @@ __device__ __forceinline__ void load_chunk(const T* __restrict__ base, int n, fl
 struct Smem {
   int item;
   int last;
+  int req;
   float red_m[kWarps];
   float red_s[kWarps];
   int red_i[kWarps];
@@ -257,47 +295,36 @@ struct Smem {
 // ------------------------------------------------------------------------------------------------
 // per-item work
 // ------------------------------------------------------------------------------------------------
-template <typename T, bool VEC>
-__device__ void item_sample(const Params& P, const T* base, int n, float2* out, Smem& sm) {
-  float v[kPer];
-  load_chunk<T, VEC>(base, n, v);
+// Sampling: each warp summarises its share of the chunk as (max, sum of 2^((z - max) * c2)) and
+// writes it to out[warp]; the request's tail merges the warps' and chunks' pairs per row.
+template <typename T>
+__device__ __forceinline__ void item_sample(const Params& P, const float (&v)[Cfg<T>::PER], float2* out) {
   float m = -INFINITY;
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) m = fmax_nan(m, v[i]);
+  for (int i = 0; i < Cfg<T>::PER; ++i) m = fmax_nan(m, v[i]);
   float s = 0.0f;
   if (m != -INFINITY) {
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) s += exp2f((v[i] - m) * P.c2);
+    for (int i = 0; i < Cfg<T>::PER; ++i) s += ex2((v[i] - m) * P.c2);
   }
   lse_warp(m, s, P.c2);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) {
-    sm.red_m[warp] = m;
-    sm.red_s[warp] = s;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    m = lane < kWarps ? sm.red_m[lane] : -INFINITY;
-    s = lane < kWarps ? sm.red_s[lane] : 0.0f;
-    lse_warp(m, s, P.c2);
-    if (lane == 0) *out = make_float2(m, s);
-  }
+  if ((threadIdx.x & 31) == 0) out[threadIdx.x >> 5] = make_float2(m, s);
 }
 
+// Greedy: each warp writes its (max, lowest token id at the max) to out[warp]; a NaN anywhere in
+// the warp's share is marked by the id -1.
 template <typename T, bool VEC>
-__device__ void item_greedy(const Params& P, const T* base, int n, float2* out, Smem& sm) {
-  float v[kPer];
-  load_chunk<T, VEC>(base, n, v);
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+__device__ __forceinline__ void item_greedy(const float (&v)[Cfg<T>::PER], int n, int v0, float2* out) {
+  const int t = threadIdx.x;
   float best = -INFINITY;
   int bi = 0x7FFFFFFF;
   bool nan = false;
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    int e = elem_of<T, VEC>(i, t);
+  for (int i = 0; i < Cfg<T>::PER; ++i) {
+    const int e = elem_of<T, VEC>(i, t);
     if (e < n) {
       nan |= v[i] != v[i];
-      amax_merge(best, bi, v[i], e);
+      amax_merge(best, bi, v[i], v0 + e);
     }
   }
 #pragma unroll
@@ -306,23 +333,8 @@ __device__ void item_greedy(const Params& P, const T* base, int n, float2* out, 
     int io = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
     amax_merge(best, bi, vo, io);
   }
-  bool anynan = __syncthreads_or(nan);
-  if (lane == 0) {
-    sm.red_m[warp] = best;
-    sm.red_i[warp] = bi;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    best = lane < kWarps ? sm.red_m[lane] : -INFINITY;
-    bi = lane < kWarps ? sm.red_i[lane] : 0x7FFFFFFF;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      float vo = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-      int io = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-      amax_merge(best, bi, vo, io);
-    }
-    if (lane == 0) *out = make_float2(best, __int_as_float(anynan ? -1 : bi));
-  }
+  nan = __any_sync(0xFFFFFFFFu, nan);
+  if ((t & 31) == 0) out[t >> 5] = make_float2(best, __int_as_float(nan ? -1 : bi));
 }
 
 // Descending bitonic sort of one key per lane across a warp.
@@ -346,17 +358,15 @@ __device__ __forceinline__ uint32_t warp_sort_desc(uint32_t x) {
 // (key, token) pairs plus a meta word (count | overflow | NaN) and the chunk's k-th largest key
 // (0 when the chunk holds fewer than k logits).
 template <typename T, bool VEC>
-__device__ void item_topk(const Params& P, const T* base, int n, int v0, uint2* cand, uint2* meta,
-                          Smem& sm, uint2* surv) {
-  float v[kPer];
-  load_chunk<T, VEC>(base, n, v);
+__device__ void item_topk(const Params& P, const float (&v)[Cfg<T>::PER], int n, int v0, uint2* cand,
+                          uint2* meta, Smem& sm, uint2* surv) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int k = P.top_k;
-  uint32_t key[kPer];
+  uint32_t key[Cfg<T>::PER];
   uint32_t tmax = 0;
   bool nan = false;
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) {
+  for (int i = 0; i < Cfg<T>::PER; ++i) {
     int e = elem_of<T, VEC>(i, t);
     bool ok = e < n && v[i] == v[i];
     nan |= (e < n) && (v[i] != v[i]);
@@ -393,7 +403,7 @@ __device__ void item_topk(const Params& P, const T* base, int n, int v0, uint2* 
   if (kp > 32 || certified < k) theta = 1u;  // no usable bound: every logit survives
   // survivors -> shared buffer
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) {
+  for (int i = 0; i < Cfg<T>::PER; ++i) {
     bool s = key[i] >= theta && key[i] != 0u;
     unsigned bal = __ballot_sync(0xFFFFFFFFu, s);
     if (bal) {
@@ -502,25 +512,29 @@ __device__ __forceinline__ void weights8(const T* pr, const T* qr, int e0, int V
     load8<T, VEC>(qr, e0, V, zq);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      float a = zp[k] >= d.Tp ? __fmul_rn(exp2f(__fmul_rn(__fsub_rn(zp[k], d.Mp), c2)), d.invSp) : 0.0f;
-      float b = zq[k] >= d.Tq ? __fmul_rn(exp2f(__fmul_rn(__fsub_rn(zq[k], d.Mq), c2)), d.invSq) : 0.0f;
+      float a = zp[k] >= d.Tp ? __fmul_rn(ex2(__fmul_rn(__fsub_rn(zp[k], d.Mp), c2)), d.invSp) : 0.0f;
+      float b = zq[k] >= d.Tq ? __fmul_rn(ex2(__fmul_rn(__fsub_rn(zq[k], d.Mq), c2)), d.invSq) : 0.0f;
       w[k] = fmaxf(__fsub_rn(a, b), 0.0f);
     }
   } else {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) w[k] = zp[k] >= d.Tp ? exp2f(__fmul_rn(__fsub_rn(zp[k], d.Mp), c2)) : 0.0f;
+    for (int k = 0; k < 8; ++k) w[k] = zp[k] >= d.Tp ? ex2(__fmul_rn(__fsub_rn(zp[k], d.Mp), c2)) : 0.0f;
   }
 }
 
-// Inverse-CDF draw over a whole row: y = the smallest v with u * R < C_v, C_v cumulative in
-// ascending token id, computed hierarchically (8 logits per lane, 256 per warp tile, tiles by
-// segments per thread).  Returns R; sets sm.y, sm.margin and the clamp flag.
+// Inverse-CDF draw over the logits [v0, vend) of a row: y = the smallest v with target < C_v,
+// C_v cumulative in ascending token id, computed hierarchically (8 logits per lane, 256 per warp
+// tile, tiles by segments per thread).  With `full`, the range is the whole row and
+// target = u * (its total), which is also the margin scale; otherwise `target` is the mass the
+// draw must pass inside the range and `Rm` the margin scale.  Returns the range total; sets
+// sm.y, sm.margin and the clamp flag.
 template <typename T, bool VEC>
-__device__ float draw_row(const Params& P, const T* pr, const T* qr, const DrawRows& d, float u,
-                          float* wt, Smem& sm, int* clamp) {
+__device__ float draw_range(const Params& P, const T* pr, const T* qr, const DrawRows& d, int v0,
+                            int vend, bool full, float u, float target_in, float Rm, float* wt,
+                            Smem& sm, int* clamp) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int V = P.V;
-  const int ntile = (V + kTile - 1) / kTile;
+  const int V = vend;
+  const int ntile = (vend - v0 + kTile - 1) / kTile;
   // pass A: tile sums
   for (int i0 = warp; i0 < ntile; i0 += kWarps * kUnrollA) {
     float w[kUnrollA][8];
@@ -528,7 +542,7 @@ __device__ float draw_row(const Params& P, const T* pr, const T* qr, const DrawR
     for (int u4 = 0; u4 < kUnrollA; ++u4) {
       int i = i0 + u4 * kWarps;
       if (i < ntile)
-        weights8<T, VEC>(pr, qr, i * kTile + lane * 8, V, d, P.c2, w[u4]);
+        weights8<T, VEC>(pr, qr, v0 + i * kTile + lane * 8, V, d, P.c2, w[u4]);
       else
 #pragma unroll
         for (int k = 0; k < 8; ++k) w[u4][k] = 0.0f;
@@ -564,9 +578,10 @@ __device__ float draw_row(const Params& P, const T* pr, const T* qr, const DrawR
   sm.incl[t] = incl;
   if (t == kThreads - 1) sm.total = incl;
   __syncthreads();
-  const float R = sm.total;
-  if (!(R > 0.0f)) return R;  // caller handles an empty residual
-  const float target = u * R;
+  const float total = sm.total;
+  if (!(total > 0.0f)) return total;  // caller handles an empty residual
+  const float R = full ? total : Rm;
+  const float target = full ? u * total : target_in;
   if (target < incl) atomicMin(&sm.seg_first, t);
   if (t == 0) sm.found = 0;
   __syncthreads();
@@ -611,7 +626,7 @@ __device__ float draw_row(const Params& P, const T* pr, const T* qr, const DrawR
     const float tbase = sm.tile_base;
     bool clamped = sm.found == 2;
     float w[8];
-    weights8<T, VEC>(pr, qr, tile * kTile + lane * 8, V, d, P.c2, w);
+    weights8<T, VEC>(pr, qr, v0 + tile * kTile + lane * 8, V, d, P.c2, w);
     float ls = 0.0f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) ls += w[k];
@@ -663,13 +678,13 @@ __device__ float draw_row(const Params& P, const T* pr, const T* qr, const DrawR
       clamped = true;
     }
     if (lane == yl) {
-      sm.y = tile * kTile + yl * 8 + ye;
+      sm.y = v0 + tile * kTile + yl * 8 + ye;
       sm.margin = clamped ? 0.0f : margin;
       if (clamped) *clamp = 1;
     }
   }
   __syncthreads();
-  return R;
+  return total;
 }
 
 // Row threshold, max and sum for top-k from the chunks' candidates.  One warp per row.
@@ -735,7 +750,7 @@ __device__ bool topk_row_fast(const Params& P, int b, int rp, uint2* buf, float&
   int kept = 0;
   for (int i = lane; i < n; i += 32) {
     if (buf[i].x >= kth) {
-      s += exp2f((keyf(buf[i].x) - M) * P.c2);
+      s += ex2((keyf(buf[i].x) - M) * P.c2);
       ++kept;
     }
   }
@@ -798,7 +813,7 @@ __device__ void topk_row_exact(const Params& P, const T* row, uint32_t* hist, Sm
   for (int e = t; e < V; e += kThreads) {
     float z = load1<T>(row + e);
     if (z >= thr) {
-      s += exp2f((z - m) * P.c2);
+      s += ex2((z - m) * P.c2);
       ++kept;
     }
   }
@@ -841,10 +856,10 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
   if (MODE == kSample) {
     for (int r = warp; r < nrows; r += kWarps) {
       const int rp = r <= Kb ? r : K + 1 + (r - Kb - 1);
-      const float2* part = P.partial + ((size_t)b * P.R + rp) * P.nchunk;
+      const float2* part = P.partial + ((size_t)b * P.R + rp) * P.nchunk * kWarps;
       float m = -INFINITY, s = 0.0f;
-      for (int c = lane; c < P.nchunk; c += 32) {
-        float2 pc = __ldcg(part + c);
+      for (int c = lane; c < P.nchunk * kWarps; c += 32) {
+        float2 pc = __ldg(part + c);
         lse_merge(m, s, pc.x, pc.y, P.c2);
       }
       lse_warp(m, s, P.c2);
@@ -857,12 +872,12 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
     }
   } else if (MODE == kGreedy) {
     for (int r = warp; r < nrows; r += kWarps) {
-      const float2* part = P.partial + ((size_t)b * P.R + r) * P.nchunk;
+      const float2* part = P.partial + ((size_t)b * P.R + r) * P.nchunk * kWarps;
       float best = -INFINITY;
       int bi = 0x7FFFFFFF;
       bool nan = false;
-      for (int c = lane; c < P.nchunk; c += 32) {
-        float2 pc = __ldcg(part + c);
+      for (int c = lane; c < P.nchunk * kWarps; c += 32) {
+        float2 pc = __ldg(part + c);
         int idx = __float_as_int(pc.y);
         if (idx < 0) nan = true;
         amax_merge(best, bi, pc.x, idx);
@@ -963,8 +978,8 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
           const float zp = load1<T>(prow<T>(P, b, lane) + x);
           const float zq = load1<T>(qrow<T>(P, b, lane) + x);
           const int rq = Kb + 1 + lane;
-          if (zp >= sm.rowT[lane]) a = exp2f((zp - sm.rowM[lane]) * P.c2) / sm.rowS[lane];
-          if (zq >= sm.rowT[rq]) cq = exp2f((zq - sm.rowM[rq]) * P.c2) / sm.rowS[rq];
+          if (zp >= sm.rowT[lane]) a = ex2((zp - sm.rowM[lane]) * P.c2) / sm.rowS[lane];
+          if (zq >= sm.rowT[rq]) cq = ex2((zq - sm.rowM[rq]) * P.c2) / sm.rowS[rq];
         }
         const float u = __ldg(P.ua + (size_t)b * K + lane);
         acc = u * cq < a;
@@ -1004,13 +1019,62 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
     const T* qr = d.resid ? qrow<T>(P, b, js) : pr;
     float* wt = reinterpret_cast<float*>(dyn + (MODE == kTopK ? (size_t)kWarps * kRowCap * sizeof(uint2) : 0));
     int clamp = 0;
-    float R = draw_row<T, VEC>(P, pr, qr, d, u, wt, sm, &clamp);
+    bool drawn = false;
+    float R = 0.0f;
+    if (MODE == kSample && !d.resid) {
+      // Bonus draw: the chunk masses follow from the stored (max, sum) pairs, so only the chunk
+      // holding u * S is read again.
+      const int nch = P.nchunk;
+      const float2* part = P.partial + ((size_t)b * P.R + js) * nch * kWarps;
+      for (int c = t; c < nch; c += kThreads) {
+        float mass = 0.0f;
+        for (int w = 0; w < kWarps; ++w) {
+          const float2 pc = __ldg(part + (size_t)c * kWarps + w);
+          if (pc.y != 0.0f) mass += pc.y * ex2((pc.x - d.Mp) * P.c2);
+        }
+        wt[c] = mass;
+      }
+      __syncthreads();
+      if (t == 0) {
+        float S = 0.0f;
+        for (int c = 0; c < nch; ++c) S += wt[c];
+        const float target = u * S;
+        float cum = 0.0f;
+        int cs = -1;
+        for (int c = 0; c < nch; ++c) {
+          if (target < cum + wt[c]) {
+            cs = c;
+            break;
+          }
+          cum += wt[c];
+        }
+        if (cs < 0) {  // rounding put u * S past the sum: the last chunk with mass (clamped below)
+          cs = nch - 1;
+          while (cs > 0 && !(wt[cs] > 0.0f)) --cs;
+          cum = 0.0f;
+          for (int c = 0; c < cs; ++c) cum += wt[c];
+        }
+        sm.tile = cs;
+        sm.tile_base = target - cum;
+        sm.total = S;
+      }
+      __syncthreads();
+      const int cs = sm.tile;
+      const float tin = sm.tile_base, S = sm.total;
+      __syncthreads();
+      const int v0 = cs * Cfg<T>::CH;
+      const float rc = draw_range<T, VEC>(P, pr, pr, d, v0, min(P.V, v0 + Cfg<T>::CH), false, u, tin, S,
+                                          wt, sm, &clamp);
+      drawn = rc > 0.0f;
+      R = S;
+    }
+    if (!drawn) R = draw_range<T, VEC>(P, pr, qr, d, 0, P.V, true, u, 0.0f, 0.0f, wt, sm, &clamp);
     float resid_mass = d.resid ? R : 0.0f;
     if (!(R > 0.0f)) {
       // max(0, p - q) vanished through rounding: draw from p instead
       d.resid = false;
       if (t == 0) sm.flags |= SPEC_FLAG_RESIDUAL_ZERO;
-      R = draw_row<T, VEC>(P, pr, pr, d, u, wt, sm, &clamp);
+      R = draw_range<T, VEC>(P, pr, pr, d, 0, P.V, true, u, 0.0f, 0.0f, wt, sm, &clamp);
     }
     if (clamp) atomicOr(&sm.flags, SPEC_FLAG_CDF_CLAMP);
     __syncthreads();
@@ -1038,7 +1102,6 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
   if (t == 0) {
     P.out_nacc[b] = sm.jstar;
     if (P.flags) P.flags[b] = sm.flags;
-    P.req_cnt[b] = 0;  // ready for the next call
   }
   if (P.lognorm) {
     const int R = 2 * K + 1;
@@ -1063,61 +1126,102 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
 // ------------------------------------------------------------------------------------------------
 // the kernel
 // ------------------------------------------------------------------------------------------------
-template <typename T, int MODE, bool VEC>
-__global__ void __launch_bounds__(kThreads, 4) verify_kernel(const Params P) {
-  extern __shared__ __align__(16) unsigned char dyn[];
-  __shared__ Smem sm;
-  const int t = threadIdx.x;
-  const uint32_t total = P.rowmap ? __ldg(P.total_rows) * (uint32_t)P.nchunk : P.uniform_items;
-  if (t == 0) sm.item = (int)atomicAdd(&P.sched[0], 1u);
-  __syncthreads();
-  uint32_t item = (uint32_t)sm.item;
-  while (item < total) {
-    uint32_t next = 0;
-    if (t == 0) next = atomicAdd(&P.sched[0], 1u);  // prefetch the next item
-    const uint32_t row = item / (uint32_t)P.nchunk;
-    const int c = (int)(item - row * (uint32_t)P.nchunk);
-    int b, rp;
-    if (P.rowmap) {
-      const uint32_t e = __ldg(P.rowmap + row);
-      b = (int)(e >> 6);
-      rp = (int)(e & 63u);
-    } else {
-      b = (int)(row / (uint32_t)P.R);
-      rp = (int)(row - (uint32_t)b * P.R);
-    }
-    const int v0 = c * kChunk;
-    const int n = min(kChunk, P.V - v0);
+// Item -> (request, padded row, chunk).
+__device__ __forceinline__ void decode_item(const Params& P, uint32_t item, int& b, int& rp, int& c) {
+  const uint32_t row = item / (uint32_t)P.nchunk;
+  c = (int)(item - row * (uint32_t)P.nchunk);
+  if (P.rowmap) {
+    const uint32_t e = __ldg(P.rowmap + row);
+    b = (int)(e >> 6);
+    rp = (int)(e & 63u);
+  } else {
+    b = (int)(row / (uint32_t)P.R);
+    rp = (int)(row - (uint32_t)b * P.R);
+  }
+}
+
+// Starts the copy of item `item`'s chunk into `stage` (nothing for item >= total) and commits.
+template <typename T>
+__device__ __forceinline__ void issue_chunk(const Params& P, uint32_t item, uint32_t total, uint4* stage) {
+  if (item < total) {
+    int b, rp, c;
+    decode_item(P, item, b, rp, c);
+    const int v0 = c * Cfg<T>::CH;
+    const int n = min(Cfg<T>::CH, P.V - v0);
     const T* base = row_ptr<T>(P, b, rp) + v0;
+#pragma unroll
+    for (int l = 0; l < Cfg<T>::LOADS; ++l) {
+      const int e0 = (l * kThreads + threadIdx.x) * Cfg<T>::VW;
+      const bool ok = e0 < n;
+      cp_async16(stage + l * kThreads + threadIdx.x, ok ? base + e0 : base, ok ? 16 : 0);
+    }
+  }
+  cp_async_commit();
+}
+
+// Pass 1: stream every valid row once.  Items (request, row, chunk) are assigned statically in
+// request-major order (item = block + i * grid), so the loads of the next kStages - 1 items are
+// always in flight in the cp.async ring; no block ever waits for another.
+template <typename T, int MODE, bool VEC>
+__global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
+  extern __shared__ __align__(128) unsigned char dyn[];
+  __shared__ Smem sm;
+  const uint32_t total = P.rowmap ? __ldg(P.total_rows) * (uint32_t)P.nchunk : P.uniform_items;
+  const uint32_t G = gridDim.x;
+  uint4* stages = reinterpret_cast<uint4*>(dyn);
+  uint2* surv = reinterpret_cast<uint2*>(dyn + (VEC ? (size_t)kStages * kChunkBytes : 0));
+  auto summarise = [&](uint32_t item, const float (&v)[Cfg<T>::PER]) {
+    int b, rp, c;
+    decode_item(P, item, b, rp, c);
+    const int v0 = c * Cfg<T>::CH;
+    const int n = min(Cfg<T>::CH, P.V - v0);
     const size_t slot = ((size_t)b * P.R + rp) * P.nchunk + c;
     if (MODE == kSample)
-      item_sample<T, VEC>(P, base, n, P.partial + slot, sm);
+      item_sample<T>(P, v, P.partial + slot * kWarps);
     else if (MODE == kGreedy)
-      item_greedy<T, VEC>(P, base, n, P.partial + slot, sm);
+      item_greedy<T, VEC>(v, n, v0, P.partial + slot * kWarps);
     else
-      item_topk<T, VEC>(P, base, n, v0, P.cand + slot * kCandCap, P.cmeta + slot, sm,
-                        reinterpret_cast<uint2*>(dyn));
-    __threadfence();
-    __syncthreads();
-    if (t == 0) {
-      const int kb = clamp_k(P, b, nullptr);
-      const uint32_t need = (uint32_t)(MODE == kGreedy ? kb + 1 : 2 * kb + 1) * (uint32_t)P.nchunk;
-      sm.last = atomicAdd(&P.req_cnt[b], 1u) == need - 1;
-      sm.item = (int)next;
+      item_topk<T, VEC>(P, v, n, v0, P.cand + slot * kCandCap, P.cmeta + slot, sm, surv);
+  };
+  if (VEC) {
+#pragma unroll
+    for (int s = 0; s < kStages; ++s)
+      issue_chunk<T>(P, blockIdx.x + s * G, total, stages + (size_t)s * (kChunkBytes / 16));
+    for (uint32_t i = 0;; ++i) {
+      const uint32_t item = blockIdx.x + i * G;
+      if (item >= total) break;
+      const int s = (int)(i % kStages);
+      uint4* st = stages + (size_t)s * (kChunkBytes / 16);
+      cp_async_wait<kStages - 1>();  // this thread's copies of item i have landed
+      int b, rp, c;
+      decode_item(P, item, b, rp, c);
+      float v[Cfg<T>::PER];
+      load_stage<T>(st, min(Cfg<T>::CH, P.V - c * Cfg<T>::CH), v);
+      issue_chunk<T>(P, item + kStages * G, total, st);  // the stage's bytes are in registers now
+      summarise(item, v);
     }
-    __syncthreads();
-    if (sm.last) {
-      __threadfence();
-      finish_request<T, MODE, VEC>(P, b, sm, dyn);
+    cp_async_wait<0>();
+  } else {
+    for (uint32_t item = blockIdx.x; item < total; item += G) {
+      int b, rp, c;
+      decode_item(P, item, b, rp, c);
+      const int v0 = c * Cfg<T>::CH;
+      float v[Cfg<T>::PER];
+      load_chunk<T, VEC>(row_ptr<T>(P, b, rp) + v0, min(Cfg<T>::CH, P.V - v0), v);
+      summarise(item, v);
     }
-    item = (uint32_t)sm.item;
-    __syncthreads();
   }
-  if (t == 0) {
-    if (atomicAdd(&P.sched[1], 1u) == gridDim.x - 1) {  // the last CTA out resets the scheduler
-      P.sched[0] = 0;
-      P.sched[1] = 0;
-    }
+}
+
+// Pass 2: one block per request merges its rows' summaries, runs the ratio test and the
+// first-rejection scan, and draws the resampled or bonus token.
+template <typename T, int MODE, bool VEC>
+__global__ void __launch_bounds__(kThreads) finish_kernel(const Params P) {
+  extern __shared__ __align__(128) unsigned char dyn[];
+  __shared__ Smem sm;
+  for (int b = blockIdx.x; b < P.B; b += gridDim.x) {
+    finish_request<T, MODE, VEC>(P, b, sm, dyn);
+    __syncthreads();
   }
 }
 
@@ -1166,26 +1270,25 @@ __global__ void __launch_bounds__(1024) build_rowmap(const int32_t* __restrict__
 // host side
 // ------------------------------------------------------------------------------------------------
 struct Layout {
-  size_t sched, req_cnt, partial, cmeta, cand, rowmap, total_rows, bytes;
+  size_t partial, cmeta, cand, rowmap, total_rows, bytes;
   int R, nchunk;
   uint64_t rows_padded;
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-static bool make_layout(int B, int K, int V, int mode, bool ragged, Layout* L) {
+// Workspace: per-chunk summaries (one pair per warp), top-k candidates, the ragged row table.
+// Nothing in it outlives a call, so it needs no initialisation.
+static bool make_layout(int B, int K, int V, int es, int mode, bool ragged, Layout* L) {
+  const int ch = kChunkBytes / es;
   L->R = mode == kGreedy ? K + 1 : 2 * K + 1;
-  L->nchunk = (V + kChunk - 1) / kChunk;
+  L->nchunk = (V + ch - 1) / ch;
   L->rows_padded = (uint64_t)B * L->R;
   const uint64_t items = L->rows_padded * (uint64_t)L->nchunk;
   if (items >= (1ull << 31) || (uint64_t)B >= (1ull << 25)) return false;
   size_t o = 0;
-  L->sched = o;
-  o = align256(o + 2 * sizeof(uint32_t));
-  L->req_cnt = o;
-  o = align256(o + (size_t)B * sizeof(uint32_t));
   L->partial = o;
-  o = align256(o + (size_t)items * sizeof(float2));
+  o = align256(o + (size_t)items * kWarps * sizeof(float2));
   L->cmeta = o;
   L->cand = o;
   if (mode == kTopK) {
@@ -1200,7 +1303,7 @@ static bool make_layout(int B, int K, int V, int mode, bool ragged, Layout* L) {
     L->total_rows = o;
     o = align256(o + sizeof(uint32_t));
   }
-  L->bytes = o;
+  L->bytes = o > 0 ? o : 256;
   return true;
 }
 
@@ -1209,47 +1312,57 @@ static int mode_of(float temperature, int top_k, int V) {
   return (top_k > 0 && top_k < V) ? kTopK : kSample;
 }
 
-static size_t dyn_smem_bytes(int mode, int V) {
+// dynamic shared memory of the two passes
+static size_t stats_smem(int mode, bool vec) {
+  return (vec ? (size_t)kStages * kChunkBytes : 0) + (mode == kTopK ? (size_t)kSurvCap * sizeof(uint2) : 0);
+}
+static size_t finish_smem(int mode, int V, int es) {
   const int ntile = (V + kTile - 1) / kTile;
-  size_t wt = (size_t)ntile * sizeof(float);
-  if (mode == kGreedy) return 0;
-  if (mode == kTopK) {
-    size_t a = (size_t)kWarps * kRowCap * sizeof(uint2) + wt;
-    size_t b = (size_t)kSurvCap * sizeof(uint2);
-    return a > b ? a : b;
-  }
+  const int nch = (V + kChunkBytes / es - 1) / (kChunkBytes / es);
+  size_t wt = (size_t)(ntile > nch ? ntile : nch) * sizeof(float);
+  if (mode == kGreedy) return 16;
+  if (mode == kTopK) wt += (size_t)kWarps * kRowCap * sizeof(uint2);
   return wt;
 }
 
+template <typename K>
+static cudaError_t prepare(K kern, size_t dsm) {
+  if (dsm > 32 * 1024) return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm);
+  return cudaSuccess;
+}
+
 template <typename T, int MODE, bool VEC>
-static cudaError_t launch_t(const Params& P, uint32_t items, size_t dsm, cudaStream_t st) {
-  auto kern = verify_kernel<T, MODE, VEC>;
-  if (dsm > 32 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm);
-    if (e != cudaSuccess) return e;
-  }
+static cudaError_t launch_t(const Params& P, uint32_t items, cudaStream_t st) {
+  const int es = (int)sizeof(T);
+  auto k1 = stats_kernel<T, MODE, VEC>;
+  auto k2 = finish_kernel<T, MODE, VEC>;
+  const size_t d1 = stats_smem(MODE, VEC), d2 = finish_smem(MODE, P.V, es);
+  cudaError_t e = prepare(k1, d1);
+  if (e == cudaSuccess) e = prepare(k2, d2);
   int dev = 0, sms = 0, occ = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, dsm);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k1, kThreads, d1);
   if (e != cudaSuccess) return e;
   if (occ < 1) occ = 1;
-  uint32_t grid = (uint32_t)sms * (uint32_t)occ;
+  uint32_t grid = (uint32_t)sms * (uint32_t)occ;  // one resident wave, static item assignment
   if (items < grid) grid = items > 0 ? items : 1;
-  kern<<<grid, kThreads, dsm, st>>>(P);
+  k1<<<grid, kThreads, d1, st>>>(P);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  k2<<<(unsigned)P.B, kThreads, d2, st>>>(P);
   return cudaGetLastError();
 }
 
 template <typename T>
-static cudaError_t launch_mode(int mode, bool vec, const Params& P, uint32_t items, size_t dsm,
-                               cudaStream_t st) {
+static cudaError_t launch_mode(int mode, bool vec, const Params& P, uint32_t items, cudaStream_t st) {
   switch (mode) {
     case kSample:
-      return vec ? launch_t<T, kSample, true>(P, items, dsm, st) : launch_t<T, kSample, false>(P, items, dsm, st);
+      return vec ? launch_t<T, kSample, true>(P, items, st) : launch_t<T, kSample, false>(P, items, st);
     case kTopK:
-      return vec ? launch_t<T, kTopK, true>(P, items, dsm, st) : launch_t<T, kTopK, false>(P, items, dsm, st);
+      return vec ? launch_t<T, kTopK, true>(P, items, st) : launch_t<T, kTopK, false>(P, items, st);
     default:
-      return vec ? launch_t<T, kGreedy, true>(P, items, dsm, st) : launch_t<T, kGreedy, false>(P, items, dsm, st);
+      return vec ? launch_t<T, kGreedy, true>(P, items, st) : launch_t<T, kGreedy, false>(P, items, st);
   }
 }
 
@@ -1267,7 +1380,8 @@ size_t spec_verify_workspace_bytes(int32_t B, int32_t K_max, int32_t V, spec_dty
   // the largest layout over the three modes, so one workspace serves any temperature
   Layout a, b;
   const int heavy = (top_k > 0 && top_k < V) ? kTopK : kSample;
-  if (!make_layout(B, K_max, V, heavy, true, &a) || !make_layout(B, K_max, V, kGreedy, true, &b)) return 0;
+  const int es = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
+  if (!make_layout(B, K_max, V, es, heavy, true, &a) || !make_layout(B, K_max, V, es, kGreedy, true, &b)) return 0;
   return a.bytes > b.bytes ? a.bytes : b.bytes;
 }
 
@@ -1283,14 +1397,14 @@ spec_status_t spec_verify(const void* p_logits, const void* q_logits, const int3
   if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED;
   const int mode = mode_of(temperature, top_k, V);
   if (mode == kTopK && top_k > SPEC_MAX_TOPK) return SPEC_ERR_UNSUPPORTED;
+  if (B == 0) return SPEC_OK;  // nothing to read or write (empty arrays may have null pointers)
   if (!p_logits || !out_tokens || !out_num_accepted) return SPEC_ERR_INVALID_ARG;
   if (K_max > 0 && !draft_tokens) return SPEC_ERR_INVALID_ARG;
   if (mode != kGreedy && (!u_resample || (K_max > 0 && (!q_logits || !u_accept))))
     return SPEC_ERR_INVALID_ARG;
-  if (B == 0) return SPEC_OK;
   const bool ragged = k_per_row != nullptr;
   Layout L;
-  if (!make_layout(B, K_max, V, mode, ragged, &L)) return SPEC_ERR_UNSUPPORTED;
+  if (!make_layout(B, K_max, V, dtype == SPEC_DTYPE_BF16 ? 2 : 4, mode, ragged, &L)) return SPEC_ERR_UNSUPPORTED;
   if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
 
   const size_t es = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
@@ -1324,8 +1438,6 @@ spec_status_t spec_verify(const void* p_logits, const void* q_logits, const int3
   const double T = temperature;
   P.c2 = mode == kGreedy ? 0.0f : (float)(1.4426950408889634 / T);
   P.invT = mode == kGreedy ? 0.0f : (float)(1.0 / T);
-  P.sched = reinterpret_cast<uint32_t*>(ws + L.sched);
-  P.req_cnt = reinterpret_cast<uint32_t*>(ws + L.req_cnt);
   P.partial = reinterpret_cast<float2*>(ws + L.partial);
   P.cmeta = reinterpret_cast<uint2*>(ws + L.cmeta);
   P.cand = reinterpret_cast<uint2*>(ws + L.cand);
@@ -1340,10 +1452,9 @@ spec_status_t spec_verify(const void* p_logits, const void* q_logits, const int3
                                     reinterpret_cast<uint32_t*>(ws + L.total_rows));
     if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
   }
-  const size_t dsm = dyn_smem_bytes(mode, V);
   const uint32_t items = P.uniform_items;  // an upper bound on the grid's useful size
-  cudaError_t e = dtype == SPEC_DTYPE_BF16 ? launch_mode<uint16_t>(mode, vec, P, items, dsm, s)
-                                           : launch_mode<float>(mode, vec, P, items, dsm, s);
+  cudaError_t e = dtype == SPEC_DTYPE_BF16 ? launch_mode<uint16_t>(mode, vec, P, items, s)
+                                           : launch_mode<float>(mode, vec, P, items, s);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

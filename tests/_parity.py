@@ -33,7 +33,7 @@ def run_gpu(d, dev="cuda:0", stats=True, k_per_row="auto", **kw):
     import speculative_decoding_rejection_verify_gb300 as sv
     kpr = d["k_per_row"]
     w = d.get("workload")
-    if k_per_row == "auto":
+    if isinstance(k_per_row, str):
         k_per_row = kpr if (w is None or w.ragged is not None) else None
     T = d["temperature"]
     greedy = T == 0.0
@@ -53,7 +53,7 @@ def run_oracle(d, nthreads=0, k_per_row="auto"):
     import oracle
     w = d.get("workload")
     kpr = d["k_per_row"]
-    if k_per_row == "auto":
+    if isinstance(k_per_row, str):
         k_per_row = kpr if (w is None or w.ragged is not None) else None
     return oracle.verify(d["p"], d["q"], d["draft"], k_per_row, d["ua"], d["ur"], d["temperature"],
                          d["top_k"], nthreads=nthreads or (os.cpu_count() or 1))
@@ -91,10 +91,10 @@ def compare(g, o, K, kb=None, check_stats=True):
         assert 0 <= tg[ng] < 1 << 30
         if not check_stats or "p_draft" not in g:
             continue
-        j = min(no, ng)
+        jj = min(min(no, ng) + 1, K)  # examined positions on both sides
         for key in ("p_draft", "q_draft"):
-            a, r = g[key][b, : j + 1], o[key][b, : j + 1]
-            sel = np.isfinite(r) & (np.arange(j + 1) < kb[b])
+            a, r = g[key][b, :jj], o[key][b, :jj]
+            sel = np.isfinite(r) & (np.arange(jj) < kb[b])
             np.testing.assert_allclose(a[sel], r[sel], rtol=RTOL, atol=1e-30, err_msg=f"b={b} {key}")
         ln_o, ln_g = o["row_lognorm"][b], g["row_lognorm"][b]
         fin = np.isfinite(ln_o)
