@@ -1126,56 +1126,157 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
 // ------------------------------------------------------------------------------------------------
 // the kernel
 // ------------------------------------------------------------------------------------------------
-// Item -> (request, padded row, chunk).
-__device__ __forceinline__ void decode_item(const Params& P, uint32_t item, int& b, int& rp, int& c) {
+// Position in the item space of one CTA's contiguous range: request b, padded row rp, chunk c,
+// and the row's first byte.  Advanced one chunk at a time without divisions.
+struct Cursor {
+  int b, rp, c;
+  uint32_t crow;  // compact row index (ragged layout)
+  const char* row;
+};
+
+template <typename T>
+__device__ __forceinline__ const char* row_bytes(const Params& P, int b, int rp) {
+  return reinterpret_cast<const char*>(row_ptr<T>(P, b, rp));
+}
+
+template <typename T>
+__device__ __forceinline__ void cursor_at(const Params& P, uint32_t item, Cursor& k) {
   const uint32_t row = item / (uint32_t)P.nchunk;
-  c = (int)(item - row * (uint32_t)P.nchunk);
+  k.c = (int)(item - row * (uint32_t)P.nchunk);
+  k.crow = row;
   if (P.rowmap) {
     const uint32_t e = __ldg(P.rowmap + row);
-    b = (int)(e >> 6);
-    rp = (int)(e & 63u);
+    k.b = (int)(e >> 6);
+    k.rp = (int)(e & 63u);
   } else {
-    b = (int)(row / (uint32_t)P.R);
-    rp = (int)(row - (uint32_t)b * P.R);
+    k.b = (int)(row / (uint32_t)P.R);
+    k.rp = (int)(row - (uint32_t)k.b * P.R);
+  }
+  k.row = row_bytes<T>(P, k.b, k.rp);
+}
+
+template <typename T>
+__device__ __forceinline__ void cursor_next(const Params& P, Cursor& k) {
+  if (++k.c < P.nchunk) return;
+  k.c = 0;
+  ++k.crow;
+  if (P.rowmap) {
+    const uint32_t e = __ldg(P.rowmap + k.crow);
+    k.b = (int)(e >> 6);
+    k.rp = (int)(e & 63u);
+  } else if (++k.rp == P.R) {
+    k.rp = 0;
+    ++k.b;
+  }
+  k.row = row_bytes<T>(P, k.b, k.rp);
+}
+
+// Starts the copy of the cursor's chunk into `stage` (16 bytes per thread per vector).
+template <typename T>
+__device__ __forceinline__ void issue_at(const Params& P, const Cursor& k, uint4* stage) {
+  const int v0 = k.c * Cfg<T>::CH;
+  const int n = min(Cfg<T>::CH, P.V - v0);
+  const char* base = k.row + (size_t)v0 * sizeof(T);
+#pragma unroll
+  for (int l = 0; l < Cfg<T>::LOADS; ++l) {
+    const int e0 = (l * kThreads + threadIdx.x) * Cfg<T>::VW;
+    const bool ok = e0 < n;
+    cp_async16(stage + l * kThreads + threadIdx.x, ok ? base + (size_t)e0 * sizeof(T) : base, ok ? 16 : 0);
   }
 }
 
-// Starts the copy of item `item`'s chunk into `stage` (nothing for item >= total) and commits.
+__device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Sampling summary of one chunk straight from its packed 16-byte vectors: the max on packed
+// values, then 2^((z - max) * c2) in packed f32x2 arithmetic, then a warp max and a rescaled warp
+// sum.  Writes (max, sum) for the warp's share to out[warp].
 template <typename T>
-__device__ __forceinline__ void issue_chunk(const Params& P, uint32_t item, uint32_t total, uint4* stage) {
-  if (item < total) {
-    int b, rp, c;
-    decode_item(P, item, b, rp, c);
-    const int v0 = c * Cfg<T>::CH;
-    const int n = min(Cfg<T>::CH, P.V - v0);
-    const T* base = row_ptr<T>(P, b, rp) + v0;
+__device__ __forceinline__ void sample_vec(const Params& P, uint4 (&raw)[Cfg<T>::LOADS], int n, float2* out) {
+  const int t = threadIdx.x;
+  if (n < Cfg<T>::CH) {  // tail chunk: vectors at or past n hold no logits
+#pragma unroll
+    for (int l = 0; l < Cfg<T>::LOADS; ++l)
+      if ((l * kThreads + t) * Cfg<T>::VW >= n)
+        raw[l] = sizeof(T) == 2 ? make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u)
+                                : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+  }
+  float m;
+  if (sizeof(T) == 2) {
+    uint32_t mx = raw[0].x;
 #pragma unroll
     for (int l = 0; l < Cfg<T>::LOADS; ++l) {
-      const int e0 = (l * kThreads + threadIdx.x) * Cfg<T>::VW;
-      const bool ok = e0 < n;
-      cp_async16(stage + l * kThreads + threadIdx.x, ok ? base + e0 : base, ok ? 16 : 0);
+      if (l > 0) mx = bmax2_nan(mx, raw[l].x);
+      mx = bmax2_nan(mx, raw[l].y);
+      mx = bmax2_nan(mx, raw[l].z);
+      mx = bmax2_nan(mx, raw[l].w);
+    }
+    m = fmax_nan(bf16_lo(mx), bf16_hi(mx));
+  } else {
+    m = -INFINITY;
+#pragma unroll
+    for (int l = 0; l < Cfg<T>::LOADS; ++l) {
+      m = fmax_nan(m, __uint_as_float(raw[l].x));
+      m = fmax_nan(m, __uint_as_float(raw[l].y));
+      m = fmax_nan(m, __uint_as_float(raw[l].z));
+      m = fmax_nan(m, __uint_as_float(raw[l].w));
     }
   }
-  cp_async_commit();
+  float s = 0.0f;
+  if (m != -INFINITY) {
+    const float2 negm = make_float2(-m, -m), cc = make_float2(P.c2, P.c2);
+    float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int l = 0; l < Cfg<T>::LOADS; ++l) {
+      const uint32_t w[4] = {raw[l].x, raw[l].y, raw[l].z, raw[l].w};
+      if (sizeof(T) == 2) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float2 d = __fmul2_rn(__fadd2_rn(make_float2(bf16_lo(w[k]), bf16_hi(w[k])), negm), cc);
+          acc = __fadd2_rn(acc, make_float2(ex2(d.x), ex2(d.y)));
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; k += 2) {
+          float2 d = __fmul2_rn(__fadd2_rn(make_float2(__uint_as_float(w[k]), __uint_as_float(w[k + 1])), negm), cc);
+          acc = __fadd2_rn(acc, make_float2(ex2(d.x), ex2(d.y)));
+        }
+      }
+    }
+    s = acc.x + acc.y;
+  }
+  // warp: max first (NaN-propagating), then every lane rescales its sum to it and the sums add up
+  float M = m;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmax_nan(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+  float sc = s == 0.0f ? 0.0f : s * ex2((m - M) * P.c2);
+  sc = warp_sum(sc);
+  if ((t & 31) == 0) out[t >> 5] = make_float2(M, sc);
 }
 
-// Pass 1: stream every valid row once.  Items (request, row, chunk) are assigned statically in
-// request-major order (item = block + i * grid), so the loads of the next kStages - 1 items are
-// always in flight in the cp.async ring; no block ever waits for another.
+// Pass 1: stream every valid row once.  Each CTA owns a contiguous range of items
+// (request, row, chunk), so successive items walk memory in order and the cursor needs no
+// divisions; the cp.async ring keeps the next kStages - 1 chunks in flight.  No block waits for
+// another and nothing is counted: pass 2 starts when this grid is done.
 template <typename T, int MODE, bool VEC>
 __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ Smem sm;
   const uint32_t total = P.rowmap ? __ldg(P.total_rows) * (uint32_t)P.nchunk : P.uniform_items;
-  const uint32_t G = gridDim.x;
+  const uint32_t lo = (uint32_t)(((uint64_t)total * blockIdx.x) / gridDim.x);
+  const uint32_t hi = (uint32_t)(((uint64_t)total * (blockIdx.x + 1)) / gridDim.x);
+  if (lo >= hi) return;
   uint4* stages = reinterpret_cast<uint4*>(dyn);
   uint2* surv = reinterpret_cast<uint2*>(dyn + (VEC ? (size_t)kStages * kChunkBytes : 0));
-  auto summarise = [&](uint32_t item, const float (&v)[Cfg<T>::PER]) {
-    int b, rp, c;
-    decode_item(P, item, b, rp, c);
-    const int v0 = c * Cfg<T>::CH;
+  Cursor cc;
+  cursor_at<T>(P, lo, cc);
+  auto summarise_f = [&](const Cursor& k, const float (&v)[Cfg<T>::PER]) {
+    const int v0 = k.c * Cfg<T>::CH;
     const int n = min(Cfg<T>::CH, P.V - v0);
-    const size_t slot = ((size_t)b * P.R + rp) * P.nchunk + c;
+    const size_t slot = ((size_t)k.b * P.R + k.rp) * P.nchunk + k.c;
     if (MODE == kSample)
       item_sample<T>(P, v, P.partial + slot * kWarps);
     else if (MODE == kGreedy)
@@ -1184,31 +1285,47 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
       item_topk<T, VEC>(P, v, n, v0, P.cand + slot * kCandCap, P.cmeta + slot, sm, surv);
   };
   if (VEC) {
+    Cursor ic = cc;
 #pragma unroll
-    for (int s = 0; s < kStages; ++s)
-      issue_chunk<T>(P, blockIdx.x + s * G, total, stages + (size_t)s * (kChunkBytes / 16));
-    for (uint32_t i = 0;; ++i) {
-      const uint32_t item = blockIdx.x + i * G;
-      if (item >= total) break;
-      const int s = (int)(i % kStages);
+    for (int s = 0; s < kStages; ++s) {
+      if (lo + s < hi) {
+        issue_at<T>(P, ic, stages + (size_t)s * (kChunkBytes / 16));
+        cursor_next<T>(P, ic);
+      }
+      cp_async_commit();
+    }
+    int s = 0;
+    for (uint32_t it = lo; it < hi; ++it) {
       uint4* st = stages + (size_t)s * (kChunkBytes / 16);
-      cp_async_wait<kStages - 1>();  // this thread's copies of item i have landed
-      int b, rp, c;
-      decode_item(P, item, b, rp, c);
-      float v[Cfg<T>::PER];
-      load_stage<T>(st, min(Cfg<T>::CH, P.V - c * Cfg<T>::CH), v);
-      issue_chunk<T>(P, item + kStages * G, total, st);  // the stage's bytes are in registers now
-      summarise(item, v);
+      cp_async_wait<kStages - 1>();  // this thread's copies of this item have landed
+      uint4 raw[Cfg<T>::LOADS];
+#pragma unroll
+      for (int l = 0; l < Cfg<T>::LOADS; ++l) raw[l] = st[l * kThreads + threadIdx.x];
+      if (it + kStages < hi) {  // the stage's bytes are in registers: refill it
+        issue_at<T>(P, ic, st);
+        cursor_next<T>(P, ic);
+      }
+      cp_async_commit();
+      const int n = min(Cfg<T>::CH, P.V - cc.c * Cfg<T>::CH);
+      if (MODE == kSample) {
+        const size_t slot = ((size_t)cc.b * P.R + cc.rp) * P.nchunk + cc.c;
+        sample_vec<T>(P, raw, n, P.partial + slot * kWarps);
+      } else {
+        float v[Cfg<T>::PER];
+        unpack<T>(raw, n, v);
+        summarise_f(cc, v);
+      }
+      cursor_next<T>(P, cc);
+      s = s + 1 == kStages ? 0 : s + 1;
     }
     cp_async_wait<0>();
   } else {
-    for (uint32_t item = blockIdx.x; item < total; item += G) {
-      int b, rp, c;
-      decode_item(P, item, b, rp, c);
-      const int v0 = c * Cfg<T>::CH;
+    for (uint32_t it = lo; it < hi; ++it) {
+      const int v0 = cc.c * Cfg<T>::CH;
       float v[Cfg<T>::PER];
-      load_chunk<T, VEC>(row_ptr<T>(P, b, rp) + v0, min(Cfg<T>::CH, P.V - v0), v);
-      summarise(item, v);
+      load_chunk<T, VEC>(reinterpret_cast<const T*>(cc.row) + v0, min(Cfg<T>::CH, P.V - v0), v);
+      summarise_f(cc, v);
+      cursor_next<T>(P, cc);
     }
   }
 }
