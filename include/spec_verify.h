@@ -143,6 +143,31 @@ spec_status_t spec_verify_host(const void* p_logits, const void* q_logits,
                                int32_t B, int32_t K_max, int32_t V, spec_dtype_t dtype,
                                void* staging, size_t staging_bytes, void* stream);
 
+/* Size of the fixed device array behind spec_verify_static (16 MiB). */
+#define SPEC_STATIC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * spec_verify without a workspace argument, for callers that cannot allocate device memory: a
+ * custom operator running inside a framework whose memory pool owns every allocation, or a loop
+ * that must never block on cudaMalloc / cudaFree.  (This entry point has no counterpart in the
+ * pages; it only changes where the scratch lives.)
+ *   - The scratch is one file-scope device array of SPEC_STATIC_SCRATCH_BYTES that every GPU
+ *     loading this library keeps until the process exits; it needs no initialisation.
+ *   - The first call on a device (the current device) looks up the array's device address with
+ *     cudaGetSymbolAddress and caches it; make that first call before any stream capture.
+ *   - Sizes whose workspace (spec_verify_workspace_bytes) exceeds the array are rejected with
+ *     SPEC_ERR_WORKSPACE: B=1024, K_max=4, V=128256 without top-k fits; large top-k batches do not.
+ *   - Every call on a device shares the one array: calls that may overlap on the GPU (other
+ *     streams, other host threads) race and corrupt each other; serialise them.
+ *   - Allocates nothing; all other arguments and results are as for spec_verify.
+ */
+spec_status_t spec_verify_static(const void* p_logits, const void* q_logits,
+                                 const int32_t* draft_tokens, const int32_t* k_per_row,
+                                 const float* u_accept, const float* u_resample, float temperature,
+                                 int32_t top_k, int32_t* out_tokens, int32_t* out_num_accepted,
+                                 const spec_verify_stats_t* out_stats, int32_t B, int32_t K_max,
+                                 int32_t V, spec_dtype_t dtype, void* stream);
+
 /* A static, human-readable name for a status code. */
 const char* spec_verify_status_string(spec_status_t status);
 

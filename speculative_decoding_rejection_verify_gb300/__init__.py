@@ -42,7 +42,8 @@ MAX_V = 2097152
 MAX_TOPK = 256
 
 EXPORTS = ("spec_verify_workspace_bytes", "spec_verify", "spec_verify_host_staging_bytes",
-           "spec_verify_host", "spec_verify_status_string")
+           "spec_verify_host", "spec_verify_static", "spec_verify_status_string")
+STATIC_SCRATCH_BYTES = 16 << 20
 
 
 class SpecVerifyError(RuntimeError):
@@ -87,6 +88,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
             lib.spec_verify_host_staging_bytes.restype = Z
             lib.spec_verify_host.argtypes = [P, P, P, P, P, P, F, I, P, P, I, I, I, I, P, Z, P]
             lib.spec_verify_host.restype = I
+            lib.spec_verify_static.argtypes = [P, P, P, P, P, P, F, I, P, P, ctypes.POINTER(StatsStruct),
+                                               I, I, I, I, P]
+            lib.spec_verify_static.restype = I
             lib.spec_verify_status_string.argtypes = [I]
             lib.spec_verify_status_string.restype = ctypes.c_char_p
             _lib = lib

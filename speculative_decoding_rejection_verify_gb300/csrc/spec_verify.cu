@@ -25,6 +25,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "spec_verify.h"
 
 namespace sv {
@@ -1657,3 +1659,44 @@ const char* spec_verify_status_string(spec_status_t status) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------------------
+// spec_verify_static: the same step with its scratch in a fixed device array
+// ------------------------------------------------------------------------------------------------
+// Some callers have no way to hand this library device memory: a custom operator inside a host
+// framework whose memory pool owns every allocation, or a loop that must never block (cudaMalloc
+// and cudaFree can synchronise the device).  For them, the scratch lives in one file-scope device
+// array that every GPU loading this library holds until the process exits.  Its address is a
+// device address that host code can only learn through cudaGetSymbolAddress, once per device.
+
+namespace sv {
+constexpr size_t kStaticScratchBytes = (size_t)SPEC_STATIC_SCRATCH_BYTES;
+constexpr int kMaxDevices = 64;
+std::atomic<void*> g_scratch_addr[kMaxDevices];  // per device: the array's device address
+}  // namespace sv
+
+static __device__ __align__(256) unsigned char g_static_scratch[sv::kStaticScratchBytes];
+
+extern "C" spec_status_t spec_verify_static(const void* p_logits, const void* q_logits,
+                                            const int32_t* draft_tokens, const int32_t* k_per_row,
+                                            const float* u_accept, const float* u_resample,
+                                            float temperature, int32_t top_k, int32_t* out_tokens,
+                                            int32_t* out_num_accepted,
+                                            const spec_verify_stats_t* out_stats, int32_t B,
+                                            int32_t K_max, int32_t V, spec_dtype_t dtype,
+                                            void* stream) {
+  const size_t need = spec_verify_workspace_bytes(B < 0 ? 0 : B, K_max, V, dtype, top_k);
+  if (B < 0 || need == 0) return SPEC_ERR_INVALID_ARG;
+  if (need > sv::kStaticScratchBytes) return SPEC_ERR_WORKSPACE;  // beyond the fixed array
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= sv::kMaxDevices) return SPEC_ERR_CUDA;
+  void* scratch = sv::g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (scratch == nullptr) {  // first call on this device (the current one): look the address up
+    if (cudaGetSymbolAddress(&scratch, g_static_scratch) != cudaSuccess || scratch == nullptr)
+      return SPEC_ERR_CUDA;
+    sv::g_scratch_addr[dev].store(scratch, std::memory_order_release);
+  }
+  return spec_verify(p_logits, q_logits, draft_tokens, k_per_row, u_accept, u_resample, temperature,
+                     top_k, out_tokens, out_num_accepted, out_stats, B, K_max, V, dtype, scratch,
+                     sv::kStaticScratchBytes, stream);
+}
