@@ -40,7 +40,9 @@ constexpr int kCandCap = 256;            // top-k candidates stored per chunk
 constexpr int kSurvCap = 1024;           // survivors examined per chunk
 constexpr int kRowCap = 256;             // candidates >= the row's lower bound, per row
 constexpr int kMaxRows = 2 * SPEC_MAX_K + 1;
-constexpr int kUnrollA = 4;              // tiles in flight per warp in the CDF passes
+constexpr int kUnrollA = 4;              // tiles in flight per warp in the CDF passes (scalar rows)
+constexpr int kDrawStages = 4;           // cp.async ring of the CDF pass over aligned rows
+constexpr int kDrawStageBytes = 16384;   // per stage: the same 8 KB span of the p row and the q row
 
 enum Mode { kSample = 0, kTopK = 1, kGreedy = 2 };
 
@@ -499,29 +501,63 @@ __device__ __forceinline__ void load8(const T* __restrict__ row, int e0, int V, 
 // Weights of the inverse-CDF draw for 8 logits: the residual max(0, P - Q) when `resid`, else the
 // (unnormalised) target weights exp((z_p - M_p)/T) on the kept set.
 struct DrawRows {
-  float Mp, invSp, Tp;  // target row: max, 1/sum, top-k threshold
-  float Mq, invSq, Tq;  // draft row
+  float Lp, Tp;  // target row: log2 normaliser (max * c2 + log2 sum), top-k threshold
+  float Lq, Tq;  // draft row
+  float Mp2;     // target row max * c2 (scale of the weights of a draw from p alone)
   bool resid;
 };
 
-template <typename T, bool VEC>
-__device__ __forceinline__ void weights8(const T* pr, const T* qr, int e0, int V, const DrawRows& d,
-                                         float c2, float (&w)[8]) {
-  float zp[8];
-  load8<T, VEC>(pr, e0, V, zp);
+// Weights of the inverse-CDF draw for 8 logits: the residual max(0, P - Q) with
+// P = 2^(z_p * c2 - Lp), Q = 2^(z_q * c2 - Lq) when `resid`, else the target weights
+// 2^(z_p * c2 - Mp2) relative to the row max.  Logits below a top-k threshold weigh 0 (MASK).
+// Both passes of a draw compute them with these same instructions, so they agree bit for bit.
+template <bool MASK>
+__device__ __forceinline__ void weights_of(const float (&zp)[8], const float (&zq)[8], const DrawRows& d,
+                                           float c2, float (&w)[8]) {
+  const float2 cc = make_float2(c2, c2);
   if (d.resid) {
-    float zq[8];
-    load8<T, VEC>(qr, e0, V, zq);
+    const float2 nlp = make_float2(-d.Lp, -d.Lp), nlq = make_float2(-d.Lq, -d.Lq);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      float a = zp[k] >= d.Tp ? __fmul_rn(ex2(__fmul_rn(__fsub_rn(zp[k], d.Mp), c2)), d.invSp) : 0.0f;
-      float b = zq[k] >= d.Tq ? __fmul_rn(ex2(__fmul_rn(__fsub_rn(zq[k], d.Mq), c2)), d.invSq) : 0.0f;
-      w[k] = fmaxf(__fsub_rn(a, b), 0.0f);
+    for (int k = 0; k < 8; k += 2) {
+      const float2 a = __ffma2_rn(make_float2(zp[k], zp[k + 1]), cc, nlp);
+      const float2 b = __ffma2_rn(make_float2(zq[k], zq[k + 1]), cc, nlq);
+      float pa = ex2(a.x), pb = ex2(a.y), qa = ex2(b.x), qb = ex2(b.y);
+      if (MASK) {
+        pa = zp[k] >= d.Tp ? pa : 0.0f;
+        pb = zp[k + 1] >= d.Tp ? pb : 0.0f;
+        qa = zq[k] >= d.Tq ? qa : 0.0f;
+        qb = zq[k + 1] >= d.Tq ? qb : 0.0f;
+      }
+      const float2 r = __fadd2_rn(make_float2(pa, pb), make_float2(-qa, -qb));
+      w[k] = fmaxf(r.x, 0.0f);
+      w[k + 1] = fmaxf(r.y, 0.0f);
     }
   } else {
+    const float2 nm = make_float2(-d.Mp2, -d.Mp2);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) w[k] = zp[k] >= d.Tp ? ex2(__fmul_rn(__fsub_rn(zp[k], d.Mp), c2)) : 0.0f;
+    for (int k = 0; k < 8; k += 2) {
+      const float2 a = __ffma2_rn(make_float2(zp[k], zp[k + 1]), cc, nm);
+      w[k] = ex2(a.x);
+      w[k + 1] = ex2(a.y);
+      if (MASK) {
+        w[k] = zp[k] >= d.Tp ? w[k] : 0.0f;
+        w[k + 1] = zp[k + 1] >= d.Tp ? w[k + 1] : 0.0f;
+      }
+    }
   }
+}
+
+template <typename T, bool VEC, bool MASK>
+__device__ __forceinline__ void weights8(const T* pr, const T* qr, int e0, int V, const DrawRows& d,
+                                         float c2, float (&w)[8]) {
+  float zp[8], zq[8];
+  load8<T, VEC>(pr, e0, V, zp);
+  if (d.resid)
+    load8<T, VEC>(qr, e0, V, zq);
+  else
+#pragma unroll
+    for (int k = 0; k < 8; ++k) zq[k] = -INFINITY;
+  weights_of<MASK>(zp, zq, d, c2, w);
 }
 
 // Inverse-CDF draw over the logits [v0, vend) of a row: y = the smallest v with target < C_v,
@@ -530,36 +566,112 @@ __device__ __forceinline__ void weights8(const T* pr, const T* qr, int e0, int V
 // target = u * (its total), which is also the margin scale; otherwise `target` is the mass the
 // draw must pass inside the range and `Rm` the margin scale.  Returns the range total; sets
 // sm.y, sm.margin and the clamp flag.
-template <typename T, bool VEC>
+template <typename T, bool VEC, bool MASK>
 __device__ float draw_range(const Params& P, const T* pr, const T* qr, const DrawRows& d, int v0,
                             int vend, bool full, float u, float target_in, float Rm, float* wt,
-                            Smem& sm, int* clamp) {
+                            uint4* ring, Smem& sm, int* clamp) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int V = vend;
   const int ntile = (vend - v0 + kTile - 1) / kTile;
   // pass A: tile sums
-  for (int i0 = warp; i0 < ntile; i0 += kWarps * kUnrollA) {
-    float w[kUnrollA][8];
+  if constexpr (VEC) {
+    // Aligned rows stream through a cp.async ring: stage k holds elements [v0 + k*SE, + SE) of the
+    // p row and of the q row (the q half is not read for a draw from p alone).  Each thread copies
+    // 4 of the stage's 16-byte vectors; after the barrier every warp reads whole tiles.
+    constexpr int SE = kDrawStageBytes / 2 / (int)sizeof(T);  // elements per row per stage
+    constexpr int TPS = SE / kTile;                            // tiles per stage
+    constexpr int VPR = kDrawStageBytes / 2 / 16;              // 16-byte vectors per row per stage
+    constexpr int VW = 16 / (int)sizeof(T);
+    const int nstage = (vend - v0 + SE - 1) / SE;
+    auto issue = [&](int k) {
+      if (k < nstage) {
+        uint4* dst = ring + (size_t)(k % kDrawStages) * (kDrawStageBytes / 16);
+        const int base = v0 + k * SE;
 #pragma unroll
-    for (int u4 = 0; u4 < kUnrollA; ++u4) {
-      int i = i0 + u4 * kWarps;
-      if (i < ntile)
-        weights8<T, VEC>(pr, qr, v0 + i * kTile + lane * 8, V, d, P.c2, w[u4]);
-      else
+        for (int i = t; i < 2 * VPR; i += kThreads) {
+          const bool isq = i >= VPR;
+          const int e = base + (isq ? i - VPR : i) * VW;
+          const bool ok = e < vend && (!isq || d.resid);
+          const T* row = isq ? qr : pr;
+          cp_async16(dst + i, ok ? row + e : row, ok ? 16 : 0);
+        }
+      }
+      cp_async_commit();
+    };
 #pragma unroll
-        for (int k = 0; k < 8; ++k) w[u4][k] = 0.0f;
+    for (int k = 0; k < kDrawStages; ++k) issue(k);
+    for (int k = 0; k < nstage; ++k) {
+      cp_async_wait<kDrawStages - 1>();
+      __syncthreads();  // every thread's copies of stage k are in shared memory
+      const uint4* st = ring + (size_t)(k % kDrawStages) * (kDrawStageBytes / 16);
+      for (int ti = warp; ti < TPS; ti += kWarps) {
+        const int tile = k * TPS + ti;
+        if (tile >= ntile) break;
+        float zp[8], zq[8];
+        const int e0 = v0 + tile * kTile + lane * 8;
+        if (sizeof(T) == 2) {
+          const uint4 a = st[ti * 32 + lane], b = st[VPR + ti * 32 + lane];
+          const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            zp[2 * q4] = bf16_lo(wa[q4]);
+            zp[2 * q4 + 1] = bf16_hi(wa[q4]);
+            zq[2 * q4] = bf16_lo(wb[q4]);
+            zq[2 * q4 + 1] = bf16_hi(wb[q4]);
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint4 a = st[ti * 64 + lane * 2 + h], b = st[VPR + ti * 64 + lane * 2 + h];
+            zp[4 * h] = __uint_as_float(a.x);
+            zp[4 * h + 1] = __uint_as_float(a.y);
+            zp[4 * h + 2] = __uint_as_float(a.z);
+            zp[4 * h + 3] = __uint_as_float(a.w);
+            zq[4 * h] = __uint_as_float(b.x);
+            zq[4 * h + 1] = __uint_as_float(b.y);
+            zq[4 * h + 2] = __uint_as_float(b.z);
+            zq[4 * h + 3] = __uint_as_float(b.w);
+          }
+        }
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8)
+          if (e0 + q8 >= vend) zp[q8] = zq[q8] = -INFINITY;  // past the range: no mass
+        float w[8];
+        weights_of<MASK>(zp, zq, d, P.c2, w);
+        float sum = 0.0f;
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) sum += w[q8];
+        sum = warp_sum(sum);
+        if (lane == 0) wt[tile] = sum;
+      }
+      __syncthreads();  // stage k fully read: its slot may be refilled
+      issue(k + kDrawStages);
     }
+    cp_async_wait<0>();
+  } else {
+    for (int i0 = warp; i0 < ntile; i0 += kWarps * kUnrollA) {
+      float w[kUnrollA][8];
 #pragma unroll
-    for (int u4 = 0; u4 < kUnrollA; ++u4) {
-      int i = i0 + u4 * kWarps;
-      float s = 0.0f;
+      for (int u4 = 0; u4 < kUnrollA; ++u4) {
+        int i = i0 + u4 * kWarps;
+        if (i < ntile)
+          weights8<T, VEC, MASK>(pr, qr, v0 + i * kTile + lane * 8, V, d, P.c2, w[u4]);
+        else
 #pragma unroll
-      for (int k = 0; k < 8; ++k) s += w[u4][k];
-      s = warp_sum(s);
-      if (lane == 0 && i < ntile) wt[i] = s;
+          for (int k = 0; k < 8; ++k) w[u4][k] = 0.0f;
+      }
+#pragma unroll
+      for (int u4 = 0; u4 < kUnrollA; ++u4) {
+        int i = i0 + u4 * kWarps;
+        float s = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) s += w[u4][k];
+        s = warp_sum(s);
+        if (lane == 0 && i < ntile) wt[i] = s;
+      }
     }
   }
-  __syncthreads();
+  __syncthreads();  // every tile sum written
   // segments of tiles per thread, then a block inclusive scan of the segment sums
   const int L = (ntile + kThreads - 1) / kThreads;
   const int s0 = t * L, s1 = min(s0 + L, ntile);
@@ -628,7 +740,7 @@ __device__ float draw_range(const Params& P, const T* pr, const T* qr, const Dra
     const float tbase = sm.tile_base;
     bool clamped = sm.found == 2;
     float w[8];
-    weights8<T, VEC>(pr, qr, v0 + tile * kTile + lane * 8, V, d, P.c2, w);
+    weights8<T, VEC, MASK>(pr, qr, v0 + tile * kTile + lane * 8, V, d, P.c2, w);
     float ls = 0.0f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) ls += w[k];
@@ -897,7 +1009,7 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
       }
     }
   } else {  // kTopK
-    uint2* buf = reinterpret_cast<uint2*>(dyn) + (size_t)warp * kRowCap;
+    uint2* buf = reinterpret_cast<uint2*>(dyn + (VEC ? (size_t)kDrawStages * kDrawStageBytes : 0)) + (size_t)warp * kRowCap;
     for (int r = warp; r < nrows; r += kWarps) {
       const int rp = r <= Kb ? r : K + 1 + (r - Kb - 1);
       float M = NAN, S = NAN, thr = NAN;
@@ -919,7 +1031,7 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
         const int rp = r <= Kb ? r : K + 1 + (r - Kb - 1);
         float M, S, thr;
         int fl = 0;
-        topk_row_exact<T, VEC>(P, row_ptr<T>(P, b, rp), reinterpret_cast<uint32_t*>(dyn), sm, M, S,
+        topk_row_exact<T, VEC>(P, row_ptr<T>(P, b, rp), reinterpret_cast<uint32_t*>(dyn + (VEC ? (size_t)kDrawStages * kDrawStageBytes : 0)), sm, M, S,
                                thr, fl);
         if (t == 0) {
           sm.rowM[r] = M;
@@ -1010,16 +1122,17 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
     const float u = __ldg(P.ur + b);
     DrawRows d;
     const int rq = Kb + 1 + js;
-    d.Mp = sm.rowM[js];
-    d.invSp = 1.0f / sm.rowS[js];
-    d.Tp = sm.rowT[js];
     d.resid = js < Kb;
-    d.Mq = d.resid ? sm.rowM[rq] : 0.0f;
-    d.invSq = d.resid ? 1.0f / sm.rowS[rq] : 0.0f;
+    d.Mp2 = sm.rowM[js] * P.c2;
+    d.Lp = d.Mp2 + log2f(sm.rowS[js]);
+    d.Tp = sm.rowT[js];
+    d.Lq = d.resid ? sm.rowM[rq] * P.c2 + log2f(sm.rowS[rq]) : 0.0f;
     d.Tq = d.resid ? sm.rowT[rq] : 0.0f;
     const T* pr = prow<T>(P, b, js);
     const T* qr = d.resid ? qrow<T>(P, b, js) : pr;
-    float* wt = reinterpret_cast<float*>(dyn + (MODE == kTopK ? (size_t)kWarps * kRowCap * sizeof(uint2) : 0));
+    uint4* ring = reinterpret_cast<uint4*>(dyn);
+    float* wt = reinterpret_cast<float*>(dyn + (VEC ? (size_t)kDrawStages * kDrawStageBytes : 0) +
+                                         (MODE == kTopK ? (size_t)kWarps * kRowCap * sizeof(uint2) : 0));
     int clamp = 0;
     bool drawn = false;
     float R = 0.0f;
@@ -1032,7 +1145,7 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
         float mass = 0.0f;
         for (int w = 0; w < kWarps; ++w) {
           const float2 pc = __ldg(part + (size_t)c * kWarps + w);
-          if (pc.y != 0.0f) mass += pc.y * ex2((pc.x - d.Mp) * P.c2);
+          if (pc.y != 0.0f) mass += pc.y * ex2(pc.x * P.c2 - d.Mp2);
         }
         wt[c] = mass;
       }
@@ -1065,18 +1178,18 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
       const float tin = sm.tile_base, S = sm.total;
       __syncthreads();
       const int v0 = cs * Cfg<T>::CH;
-      const float rc = draw_range<T, VEC>(P, pr, pr, d, v0, min(P.V, v0 + Cfg<T>::CH), false, u, tin, S,
-                                          wt, sm, &clamp);
+      const float rc = draw_range<T, VEC, MODE == kTopK>(P, pr, pr, d, v0, min(P.V, v0 + Cfg<T>::CH), false, u, tin, S,
+                                          wt, ring, sm, &clamp);
       drawn = rc > 0.0f;
       R = S;
     }
-    if (!drawn) R = draw_range<T, VEC>(P, pr, qr, d, 0, P.V, true, u, 0.0f, 0.0f, wt, sm, &clamp);
+    if (!drawn) R = draw_range<T, VEC, MODE == kTopK>(P, pr, qr, d, 0, P.V, true, u, 0.0f, 0.0f, wt, ring, sm, &clamp);
     float resid_mass = d.resid ? R : 0.0f;
     if (!(R > 0.0f)) {
       // max(0, p - q) vanished through rounding: draw from p instead
       d.resid = false;
       if (t == 0) sm.flags |= SPEC_FLAG_RESIDUAL_ZERO;
-      R = draw_range<T, VEC>(P, pr, pr, d, 0, P.V, true, u, 0.0f, 0.0f, wt, sm, &clamp);
+      R = draw_range<T, VEC, MODE == kTopK>(P, pr, pr, d, 0, P.V, true, u, 0.0f, 0.0f, wt, ring, sm, &clamp);
     }
     if (clamp) atomicOr(&sm.flags, SPEC_FLAG_CDF_CLAMP);
     __syncthreads();
@@ -1435,13 +1548,14 @@ static int mode_of(float temperature, int top_k, int V) {
 static size_t stats_smem(int mode, bool vec) {
   return (vec ? (size_t)kStages * kChunkBytes : 0) + (mode == kTopK ? (size_t)kSurvCap * sizeof(uint2) : 0);
 }
-static size_t finish_smem(int mode, int V, int es) {
+static size_t finish_smem(int mode, int V, int es, bool vec) {
   const int ntile = (V + kTile - 1) / kTile;
   const int nch = (V + kChunkBytes / es - 1) / (kChunkBytes / es);
-  size_t wt = (size_t)(ntile > nch ? ntile : nch) * sizeof(float);
+  size_t bytes = (size_t)(ntile > nch ? ntile : nch) * sizeof(float);  // tile / chunk sums
   if (mode == kGreedy) return 16;
-  if (mode == kTopK) wt += (size_t)kWarps * kRowCap * sizeof(uint2);
-  return wt;
+  if (mode == kTopK) bytes += (size_t)kWarps * kRowCap * sizeof(uint2);
+  if (vec) bytes += (size_t)kDrawStages * kDrawStageBytes;  // cp.async ring of the CDF pass
+  return bytes;
 }
 
 template <typename K>
@@ -1455,7 +1569,7 @@ static cudaError_t launch_t(const Params& P, uint32_t items, cudaStream_t st) {
   const int es = (int)sizeof(T);
   auto k1 = stats_kernel<T, MODE, VEC>;
   auto k2 = finish_kernel<T, MODE, VEC>;
-  const size_t d1 = stats_smem(MODE, VEC), d2 = finish_smem(MODE, P.V, es);
+  const size_t d1 = stats_smem(MODE, VEC), d2 = finish_smem(MODE, P.V, es, VEC);
   cudaError_t e = prepare(k1, d1);
   if (e == cudaSuccess) e = prepare(k2, d2);
   int dev = 0, sms = 0, occ = 0;
