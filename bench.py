@@ -267,15 +267,20 @@ def run_gpu(args, w: W.Workload):
     nacc = torch.empty((B,), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(i):
+    def step(i, mid=None):
         c = copies[i & 1]
         sv.verify(c["p"], c["q"], c["x"], c["k"], c["ua"], c["ur"], w.temperature, w.top_k,
-                  workspace_tensor=ws, stream=stream, out=(tok, nacc))
+                  workspace_tensor=ws, stream=stream, out=(tok, nacc), pass1_event=mid)
 
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    # per step: start -> (streaming pass) -> mid -> (per-request pass) -> end, all on the launch stream
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
+    for e in ev:  # create the events before the timed region
+        for x in e:
+            x.record(stream)
+    torch.cuda.synchronize()
     gpu_id = "0"
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
@@ -289,13 +294,14 @@ def run_gpu(args, w: W.Workload):
         t_start.record(stream)
         for i in range(args.steps):
             ev[i][0].record(stream)
-            step(i)
-            ev[i][1].record(stream)
+            step(i, ev[i][1])
+            ev[i][2].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
         barrier(world)
     total_ms = t_start.elapsed_time(t_end)
-    per_launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    pass1_ms = statistics.mean(a.elapsed_time(m) for a, m, _ in ev)
+    pass2_ms = statistics.mean(m.elapsed_time(z) for _, m, z in ev)
     step_ms = max_over_ranks(total_ms / args.steps, world, dev)
     all_positions = sum_over_ranks(positions, world, dev)
     value = all_positions / (step_ms * 1e-3)
@@ -328,7 +334,7 @@ def run_gpu(args, w: W.Workload):
     if rank != 0:
         return 0
     peak, peak_kind = measured_peak()
-    achieved = logits_bytes / (per_launch_ms * 1e-3) / 1e9
+    achieved = logits_bytes / (pass1_ms * 1e-3) / 1e9  # the streaming pass reads every logit once
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
@@ -337,11 +343,13 @@ def run_gpu(args, w: W.Workload):
                    "top_k": w.top_k, "logits_bytes_per_step": logits_bytes,
                    "l2": "inputs larger than L2 (129 MB); two input copies alternate between steps",
                    "parallelism": f"{world} independent batches (no collective)"},
-        "logits_gbs": achieved,
+        "logits_gbs": logits_bytes / (step_ms * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": traffic_for(w.key if not w.greedy else "c5_greedy"),
-                     "kernel": "verify_kernel", "per_launch_ms": per_launch_ms},
+                     "kernel": "stats_kernel (streaming pass)", "per_launch_ms": pass1_ms,
+                     "step_frac": logits_bytes / (step_ms * 1e-3) / 1e9 / peak,
+                     "pass2_ms": pass2_ms},
         "gpu_launches": args.steps * (3 if ragged else 2),
         "clocks": clk.summary(),
     }

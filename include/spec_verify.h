@@ -72,7 +72,10 @@ typedef enum {
  *   residual_mass [B] float: sum_v max(0, p - q) at the first rejected position, 0 for a bonus draw;
  *   row_lognorm [B * (2*K_max + 1)] float: per row, max(z)/T + ln sum_v exp((z_v - max z)/T) over
  *       the kept set; p rows 0..K_max then q rows 0..K_max-1; NaN for rows past K_b and in greedy mode;
- *   flags [B] int32: SPEC_FLAG_* bits.
+ *   flags [B] int32: SPEC_FLAG_* bits;
+ *   pass1_done: a cudaEvent_t (host handle, cast to void*) recorded on the stream between the
+ *       streaming pass and the per-request pass, so a caller can time the two passes apart; NULL
+ *       = not recorded.  It is the one field that is not device memory.
  */
 typedef struct {
   float* p_draft;
@@ -82,6 +85,7 @@ typedef struct {
   float* residual_mass;
   float* row_lognorm;
   int32_t* flags;
+  void* pass1_done;
 } spec_verify_stats_t;
 
 /*

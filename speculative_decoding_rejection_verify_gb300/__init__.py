@@ -54,7 +54,8 @@ class SpecVerifyError(RuntimeError):
 
 class StatsStruct(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
-                ("p_draft", "q_draft", "accept_margin", "sample_margin", "residual_mass", "row_lognorm", "flags")]
+                ("p_draft", "q_draft", "accept_margin", "sample_margin", "residual_mass", "row_lognorm", "flags",
+                 "pass1_done")]
 
 
 _lib = None
@@ -148,11 +149,13 @@ def _check(t, name, shape, dtype, device):
 
 
 def verify(p, q, draft, k_per_row=None, u_accept=None, u_resample=None, temperature: float = 1.0,
-           top_k: int = 0, stats: bool = False, workspace_tensor=None, stream=None, out=None):
+           top_k: int = 0, stats: bool = False, workspace_tensor=None, stream=None, out=None,
+           pass1_event=None):
     """Run spec_verify on device tensors; returns (tokens, num_accepted, stats | None).
 
     ``out``: optional (tokens, num_accepted) tensors to write into.  ``stream``: a
-    torch.cuda.Stream (default: the current stream).  The call is asynchronous."""
+    torch.cuda.Stream (default: the current stream).  ``pass1_event``: a torch.cuda.Event
+    recorded between the streaming pass and the per-request pass.  The call is asynchronous."""
     torch = _torch()
     lib = load()
     if p.dim() != 3:
@@ -190,6 +193,11 @@ def verify(p, q, draft, k_per_row=None, u_accept=None, u_resample=None, temperat
                   residual_mass=torch.empty((B,), **f32), row_lognorm=torch.empty((B, 2 * K + 1), **f32),
                   flags=torch.empty((B,), dtype=torch.int32, device=dev))
         sp = StatsStruct(**{k: v.data_ptr() for k, v in sd.items()})
+    if pass1_event is not None:
+        if pass1_event.cuda_event == 0:  # torch creates the event on its first record
+            pass1_event.record(st)
+        sp = sp if sp is not None else StatsStruct()
+        sp.pass1_done = pass1_event.cuda_event
     nbytes = workspace_bytes(B, K, V, dt, top_k)
     ws = workspace_tensor if workspace_tensor is not None else workspace(nbytes, dev, handle)
     rc = lib.spec_verify(_ptr(p), _ptr(q), _ptr(draft), _ptr(k_per_row), _ptr(u_accept), _ptr(u_resample),

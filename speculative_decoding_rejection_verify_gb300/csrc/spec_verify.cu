@@ -41,7 +41,7 @@ constexpr int kSurvCap = 1024;           // survivors examined per chunk
 constexpr int kRowCap = 256;             // candidates >= the row's lower bound, per row
 constexpr int kMaxRows = 2 * SPEC_MAX_K + 1;
 constexpr int kUnrollA = 4;              // tiles in flight per warp in the CDF passes (scalar rows)
-constexpr int kDrawStages = 4;           // cp.async ring of the CDF pass over aligned rows
+constexpr int kDrawStages = 2;           // cp.async ring of the CDF pass over aligned rows
 constexpr int kDrawStageBytes = 16384;   // per stage: the same 8 KB span of the p row and the q row
 
 enum Mode { kSample = 0, kTopK = 1, kGreedy = 2 };
@@ -76,6 +76,7 @@ struct Params {
   float* resid_mass;
   float* lognorm;
   int32_t* flags;
+  void* pass1_done;               // optional cudaEvent_t recorded after the streaming pass
   int B, K, V, top_k, nchunk, R;  // R = padded rows per request (2K+1, or K+1 in greedy)
   float c2;                       // log2(e) / T
   float invT;                     // 1 / T
@@ -430,15 +431,22 @@ __device__ void item_topk(const Params& P, const float (&v)[Cfg<T>::PER], int n,
     }
     return;
   }
-  // exact selection among the survivors: keep those with fewer than k survivors strictly greater
+  // exact selection among the survivors: keep those with fewer than k survivors strictly greater,
+  // each written at its rank (key descending, survivor index ascending among equal keys), so the
+  // chunk's list is sorted
   uint32_t kth = 0xFFFFFFFFu;
   for (int i = t; i < ns; i += kThreads) {
     uint32_t ki = surv[i].x;
-    int greater = 0;
-    for (int j = 0; j < ns; ++j) greater += surv[j].x > ki;
+    int greater = 0, before = 0;
+    for (int j = 0; j < ns; ++j) {
+      const uint32_t kj = surv[j].x;
+      greater += kj > ki;
+      before += (kj == ki) & (j < i);
+    }
     if (greater < k) {
-      int slot = atomicAdd(&sm.nkept, 1);
-      if (slot < kCandCap) cand[slot] = surv[i];
+      atomicAdd(&sm.nkept, 1);
+      const int pos = greater + before;
+      if (pos < kCandCap) cand[pos] = surv[i];
       kth = min(kth, ki);
     }
   }
@@ -633,9 +641,11 @@ __device__ float draw_range(const Params& P, const T* pr, const T* qr, const Dra
             zq[4 * h + 3] = __uint_as_float(b.w);
           }
         }
+        if (e0 + 8 > vend) {  // the range's last, partial tile: logits past it carry no mass
 #pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8)
-          if (e0 + q8 >= vend) zp[q8] = zq[q8] = -INFINITY;  // past the range: no mass
+          for (int q8 = 0; q8 < 8; ++q8)
+            if (e0 + q8 >= vend) zp[q8] = zq[q8] = -INFINITY;
+        }
         float w[8];
         weights_of<MASK>(zp, zq, d, P.c2, w);
         float sum = 0.0f;
@@ -810,40 +820,77 @@ __device__ bool topk_row_fast(const Params& P, int b, int rp, uint2* buf, float&
   const int nch = P.nchunk;
   const uint2* meta = P.cmeta + ((size_t)b * P.R + rp) * nch;
   const uint2* cand = P.cand + ((size_t)b * P.R + rp) * nch * (size_t)kCandCap;
-  // lower bound L = the largest chunk-local k-th largest
-  uint32_t Lk = 0;
   bool ovf = false, nan = false;
   for (int c = lane; c < nch; c += 32) {
-    uint2 mt = __ldcg(meta + c);
-    Lk = max(Lk, mt.x);
+    const uint2 mt = __ldcg(meta + c);
     ovf |= (mt.y & kMetaOverflow) != 0;
     nan |= (mt.y & kMetaNaN) != 0;
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) Lk = max(Lk, __shfl_xor_sync(0xFFFFFFFFu, Lk, o));
   ovf = __any_sync(0xFFFFFFFFu, ovf);
   nan = __any_sync(0xFFFFFFFFu, nan);
   if (nan) flags |= SPEC_FLAG_NONFINITE;
   if (ovf) return false;
-  // gather candidates >= L into the warp's buffer
-  int n = 0;
-  for (int c = 0; c < nch; ++c) {
-    const int cnt = (int)(__ldcg(&meta[c].y) & kMetaCount);
-    for (int i0 = 0; i0 < cnt; i0 += 32) {
-      const int i = i0 + lane;
-      uint2 e = make_uint2(0u, 0u);
-      if (i < cnt) e = __ldcg(cand + (size_t)c * kCandCap + i);
-      const bool s = i < cnt && e.x >= Lk;
-      const unsigned bal = __ballot_sync(0xFFFFFFFFu, s);
-      const int slot = n + __popc(bal & ((1u << lane) - 1u));
-      if (s && slot < kRowCap) buf[slot] = e;
-      n += __popc(bal);
+  const int k = P.top_k;
+  // Lower bound L on the row's k-th largest: pool the m = ceil(k / nch) largest keys of every
+  // chunk (each list is sorted); the pool's k-th largest has >= k distinct logits at or above it.
+  const int m = (k + nch - 1) / nch;
+  int np = 0;
+  for (int c0 = 0; c0 < nch; c0 += 32) {
+    const int c = c0 + lane;
+    const int cnt = c < nch ? (int)(__ldcg(&meta[c].y) & kMetaCount) : 0;
+    const int take = min(m, cnt);
+    int off = take;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, off, o);
+      if (lane >= o) off += y;
     }
+    const int base = np + off - take;
+    for (int i = 0; i < take; ++i)
+      if (base + i < kRowCap) buf[base + i] = __ldcg(cand + (size_t)c * kCandCap + i);
+    np += __shfl_sync(0xFFFFFFFFu, off, 31);
+  }
+  if (np > kRowCap) return false;
+  __syncwarp();
+  uint32_t Lk = 0;
+  if (np >= k) {  // the k-th largest pooled key, by counting (ties share a rank)
+    uint32_t cand_k = 0;
+    for (int i = lane; i < np; i += 32) {
+      const uint32_t ki = buf[i].x;
+      int greater = 0;
+      for (int j = 0; j < np; ++j) greater += buf[j].x > ki;
+      if (greater < k) cand_k = cand_k == 0 ? ki : min(cand_k, ki);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, cand_k, o);
+      cand_k = cand_k == 0 ? y : (y == 0 ? cand_k : min(cand_k, y));
+    }
+    Lk = cand_k;
+  }
+  __syncwarp();
+  // gather every candidate >= L: a prefix of each chunk's sorted list
+  int n = 0;
+  for (int c0 = 0; c0 < nch; c0 += 32) {
+    const int c = c0 + lane;
+    const int cnt = c < nch ? (int)(__ldcg(&meta[c].y) & kMetaCount) : 0;
+    const uint2* lst = cand + (size_t)(c < nch ? c : 0) * kCandCap;
+    int take = 0;
+    while (take < cnt && __ldcg(&lst[take].x) >= Lk) ++take;
+    int off = take;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, off, o);
+      if (lane >= o) off += y;
+    }
+    const int base = n + off - take;
+    for (int i = 0; i < take; ++i)
+      if (base + i < kRowCap) buf[base + i] = __ldcg(lst + i);
+    n += __shfl_sync(0xFFFFFFFFu, off, 31);
   }
   if (n > kRowCap) return false;
   __syncwarp();
   // exact k-th largest among the gathered candidates
-  const int k = P.top_k;
   uint32_t kth = 0xFFFFFFFFu, mx = 0;
   for (int i = lane; i < n; i += 32) {
     uint32_t ki = buf[i].x;
@@ -1372,6 +1419,62 @@ __device__ __forceinline__ void sample_vec(const Params& P, uint4 (&raw)[Cfg<T>:
   if ((t & 31) == 0) out[t >> 5] = make_float2(M, sc);
 }
 
+// Greedy summary of one chunk straight from its packed vectors: the warp's max (on packed values,
+// NaN-propagating), then only lanes whose own max equals it look for their first element at that
+// value; the warp keeps the lowest token id.  A NaN is marked by the id -1.
+template <typename T>
+__device__ __forceinline__ void greedy_vec(uint4 (&raw)[Cfg<T>::LOADS], int n, int v0, float2* out) {
+  const int t = threadIdx.x, lane = t & 31;
+  constexpr int VW = Cfg<T>::VW;
+  if (n < Cfg<T>::CH) {  // tail chunk: vectors at or past n hold no logits
+#pragma unroll
+    for (int l = 0; l < Cfg<T>::LOADS; ++l)
+      if ((l * kThreads + t) * VW >= n)
+        raw[l] = sizeof(T) == 2 ? make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u)
+                                : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+  }
+  float m;
+  if (sizeof(T) == 2) {
+    uint32_t mx = raw[0].x;
+#pragma unroll
+    for (int l = 0; l < Cfg<T>::LOADS; ++l) {
+      if (l > 0) mx = bmax2_nan(mx, raw[l].x);
+      mx = bmax2_nan(mx, raw[l].y);
+      mx = bmax2_nan(mx, raw[l].z);
+      mx = bmax2_nan(mx, raw[l].w);
+    }
+    m = fmax_nan(bf16_lo(mx), bf16_hi(mx));
+  } else {
+    m = -INFINITY;
+#pragma unroll
+    for (int l = 0; l < Cfg<T>::LOADS; ++l) {
+      m = fmax_nan(m, __uint_as_float(raw[l].x));
+      m = fmax_nan(m, __uint_as_float(raw[l].y));
+      m = fmax_nan(m, __uint_as_float(raw[l].z));
+      m = fmax_nan(m, __uint_as_float(raw[l].w));
+    }
+  }
+  float M = m;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmax_nan(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+  int idx = 0x7FFFFFFF;
+  if (M == M && m == M) {  // this lane holds the max: its first element at that value
+#pragma unroll
+    for (int l = Cfg<T>::LOADS - 1; l >= 0; --l) {
+      const uint32_t w[4] = {raw[l].x, raw[l].y, raw[l].z, raw[l].w};
+      const int e0 = (l * kThreads + t) * VW;
+#pragma unroll
+      for (int k = VW - 1; k >= 0; --k) {
+        const float z = sizeof(T) == 2 ? (k & 1 ? bf16_hi(w[k >> 1]) : bf16_lo(w[k >> 1])) : __uint_as_float(w[k]);
+        if (z == M) idx = e0 + k;  // scanning downwards leaves the lowest index
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(0xFFFFFFFFu, idx, o));
+  if (lane == 0) out[t >> 5] = make_float2(M, __int_as_float(M == M ? v0 + idx : -1));
+}
+
 // Pass 1: stream every valid row once.  Each CTA owns a contiguous range of items
 // (request, row, chunk), so successive items walk memory in order and the cursor needs no
 // divisions; the cp.async ring keeps the next kStages - 1 chunks in flight.  No block waits for
@@ -1425,6 +1528,9 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
       if (MODE == kSample) {
         const size_t slot = ((size_t)cc.b * P.R + cc.rp) * P.nchunk + cc.c;
         sample_vec<T>(P, raw, n, P.partial + slot * kWarps);
+      } else if (MODE == kGreedy) {
+        const size_t slot = ((size_t)cc.b * P.R + cc.rp) * P.nchunk + cc.c;
+        greedy_vec<T>(raw, n, cc.c * Cfg<T>::CH, P.partial + slot * kWarps);
       } else {
         float v[Cfg<T>::PER];
         unpack<T>(raw, n, v);
@@ -1582,6 +1688,7 @@ static cudaError_t launch_t(const Params& P, uint32_t items, cudaStream_t st) {
   if (items < grid) grid = items > 0 ? items : 1;
   k1<<<grid, kThreads, d1, st>>>(P);
   e = cudaGetLastError();
+  if (e == cudaSuccess && P.pass1_done) e = cudaEventRecord(static_cast<cudaEvent_t>(P.pass1_done), st);
   if (e != cudaSuccess) return e;
   k2<<<(unsigned)P.B, kThreads, d2, st>>>(P);
   return cudaGetLastError();
@@ -1662,6 +1769,7 @@ spec_status_t spec_verify(const void* p_logits, const void* q_logits, const int3
   P.resid_mass = st.residual_mass;
   P.lognorm = st.row_lognorm;
   P.flags = st.flags;
+  P.pass1_done = st.pass1_done;
   P.B = B;
   P.K = K_max;
   P.V = V;
