@@ -37,7 +37,8 @@ constexpr int kChunkBytes = 16384;      // bytes of logits per work item (16 B p
 constexpr int kStages = 4;               // work items in flight per CTA (cp.async ring)
 constexpr int kTile = 256;               // inverse-CDF tile: 32 lanes x 8 logits
 constexpr int kCandCap = 256;            // top-k candidates stored per chunk
-constexpr int kSurvCap = 1024;           // survivors examined per chunk
+constexpr int kSegCap = 1024;            // running top-k candidates of a row segment (per buffer)
+constexpr int kSegCompact = 640;         // compact the running set once it grows past this
 constexpr int kRowCap = 256;             // candidates >= the row's lower bound, per row
 constexpr int kMaxRows = 2 * SPEC_MAX_K + 1;
 constexpr int kUnrollA = 4;              // tiles in flight per warp in the CDF passes (scalar rows)
@@ -210,10 +211,11 @@ template <typename T>
 __device__ __forceinline__ void unpack(const uint4 (&raw)[Cfg<T>::LOADS], int n, float (&v)[Cfg<T>::PER]) {
   constexpr int VW = Cfg<T>::VW;
   const int t = threadIdx.x;
+  const bool full = n >= Cfg<T>::CH;
 #pragma unroll
   for (int l = 0; l < Cfg<T>::LOADS; ++l) {
     const uint32_t w[4] = {raw[l].x, raw[l].y, raw[l].z, raw[l].w};
-    const bool ok = (l * kThreads + t) * VW < n;
+    const bool ok = full || (l * kThreads + t) * VW < n;
     if (sizeof(T) == 2) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -283,6 +285,10 @@ struct Smem {
   int nsurv;
   int nkept;
   uint32_t meta;
+  // running top-k of the row segment a block streams
+  int seg_n, seg_c0, seg_flags, seg_tight, seg_cur, seg_kept;
+  uint32_t seg_theta;
+  uint32_t hist[256];
   // finisher
   float rowM[kMaxRows];
   float rowS[kMaxRows];
@@ -359,44 +365,44 @@ __device__ __forceinline__ uint32_t warp_sort_desc(uint32_t x) {
   return x;
 }
 
-// Top-k candidates of one chunk: every logit >= the chunk's k-th largest (ties kept).  Stored as
-// (key, token) pairs plus a meta word (count | overflow | NaN) and the chunk's k-th largest key
-// (0 when the chunk holds fewer than k logits).
+// ------------------------------------------------------------------------------------------------
+// top-k in the streaming pass: a running candidate set per row segment
+// ------------------------------------------------------------------------------------------------
+// A block streams a contiguous range of items, i.e. whole rows or a row's head or tail (a
+// segment).  It keeps the segment's candidates in shared memory together with a lower bound
+// theta on the row's k-th largest logit: every logit < theta can be dropped, since k logits of the
+// row are already known to be >= theta.  After the first chunk theta is tight, so almost every
+// logit of the following chunks is settled by one compare.  At the segment's end the candidates
+// >= the segment's k-th largest (ties kept) are written, sorted, at the segment's first chunk slot.
+
+// Lower bound on a chunk's k-th largest from the per-thread maxima (whole block): in each warp with
+// data, the c_w-th largest thread maximum, c_w = min(ceil(k / warps with data), threads with data);
+// those maxima are distinct logits, so >= sum_w c_w logits are >= min_w.  Returns key 0 if that
+// count falls short of k.
 template <typename T, bool VEC>
-__device__ void item_topk(const Params& P, const float (&v)[Cfg<T>::PER], int n, int v0, uint2* cand,
-                          uint2* meta, Smem& sm, uint2* surv) {
+__device__ uint32_t chunk_bound(const float (&v)[Cfg<T>::PER], int n, int k, Smem& sm) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int k = P.top_k;
-  uint32_t key[Cfg<T>::PER];
   uint32_t tmax = 0;
-  bool nan = false;
 #pragma unroll
   for (int i = 0; i < Cfg<T>::PER; ++i) {
-    int e = elem_of<T, VEC>(i, t);
-    bool ok = e < n && v[i] == v[i];
-    nan |= (e < n) && (v[i] != v[i]);
-    key[i] = ok ? fkey(v[i]) : 0u;  // 0 = no logit (every real key is > 0)
-    tmax = max(tmax, key[i]);
+    const int e = elem_of<T, VEC>(i, t);
+    if (e < n && v[i] == v[i]) tmax = max(tmax, fkey(v[i]));
   }
-  // Lower bound theta0 on the chunk's k-th largest: in each warp with data, the c_w-th largest of
-  // its per-thread maxima, c_w = min(ceil(k / warps with data), threads with data).  Those maxima
-  // are distinct logits, so at least sum_w c_w logits are >= min_w theta_w.
-  unsigned has = __ballot_sync(0xFFFFFFFFu, tmax != 0u);
+  const unsigned has = __ballot_sync(0xFFFFFFFFu, tmax != 0u);
   if (lane == 0) sm.red_c[warp] = __popc(has);
   __syncthreads();
   int nw = 0;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) nw += sm.red_c[w] > 0;
   const int kp = (k + nw - 1) / max(nw, 1);
-  uint32_t sorted = warp_sort_desc(tmax);
-  int cw = min(kp, __popc(has));
-  uint32_t thw = cw > 0 ? __shfl_sync(0xFFFFFFFFu, sorted, cw - 1) : 0xFFFFFFFFu;
-  __syncthreads();  // red_c reads done
+  const uint32_t sorted = warp_sort_desc(tmax);
+  const int cw = min(kp, __popc(has));
+  const uint32_t thw = cw > 0 ? __shfl_sync(0xFFFFFFFFu, sorted, cw - 1) : 0xFFFFFFFFu;
+  __syncthreads();
   if (lane == 0) {
     sm.red_k[warp] = thw;
     sm.red_c[warp] = cw;
   }
-  if (t == 0) sm.nsurv = 0;
   __syncthreads();
   uint32_t theta = 0xFFFFFFFFu;
   int certified = 0;
@@ -405,62 +411,189 @@ __device__ void item_topk(const Params& P, const float (&v)[Cfg<T>::PER], int n,
     if (sm.red_c[w] > 0) theta = min(theta, sm.red_k[w]);
     certified += sm.red_c[w];
   }
-  if (kp > 32 || certified < k) theta = 1u;  // no usable bound: every logit survives
-  // survivors -> shared buffer
+  __syncthreads();
+  return (kp > 32 || certified < k) ? 0u : theta;
+}
+
+// Appends the chunk's logits >= theta (key 0: every logit) to the segment buffer.  Once theta is
+// tight almost no logit survives, so each thread first checks its own maximum and a warp only
+// walks its logits one by one when some lane may have a survivor.
+template <typename T, bool VEC>
+__device__ void seg_filter(const float (&v)[Cfg<T>::PER], int n, int v0, uint32_t theta, uint2* buf, Smem& sm) {
+  const int t = threadIdx.x, lane = t & 31;
+  const float tf = theta == 0u ? -INFINITY : keyf(theta);
+  const bool full = n >= Cfg<T>::CH;  // no logit past the row in this chunk
+  float mx = -INFINITY;
+  if (full) {
 #pragma unroll
-  for (int i = 0; i < Cfg<T>::PER; ++i) {
-    bool s = key[i] >= theta && key[i] != 0u;
-    unsigned bal = __ballot_sync(0xFFFFFFFFu, s);
-    if (bal) {
-      int base_slot = 0;
-      if (lane == 0) base_slot = atomicAdd(&sm.nsurv, __popc(bal));
-      base_slot = __shfl_sync(0xFFFFFFFFu, base_slot, 0);
-      if (s) {
-        int slot = base_slot + __popc(bal & ((1u << lane) - 1u));
-        if (slot < kSurvCap) surv[slot] = make_uint2(key[i], (uint32_t)(v0 + elem_of<T, VEC>(i, t)));
+    for (int i = 0; i < Cfg<T>::PER; ++i) mx = fmax_nan(mx, v[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < Cfg<T>::PER; ++i)
+      if (elem_of<T, VEC>(i, t) < n) mx = fmax_nan(mx, v[i]);
+  }
+  if (__any_sync(0xFFFFFFFFu, mx != mx) && lane == 0) atomicOr(&sm.seg_flags, (int)kMetaNaN);
+  if (!__any_sync(0xFFFFFFFFu, mx >= tf)) return;
+  int cnt = 0;
+  if (mx >= tf) {
+#pragma unroll
+    for (int i = 0; i < Cfg<T>::PER; ++i) cnt += (full || elem_of<T, VEC>(i, t) < n) && v[i] >= tf;
+  }
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  int base = 0;
+  if (lane == 31) base = atomicAdd(&sm.seg_n, incl);
+  base = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
+  if (cnt) {
+#pragma unroll
+    for (int i = 0; i < Cfg<T>::PER; ++i) {
+      const int e = elem_of<T, VEC>(i, t);
+      if ((full || e < n) && v[i] >= tf) {
+        if (base < kSegCap) buf[base] = make_uint2(fkey(v[i]), (uint32_t)(v0 + e));
+        ++base;
       }
     }
   }
-  bool anynan = __syncthreads_or(nan);
-  const int ns = sm.nsurv;
-  if (t == 0) sm.nkept = 0;
-  __syncthreads();
-  if (ns > kSurvCap) {
-    if (t == 0) {
-      *meta = make_uint2(0u, kMetaOverflow | (anynan ? kMetaNaN : 0u));
+}
+
+// The k-th largest key (counted with multiplicity) among src[0..n), n >= k, by radix selection on
+// 8-bit digits with a shared histogram.  Whole block.
+__device__ uint32_t seg_kth(const uint2* src, int n, int k, Smem& sm) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  uint32_t prefix = 0, mask = 0;
+  int kk = k;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    sm.hist[t] = 0;  // 256 threads, 256 bins
+    __syncthreads();
+    for (int i0 = 0; i0 < n; i0 += kThreads) {  // keys of a row share their top digits: one
+      const int i = i0 + t;                          // atomic per distinct digit per warp
+      const uint32_t key = i < n ? src[i].x : 0u;
+      const bool in = i < n && (key & mask) == prefix;
+      const uint32_t dig = in ? (key >> shift) & 255u : 256u;
+      const unsigned peers = __match_any_sync(0xFFFFFFFFu, dig);
+      if (in && (__ffs(peers) - 1) == lane) atomicAdd(&sm.hist[dig], (unsigned)__popc(peers));
     }
-    return;
-  }
-  // exact selection among the survivors: keep those with fewer than k survivors strictly greater,
-  // each written at its rank (key descending, survivor index ascending among equal keys), so the
-  // chunk's list is sorted
-  uint32_t kth = 0xFFFFFFFFu;
-  for (int i = t; i < ns; i += kThreads) {
-    uint32_t ki = surv[i].x;
-    int greater = 0, before = 0;
-    for (int j = 0; j < ns; ++j) {
-      const uint32_t kj = surv[j].x;
-      greater += kj > ki;
-      before += (kj == ki) & (j < i);
-    }
-    if (greater < k) {
-      atomicAdd(&sm.nkept, 1);
-      const int pos = greater + before;
-      if (pos < kCandCap) cand[pos] = surv[i];
-      kth = min(kth, ki);
-    }
-  }
-  // the chunk's k-th largest is the smallest kept key when the chunk holds >= k logits
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns digits 255-8l .. 248-8l (descending); find the digit where the count of keys
+      // with a larger-or-equal digit first reaches kk
+      int c8[8], s = 0;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) kth = min(kth, __shfl_xor_sync(0xFFFFFFFFu, kth, o));
-  if (lane == 0) sm.red_k[warp] = kth;
+      for (int q = 0; q < 8; ++q) {
+        c8[q] = (int)sm.hist[255 - 8 * lane - q];
+        s += c8[q];
+      }
+      int incl = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl >= kk);
+      const int hl = __ffs(hit) - 1;  // hit != 0: n >= kk keys match the prefix
+      if (lane == hl) {
+        int acc = incl - s, q = 0;
+        while (q < 7 && acc + c8[q] < kk) acc += c8[q++];
+        sm.red_c[0] = 255 - 8 * lane - q;
+        sm.red_c[1] = kk - acc;
+      }
+    }
+    __syncthreads();
+    prefix |= (uint32_t)sm.red_c[0] << shift;
+    mask |= 255u << shift;
+    kk = sm.red_c[1];
+    __syncthreads();
+  }
+  return prefix;
+}
+
+// Keeps the segment's entries >= its k-th largest (all of them when fewer than k) in the other
+// buffer; theta becomes that k-th largest.  With `sorted` the kept entries are placed by key
+// descending (buffer index ascending among equal keys).  Whole block.
+__device__ void seg_compact(int k, bool sorted, uint2* bufs, Smem& sm) {
+  const int t = threadIdx.x;
+  const int cur = sm.seg_cur;
+  const uint2* src = bufs + (size_t)cur * kSegCap;
+  uint2* dst = bufs + (size_t)(cur ^ 1) * kSegCap;
+  int n = sm.seg_n;
+  if (n > kSegCap) {  // candidates were lost: the row takes the exact path
+    if (t == 0) sm.seg_flags |= (int)kMetaOverflow;
+    n = kSegCap;
+  }
+  const uint32_t kth = n >= k ? seg_kth(src, n, k, sm) : 0u;
+  if (t == 0) sm.seg_kept = 0;
+  __syncthreads();
+  for (int i = t; i < n; i += kThreads)  // keep the entries >= kth (unordered)
+    if (src[i].x >= kth) dst[atomicAdd(&sm.seg_kept, 1)] = src[i];
+  if (sorted) {  // place the kept entries by key descending, then position, back in src
+    __syncthreads();
+    const int m = sm.seg_kept;
+    uint2* out = const_cast<uint2*>(src);
+    for (int i = t; i < m; i += kThreads) {
+      const uint32_t ki = dst[i].x, vi = dst[i].y;
+      int pos = 0;
+      for (int j = 0; j < m; ++j) {
+        const uint32_t kj = dst[j].x;
+        pos += (kj > ki) | ((kj == ki) & (dst[j].y < vi));
+      }
+      out[pos] = dst[i];
+    }
+  }
   __syncthreads();
   if (t == 0) {
-    uint32_t mk = 0xFFFFFFFFu;
-    for (int w = 0; w < kWarps; ++w) mk = min(mk, sm.red_k[w]);
-    int nk = sm.nkept;
-    uint32_t fl = (anynan ? kMetaNaN : 0u) | (nk > kCandCap ? kMetaOverflow : 0u);
-    *meta = make_uint2(ns >= k ? mk : 0u, (uint32_t)min(nk, kCandCap) | fl);
+    sm.seg_n = sm.seg_kept;
+    sm.seg_cur = sorted ? cur : cur ^ 1;
+    if (n >= k) {
+      sm.seg_theta = max(sm.seg_theta, kth);
+      sm.seg_tight = 1;
+    }
+  }
+  __syncthreads();
+}
+
+// One chunk of a top-k row in the streaming pass.
+template <typename T, bool VEC>
+__device__ void topk_chunk(const Params& P, const float (&v)[Cfg<T>::PER], int n, int b, int rp, int c,
+                           bool seg_start, bool seg_end, uint2* bufs, Smem& sm) {
+  const int k = P.top_k;
+  if (seg_start) {
+    if (threadIdx.x == 0) {
+      sm.seg_n = 0;
+      sm.seg_theta = 0;
+      sm.seg_c0 = c;
+      sm.seg_flags = 0;
+      sm.seg_tight = 0;
+      sm.seg_cur = 0;
+    }
+    __syncthreads();
+  }
+  uint32_t theta = sm.seg_theta;
+  if (!sm.seg_tight) theta = max(theta, chunk_bound<T, VEC>(v, n, k, sm));
+  const bool tight = sm.seg_tight;
+  seg_filter<T, VEC>(v, n, c * Cfg<T>::CH, theta, bufs + (size_t)sm.seg_cur * kSegCap, sm);
+  // Once theta is tight a chunk adds few candidates, so the block meets (and maybe compacts) only
+  // every 4th chunk; the buffer's headroom above kSegCompact absorbs the chunks in between.
+  if (seg_end || !tight || ((c - sm.seg_c0) & 3) == 3) {
+    __syncthreads();
+    if (seg_end || sm.seg_n > kSegCompact || (!tight && sm.seg_n >= k)) seg_compact(k, seg_end, bufs, sm);
+  }
+  const size_t row_slot = ((size_t)b * P.R + rp) * P.nchunk;
+  if (threadIdx.x == 0 && c != sm.seg_c0) P.cmeta[row_slot + c] = make_uint2(0u, 0u);
+  if (seg_end) {  // the segment's list, sorted, at its first chunk's slot
+    const int nk = sm.seg_n;
+    const uint2* src = bufs + (size_t)sm.seg_cur * kSegCap;
+    uint2* out = P.cand + (row_slot + sm.seg_c0) * kCandCap;
+    for (int i = threadIdx.x; i < min(nk, kCandCap); i += kThreads) out[i] = src[i];
+    if (threadIdx.x == 0) {
+      const uint32_t fl = (uint32_t)sm.seg_flags | (nk > kCandCap ? kMetaOverflow : 0u);
+      P.cmeta[row_slot + sm.seg_c0] = make_uint2(nk >= k ? sm.seg_theta : 0u, (uint32_t)min(nk, kCandCap) | fl);
+    }
+    __syncthreads();
   }
 }
 
@@ -1491,6 +1624,7 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
   uint2* surv = reinterpret_cast<uint2*>(dyn + (VEC ? (size_t)kStages * kChunkBytes : 0));
   Cursor cc;
   cursor_at<T>(P, lo, cc);
+  bool seg_start = true, seg_end = false;  // row segments of the top-k path
   auto summarise_f = [&](const Cursor& k, const float (&v)[Cfg<T>::PER]) {
     const int v0 = k.c * Cfg<T>::CH;
     const int n = min(Cfg<T>::CH, P.V - v0);
@@ -1500,7 +1634,7 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
     else if (MODE == kGreedy)
       item_greedy<T, VEC>(v, n, v0, P.partial + slot * kWarps);
     else
-      item_topk<T, VEC>(P, v, n, v0, P.cand + slot * kCandCap, P.cmeta + slot, sm, surv);
+      topk_chunk<T, VEC>(P, v, n, k.b, k.rp, k.c, seg_start, seg_end, surv, sm);
   };
   if (VEC) {
     Cursor ic = cc;
@@ -1524,6 +1658,7 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
         cursor_next<T>(P, ic);
       }
       cp_async_commit();
+      seg_end = it + 1 == hi || cc.c + 1 == P.nchunk;
       const int n = min(Cfg<T>::CH, P.V - cc.c * Cfg<T>::CH);
       if (MODE == kSample) {
         const size_t slot = ((size_t)cc.b * P.R + cc.rp) * P.nchunk + cc.c;
@@ -1536,6 +1671,7 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
         unpack<T>(raw, n, v);
         summarise_f(cc, v);
       }
+      seg_start = seg_end;
       cursor_next<T>(P, cc);
       s = s + 1 == kStages ? 0 : s + 1;
     }
@@ -1545,7 +1681,9 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
       const int v0 = cc.c * Cfg<T>::CH;
       float v[Cfg<T>::PER];
       load_chunk<T, VEC>(reinterpret_cast<const T*>(cc.row) + v0, min(Cfg<T>::CH, P.V - v0), v);
+      seg_end = it + 1 == hi || cc.c + 1 == P.nchunk;
       summarise_f(cc, v);
+      seg_start = seg_end;
       cursor_next<T>(P, cc);
     }
   }
@@ -1652,7 +1790,7 @@ static int mode_of(float temperature, int top_k, int V) {
 
 // dynamic shared memory of the two passes
 static size_t stats_smem(int mode, bool vec) {
-  return (vec ? (size_t)kStages * kChunkBytes : 0) + (mode == kTopK ? (size_t)kSurvCap * sizeof(uint2) : 0);
+  return (vec ? (size_t)kStages * kChunkBytes : 0) + (mode == kTopK ? (size_t)2 * kSegCap * sizeof(uint2) : 0);
 }
 static size_t finish_smem(int mode, int V, int es, bool vec) {
   const int ntile = (V + kTile - 1) / kTile;
