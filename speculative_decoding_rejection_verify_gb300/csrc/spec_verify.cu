@@ -1137,14 +1137,28 @@ template <typename T, int MODE, bool VEC>
 __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* dyn) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int K = P.K;
+  // Warp 0 starts the loads of the ratio test right away (draft tokens, uniforms, the logits at
+  // the draft tokens; rows j < K always exist in the padded layout), so they overlap the merge of
+  // the row summaries instead of following it.
+  int x = 0;
+  float zpx = -INFINITY, zqx = -INFINITY, uu = 0.0f;
+  if (warp == 0 && lane < K) {
+    x = __ldg(P.draft + (size_t)b * K + lane);
+    if (MODE != kGreedy) {
+      uu = __ldg(P.ua + (size_t)b * K + lane);
+      if (x >= 0 && x < P.V) {
+        zpx = load1<T>(prow<T>(P, b, lane) + x);
+        zqx = load1<T>(qrow<T>(P, b, lane) + x);
+      }
+    }
+  }
+  int bad_k = 0;
+  const int Kb = clamp_k(P, b, &bad_k);  // every thread reads it: no barrier needed
   if (t == 0) {
-    int bad = 0;
-    sm.Kb = clamp_k(P, b, &bad);
-    sm.flags = bad ? SPEC_FLAG_BAD_K : 0;
+    sm.Kb = Kb;
+    sm.flags = bad_k ? SPEC_FLAG_BAD_K : 0;
     sm.nonfinite = 0;
   }
-  __syncthreads();
-  const int Kb = sm.Kb;
   const int nrows = MODE == kGreedy ? Kb + 1 : 2 * Kb + 1;
   // ---- row statistics ----
   if (MODE == kSample) {
@@ -1152,6 +1166,7 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
       const int rp = r <= Kb ? r : K + 1 + (r - Kb - 1);
       const float2* part = P.partial + ((size_t)b * P.R + rp) * P.nchunk * kWarps;
       float m = -INFINITY, s = 0.0f;
+#pragma unroll 4
       for (int c = lane; c < P.nchunk * kWarps; c += 32) {
         float2 pc = __ldg(part + c);
         lse_merge(m, s, pc.x, pc.y, P.c2);
@@ -1238,11 +1253,9 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
     bool examined_bad = false;
     int jstar;
     float a = NAN, cq = NAN, am = NAN;
-    int x = 0;
     if (MODE == kGreedy) {
       bool acc = true, bad = false;
       if (lane < Kb) {
-        x = __ldg(P.draft + (size_t)b * K + lane);
         bad = x < 0 || x >= P.V;
         acc = x == sm.rowG[lane];
       }
@@ -1264,20 +1277,16 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
     } else {
       bool acc = true, bad = false;
       if (lane < Kb) {
-        x = __ldg(P.draft + (size_t)b * K + lane);
         bad = x < 0 || x >= P.V;
         a = 0.0f;
         cq = 0.0f;
         if (!bad) {
-          const float zp = load1<T>(prow<T>(P, b, lane) + x);
-          const float zq = load1<T>(qrow<T>(P, b, lane) + x);
           const int rq = Kb + 1 + lane;
-          if (zp >= sm.rowT[lane]) a = ex2((zp - sm.rowM[lane]) * P.c2) / sm.rowS[lane];
-          if (zq >= sm.rowT[rq]) cq = ex2((zq - sm.rowM[rq]) * P.c2) / sm.rowS[rq];
+          if (zpx >= sm.rowT[lane]) a = ex2((zpx - sm.rowM[lane]) * P.c2) / sm.rowS[lane];
+          if (zqx >= sm.rowT[rq]) cq = ex2((zqx - sm.rowM[rq]) * P.c2) / sm.rowS[rq];
         }
-        const float u = __ldg(P.ua + (size_t)b * K + lane);
-        acc = u * cq < a;
-        am = cq > 0.0f ? fabsf(u - a / cq) : INFINITY;
+        acc = uu * cq < a;
+        am = cq > 0.0f ? fabsf(uu - a / cq) : INFINITY;
       }
       unsigned rej = __ballot_sync(0xFFFFFFFFu, lane < Kb && !acc);
       jstar = rej ? __ffs(rej) - 1 : Kb;
