@@ -15,11 +15,16 @@
  *                                position; keep the accepted part and start drafting again
  *   gsyq.cn/news/428210    §3.2  E = 1 + a + ... + a^K: the target emits one token beyond the accepted
  *                                drafts, which is the bonus token when all K are accepted
- *   gsyq.cn/news/428210    §3.3  temperature and top-k are sampling parameters shared by draft and target
+ *   gsyq.cn/news/428210    §3.3  temperature, top-k and top-p are sampling parameters that draft and
+ *                                target must share
+ *   2kiu.com/news/5895634  §7    the draft may sample at its own, lower temperature
  *
  * Readings taken where the pages are silent (each is also listed in the design notes):
- *   - temperature divides the logits of both p and q; top-k keeps every logit >= the k-th largest
- *     (ties kept, flagged); the kept set is applied to the raw logits;
+ *   - temperature divides the logits of both p and q (q may have its own draft temperature);
+ *     top-k keeps every logit >= the k-th largest (ties kept, flagged), on the raw logits;
+ *   - top-p (nucleus) comes after temperature and top-k: it keeps the smallest set of most likely
+ *     tokens whose mass reaches top_p, every token tied with the last one included, and
+ *     renormalises; top_p >= 1 is off;
  *   - accept iff u * q(x) < p(x)  (strict; q(x) = 0 accepts iff p(x) > 0);
  *   - the inverse CDF runs in ascending token id with the strict rule u * R < C_v;
  *   - n_acc counts accepted drafts; one more token (resampled or bonus) is always emitted;
@@ -64,26 +69,44 @@ static int cmp_desc(const void* a, const void* b) {
   return (x < y) - (x > y);
 }
 
+/* (logit, token) pairs ordered by logit, descending; equal logits by token id. */
+typedef struct {
+  double z;
+  int v;
+} zv_t;
+
+static int cmp_zv_desc(const void* a, const void* b) {
+  const zv_t* x = (const zv_t*)a;
+  const zv_t* y = (const zv_t*)b;
+  if (x->z != y->z) return (x->z < y->z) - (x->z > y->z);
+  return (x->v > y->v) - (x->v < y->v);
+}
+
 /*
- * Distribution of one row (gsyq.cn §3.3: temperature and top-k).
- *   z: V logits; T > 0; top_k: 0 or >= V means no truncation.
+ * Distribution of one row (gsyq.cn §3.3: temperature, top-k and top-p; 2kiu.com §7: a draft row
+ * takes the draft's own temperature, passed here as T).
+ *   z: V logits; T > 0; top_k: 0 or >= V means no truncation; top_p in (0, 1], >= 1 means off.
  *   P_out: V doubles, the normalised probabilities.
- *   info_out (nullable): [0] m = max kept logit, [1] log-normaliser m/T + ln sum_v w_v,
- *                        [2] top-k threshold t (-inf when off), [3] kept count.
+ *   info_out (nullable, 6 doubles): [0] m = max kept logit, [1] log-normaliser m/T + ln sum_v w_v
+ *       over the kept set, [2] top-k threshold t (-inf when off), [3] kept count, [4] top-p
+ *       threshold t_p (-inf when off), [5] nucleus margin: the distance of top_p to the nearer of
+ *       the two cumulative masses around the cut (inf when off).
  * Returns OR_FLAG_NONFINITE if the row holds NaN or +inf or keeps nothing finite,
- * OR_FLAG_TOPK_TIE if ties made the kept set larger than k.
+ * OR_FLAG_TOPK_TIE if ties made the top-k set larger than k.
  */
-int oracle_row_dist(const void* z, int dtype, int V, double T, int top_k, double* P_out,
-                    double* info_out) {
+int oracle_row_dist_ex(const void* z, int dtype, int V, double T, int top_k, double top_p,
+                       double* P_out, double* info_out) {
   int flags = 0;
   double t = -INFINITY;
+  double info[6] = {NAN, NAN, NAN, NAN, -INFINITY, INFINITY};
   for (int v = 0; v < V; ++v) {
     double x = logit_at(z, dtype, (size_t)v);
     if (isnan(x) || (isinf(x) && x > 0)) flags |= OR_FLAG_NONFINITE;
   }
   if (flags) {
     for (int v = 0; v < V; ++v) P_out[v] = NAN;
-    if (info_out) info_out[0] = info_out[1] = info_out[2] = info_out[3] = NAN;
+    info[4] = info[5] = NAN;
+    if (info_out) memcpy(info_out, info, sizeof info);
     return flags;
   }
   if (top_k > 0 && top_k < V) {
@@ -104,14 +127,12 @@ int oracle_row_dist(const void* z, int dtype, int V, double T, int top_k, double
     }
   }
   if (top_k > 0 && top_k < V && kept > top_k) flags |= OR_FLAG_TOPK_TIE;
+  info[0] = m;
+  info[2] = t;
+  info[3] = kept;
   if (!(m > -INFINITY)) { /* every kept logit is -inf: nothing to sample from */
     for (int v = 0; v < V; ++v) P_out[v] = NAN;
-    if (info_out) {
-      info_out[0] = m;
-      info_out[1] = NAN;
-      info_out[2] = t;
-      info_out[3] = kept;
-    }
+    if (info_out) memcpy(info_out, info, sizeof info);
     return flags | OR_FLAG_NONFINITE;
   }
   double sum = 0.0;
@@ -122,13 +143,64 @@ int oracle_row_dist(const void* z, int dtype, int V, double T, int top_k, double
     sum += w;
   }
   for (int v = 0; v < V; ++v) P_out[v] /= sum;
-  if (info_out) {
-    info_out[0] = m;
-    info_out[1] = m / T + log(sum);
-    info_out[2] = t;
-    info_out[3] = kept;
+  info[1] = m / T + log(sum);
+
+  if (top_p < 1.0) {
+    /* Nucleus: walk the kept tokens from the most likely down (a library sort as the step),
+       one group of equal logits at a time, until the mass taken reaches top_p; the group that
+       reaches it is kept whole. */
+    zv_t* o = (zv_t*)malloc(sizeof(zv_t) * (size_t)V);
+    int n = 0;
+    for (int v = 0; v < V; ++v)
+      if (P_out[v] > 0.0) {
+        o[n].z = logit_at(z, dtype, (size_t)v);
+        o[n].v = v;
+        ++n;
+      }
+    qsort(o, (size_t)n, sizeof(zv_t), cmp_zv_desc);
+    double taken = 0.0, tp = o[n - 1].z, margin = 0.0;
+    for (int i = 0; i < n;) {
+      double g = 0.0;
+      int j = i;
+      while (j < n && o[j].z == o[i].z) g += P_out[o[j++].v];
+      if (taken + g >= top_p) {
+        tp = o[i].z;
+        margin = fmin(top_p - taken, taken + g - top_p);
+        break;
+      }
+      taken += g;
+      i = j;
+    }
+    free(o);
+    /* keep z >= t_p and renormalise; the normaliser of the kept weights follows */
+    double wsum = 0.0, mass = 0.0;
+    int nk = 0;
+    for (int v = 0; v < V; ++v) {
+      if (P_out[v] > 0.0 && logit_at(z, dtype, (size_t)v) >= tp) {
+        mass += P_out[v];
+        wsum += exp((logit_at(z, dtype, (size_t)v) - m) / T);
+        ++nk;
+      } else {
+        P_out[v] = 0.0;
+      }
+    }
+    for (int v = 0; v < V; ++v) P_out[v] /= mass;
+    info[1] = m / T + log(wsum);
+    info[3] = nk;
+    info[4] = tp;
+    info[5] = margin;
   }
+  if (info_out) memcpy(info_out, info, sizeof info);
   return flags;
+}
+
+/* The same without top-p; info_out (nullable) gets the first four entries. */
+int oracle_row_dist(const void* z, int dtype, int V, double T, int top_k, double* P_out,
+                    double* info_out) {
+  double info[6];
+  int f = oracle_row_dist_ex(z, dtype, V, T, top_k, 1.0, P_out, info);
+  if (info_out) memcpy(info_out, info, 4 * sizeof(double));
+  return f;
 }
 
 /*
@@ -257,19 +329,26 @@ static int32_t argmax_row(const void* z, int dtype, int V, int* flags) {
  * Outputs (all host, all required): out_tokens [B, K_max+1], out_n_acc [B], p_draft / q_draft /
  * accept_margin [B, K_max], sample_margin / residual_mass [B], row_lognorm [B, 2*K_max+1]
  * (p rows 0..K_max, then q rows 0..K_max-1; NaN where unused), flags [B].
+ * Sampling parameters: temperature (T_p of the target; 0 = greedy), draft_temperature (T_q of the
+ * draft rows, > 0 unless greedy, where it is not used), top_k, top_p (in (0, 1]; 1 = off).
+ * row_nucleus_margin (nullable) [B, 2*K_max+1]: each row's nucleus margin (inf when top-p is off,
+ * NaN where unused).
  * A request whose rows are non-finite gets n_acc = 0 and tokens -1 (its result is unspecified).
  * nthreads > 1 runs requests in parallel (OpenMP); the result does not depend on it.
  */
-int oracle_verify(const void* p, const void* q, const int32_t* draft, const int32_t* k_per_row,
-                  const float* ua, const float* ur, float temperature, int top_k, int32_t* out_tokens,
-                  int32_t* out_n_acc, double* p_draft, double* q_draft, double* accept_margin,
-                  double* sample_margin, double* residual_mass, double* row_lognorm,
-                  int32_t* out_flags, int B, int K_max, int V, int dtype, int nthreads) {
+int oracle_verify_ex(const void* p, const void* q, const int32_t* draft, const int32_t* k_per_row,
+                     const float* ua, const float* ur, float temperature, float draft_temperature,
+                     int top_k, float top_p, int32_t* out_tokens, int32_t* out_n_acc, double* p_draft,
+                     double* q_draft, double* accept_margin, double* sample_margin,
+                     double* residual_mass, double* row_lognorm, double* row_nucleus_margin,
+                     int32_t* out_flags, int B, int K_max, int V, int dtype, int nthreads) {
   if (B < 0 || K_max < 0 || K_max > 64 || V <= 0 || !(temperature >= 0.0f) || top_k < 0) return 1;
+  if (temperature > 0.0f && !(draft_temperature > 0.0f)) return 1;
+  if (!(top_p > 0.0f)) return 1;
   if (nthreads < 1) nthreads = 1;
   const int rows_lognorm = 2 * K_max + 1;
   const size_t es = dtype == OR_DTYPE_F32 ? 4 : 2;
-  const double T = (double)temperature;
+  const double T = (double)temperature, Tq = (double)draft_temperature, tp = (double)top_p;
 
 #pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
   for (int b = 0; b < B; ++b) {
@@ -290,7 +369,10 @@ int oracle_verify(const void* p, const void* q, const int32_t* draft, const int3
     double* ln = row_lognorm + (size_t)b * rows_lognorm;
     for (int j = 0; j <= K_max; ++j) tok[j] = -1;
     for (int j = 0; j < K_max; ++j) pd[j] = qd[j] = am[j] = NAN;
+    double* nm = row_nucleus_margin ? row_nucleus_margin + (size_t)b * rows_lognorm : NULL;
     for (int r = 0; r < rows_lognorm; ++r) ln[r] = NAN;
+    if (nm)
+      for (int r = 0; r < rows_lognorm; ++r) nm[r] = NAN;
     sample_margin[b] = NAN;
     residual_mass[b] = NAN;
 
@@ -330,14 +412,16 @@ int oracle_verify(const void* p, const void* q, const int32_t* draft, const int3
     double* Pr = (double*)malloc(sizeof(double) * (size_t)(K + 1) * V);
     double* Qr = (double*)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1) * V);
     double* work = (double*)malloc(sizeof(double) * (size_t)V);
-    double info[4];
+    double info[6];
     for (int j = 0; j <= K; ++j) {
-      flags |= oracle_row_dist(pb + (size_t)j * V * es, dtype, V, T, top_k, Pr + (size_t)j * V, info);
+      flags |= oracle_row_dist_ex(pb + (size_t)j * V * es, dtype, V, T, top_k, tp, Pr + (size_t)j * V, info);
       ln[j] = info[1];
+      if (nm) nm[j] = info[5];
     }
     for (int j = 0; j < K; ++j) {
-      flags |= oracle_row_dist(qb + (size_t)j * V * es, dtype, V, T, top_k, Qr + (size_t)j * V, info);
+      flags |= oracle_row_dist_ex(qb + (size_t)j * V * es, dtype, V, Tq, top_k, tp, Qr + (size_t)j * V, info);
       ln[K_max + 1 + j] = info[1];
+      if (nm) nm[K_max + 1 + j] = info[5];
     }
     int32_t n = 0;
     if (flags & OR_FLAG_NONFINITE) {
@@ -353,6 +437,17 @@ int oracle_verify(const void* p, const void* q, const int32_t* draft, const int3
     free(work);
   }
   return 0;
+}
+
+/* The verify step with one temperature for both sides and no top-p. */
+int oracle_verify(const void* p, const void* q, const int32_t* draft, const int32_t* k_per_row,
+                  const float* ua, const float* ur, float temperature, int top_k, int32_t* out_tokens,
+                  int32_t* out_n_acc, double* p_draft, double* q_draft, double* accept_margin,
+                  double* sample_margin, double* residual_mass, double* row_lognorm,
+                  int32_t* out_flags, int B, int K_max, int V, int dtype, int nthreads) {
+  return oracle_verify_ex(p, q, draft, k_per_row, ua, ur, temperature, temperature, top_k, 1.0f,
+                          out_tokens, out_n_acc, p_draft, q_draft, accept_margin, sample_margin,
+                          residual_mass, row_lognorm, NULL, out_flags, B, K_max, V, dtype, nthreads);
 }
 
 /*
