@@ -167,7 +167,11 @@ def traffic_for(workload_key: str):
 def describe(w: W.Workload) -> str:
     kk = f"K_b~U{{{w.ragged[0]}..{w.ragged[1]}}}" if w.ragged else f"K={w.K}"
     extra = " greedy" if w.temperature == 0 else f" T={w.temperature:g}" + (f" top_k={w.top_k}" if w.top_k else "")
-    return f"{w.key if not w.greedy else 'c5_greedy'}: B={w.B} {kk} V={w.V} {w.dtype}{extra}" + \
+    if w.temperature and w.tq != w.temperature:
+        extra += f" T_q={w.tq:g}"
+    if w.temperature and w.top_p < 1.0:
+        extra += f" top_p={w.top_p:g}"
+    return f"{w.label}: B={w.B} {kk} V={w.V} {w.dtype}{extra}" + \
         (f" alpha~{w.alpha:g}" if w.alpha is not None and not w.greedy else "")
 
 
@@ -183,7 +187,7 @@ def cpu_baseline(w: W.Workload, budget_requests: int, seconds: float = 10.0):
     t0 = time.perf_counter()
     while True:
         oracle.verify(d["p"], None if w.temperature == 0 else d["q"], d["draft"], kpr, d["ua"], d["ur"],
-                      w.temperature, w.top_k, nthreads=cores)
+                      w.temperature, w.top_k, nthreads=cores, draft_temperature=w.tq, top_p=w.top_p)
         calls += 1
         dt = time.perf_counter() - t0
         if dt >= seconds:
@@ -210,7 +214,7 @@ def run_reference(args, w: W.Workload):
     probe = W.generate(w, requests=range(min(8, w.B)))
     t0 = time.perf_counter()
     oracle.verify(probe["p"], q_of(probe), probe["draft"], kpr_of(probe), probe["ua"], probe["ur"], w.temperature,
-                  w.top_k, nthreads=cores)
+                  w.top_k, nthreads=cores, draft_temperature=w.tq, top_p=w.top_p)
     per_req = (time.perf_counter() - t0) / probe["p"].shape[0]
     budget = args.ref_seconds / max(1, args.steps + args.warmup)
     n = int(max(1, min(args.ref_requests, w.B, budget / max(per_req, 1e-9))))
@@ -218,7 +222,7 @@ def run_reference(args, w: W.Workload):
 
     def one():
         oracle.verify(d["p"], q_of(d), d["draft"], kpr_of(d), d["ua"], d["ur"], w.temperature, w.top_k,
-                      nthreads=cores)
+                      nthreads=cores, draft_temperature=w.tq, top_p=w.top_p)
 
     for _ in range(args.warmup):
         one()
@@ -280,7 +284,8 @@ def run_gpu(args, w: W.Workload):
     def launch(i, st, mid=None):
         c = copies[i & 1]
         sv.verify(c["p"], c["q"], c["x"], c["k"], c["ua"], c["ur"], w.temperature, w.top_k,
-                  workspace_tensor=ws, stream=st, out=(tok, nacc), pass1_event=mid)
+                  workspace_tensor=ws, stream=st, out=(tok, nacc), pass1_event=mid,
+                  draft_temperature=w.tq, top_p=w.top_p)
 
     graphs = None
     if args.graph:
@@ -349,7 +354,7 @@ def run_gpu(args, w: W.Workload):
 
         def hstep():
             sv.verify_host(hp["p"], hp["q"], hp["x"], hp["k"], hp["ua"], hp["ur"], w.temperature, w.top_k,
-                           device=dev, stream=stream, out=(htok, hn))
+                           device=dev, stream=stream, out=(htok, hn), draft_temperature=w.tq, top_p=w.top_p)
 
         for _ in range(2):
             hstep()
@@ -378,13 +383,14 @@ def run_gpu(args, w: W.Workload):
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded generator; no dataset)",
         "config": {"workload": describe(w), "B_per_gpu": B, "K": K, "V": V, "temperature": w.temperature,
-                   "top_k": w.top_k, "logits_bytes_per_step": logits_bytes,
+                   "draft_temperature": w.tq, "top_k": w.top_k, "top_p": w.top_p,
+                   "logits_bytes_per_step": logits_bytes,
                    "l2": l2_note, "launch": "CUDA graph replay" if graphs else "direct launches",
                    "parallelism": f"{world} independent batches (no collective)"},
         "logits_gbs": logits_bytes / (step_ms * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
-                     "traffic": traffic_for(w.key if not w.greedy else "c5_greedy"),
+                     "traffic": traffic_for(w.label),
                      "kernel": "stats_kernel (streaming pass)" if graphs is None else "whole step (graph replay)",
                      "per_launch_ms": pass1_ms,
                      "step_frac": logits_bytes / (step_ms * 1e-3) / 1e9 / peak,

@@ -10,7 +10,8 @@
  *   - gsyq.cn/news/428210 §3.2 and 2kiu.com/news/5895634 §3.1: one target forward yields
  *     1 + a + ... + a^K tokens on average, i.e. when every draft is accepted one more token is
  *     drawn from p at position K (the bonus token);
- *   - gsyq.cn/news/428210 §3.3: temperature and top-k are shared sampling parameters of both sides.
+ *   - gsyq.cn/news/428210 §3.3: temperature, top-k and top-p are shared sampling parameters of
+ *     both sides; 2kiu.com/news/5895634 §7: the draft may sample at its own temperature.
  * Readings where the pages are silent: temperature divides both logit sets; top-k keeps every
  * logit >= the k-th largest (ties kept and flagged); accept iff u * q(x) < p(x); the inverse CDF
  * runs in ascending token id with the strict rule u * R < C_v; temperature 0 is the greedy limit
@@ -126,6 +127,42 @@ spec_status_t spec_verify(const void* p_logits, const void* q_logits, const int3
                           size_t workspace_bytes, void* stream);
 
 /*
+ * Sampling parameters of spec_verify_ex.
+ *   temperature        T of the target rows: > 0, or 0 for greedy argmax-match (then the other
+ *                      fields are not used);
+ *   draft_temperature  T_q the draft sampled its tokens with (2kiu.com/news/5895634 §7: the draft
+ *                      may run cooler than the target); > 0; the q rows are divided by it;
+ *   top_k              as for spec_verify (0 or >= V = off, else <= SPEC_MAX_TOPK);
+ *   top_p              nucleus mass in (0, 1]; >= 1 = off (gsyq.cn/news/428210 §3.3 names top_p
+ *                      among the parameters draft and target must share).  After temperature and
+ *                      top-k, every row keeps the smallest set of most likely tokens whose mass
+ *                      reaches top_p, with every token tied with the last one, and is
+ *                      renormalised.  The cut compares fp32 sums with top_p: where the cumulative
+ *                      mass lies within ~1e-6 of top_p the kept set may differ from an exact one.
+ */
+typedef struct {
+  float temperature;
+  float draft_temperature;
+  int32_t top_k;
+  float top_p;
+} spec_sampling_t;
+
+/*
+ * spec_verify with the sampling parameters of spec_sampling_t (all other arguments, the
+ * workspace size and the results as for spec_verify; `sampling` is a host pointer read before
+ * the call returns).  spec_verify(..., T, top_k, ...) is spec_verify_ex with {T, T, top_k, 1}.
+ * With top_p < 1 the per-request pass also reads every valid row once or more (two levels for
+ * bf16, four for f32, the later ones mostly from L2) to find each row's nucleus.
+ * Returns SPEC_ERR_INVALID_ARG for sampling == NULL, T_q <= 0 with T > 0, or top_p <= 0 / NaN.
+ */
+spec_status_t spec_verify_ex(const void* p_logits, const void* q_logits, const int32_t* draft_tokens,
+                             const int32_t* k_per_row, const float* u_accept, const float* u_resample,
+                             const spec_sampling_t* sampling, int32_t* out_tokens,
+                             int32_t* out_num_accepted, const spec_verify_stats_t* out_stats, int32_t B,
+                             int32_t K_max, int32_t V, spec_dtype_t dtype, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/*
  * Device bytes spec_verify_host needs as staging for these sizes (inputs, outputs and the
  * spec_verify workspace, each 256-B aligned), or 0 for invalid sizes.
  */
@@ -146,6 +183,17 @@ spec_status_t spec_verify_host(const void* p_logits, const void* q_logits,
                                int32_t top_k, int32_t* out_tokens, int32_t* out_num_accepted,
                                int32_t B, int32_t K_max, int32_t V, spec_dtype_t dtype,
                                void* staging, size_t staging_bytes, void* stream);
+
+/*
+ * spec_verify_host with the sampling parameters of spec_sampling_t (staging size as for
+ * spec_verify_host; spec_verify_host(..., T, top_k, ...) is this call with {T, T, top_k, 1}).
+ */
+spec_status_t spec_verify_host_ex(const void* p_logits, const void* q_logits,
+                                  const int32_t* draft_tokens, const int32_t* k_per_row,
+                                  const float* u_accept, const float* u_resample,
+                                  const spec_sampling_t* sampling, int32_t* out_tokens,
+                                  int32_t* out_num_accepted, int32_t B, int32_t K_max, int32_t V,
+                                  spec_dtype_t dtype, void* staging, size_t staging_bytes, void* stream);
 
 /* Size of the fixed device array behind spec_verify_static (16 MiB). */
 #define SPEC_STATIC_SCRATCH_BYTES (16u << 20)

@@ -90,7 +90,8 @@ static int cmp_zv_desc(const void* a, const void* b) {
  *   info_out (nullable, 6 doubles): [0] m = max kept logit, [1] log-normaliser m/T + ln sum_v w_v
  *       over the kept set, [2] top-k threshold t (-inf when off), [3] kept count, [4] top-p
  *       threshold t_p (-inf when off), [5] nucleus margin: the distance of top_p to the nearer of
- *       the two cumulative masses around the cut (inf when off).
+ *       the two cumulative masses around the cut, the mass before the first group (exactly 0)
+ *       left out (inf when off).
  * Returns OR_FLAG_NONFINITE if the row holds NaN or +inf or keeps nothing finite,
  * OR_FLAG_TOPK_TIE if ties made the top-k set larger than k.
  */
@@ -165,7 +166,8 @@ int oracle_row_dist_ex(const void* z, int dtype, int V, double T, int top_k, dou
       while (j < n && o[j].z == o[i].z) g += P_out[o[j++].v];
       if (taken + g >= top_p) {
         tp = o[i].z;
-        margin = fmin(top_p - taken, taken + g - top_p);
+        /* before the first group the mass taken is exactly 0: only the far side can move */
+        margin = taken > 0.0 ? fmin(top_p - taken, taken + g - top_p) : taken + g - top_p;
         break;
       }
       taken += g;

@@ -30,8 +30,8 @@ def mean_alpha(w: W.Workload, tau: float, requests: int) -> float:
     vals = []
     for i in range(d["p"].shape[0]):
         for j in range(int(d["k_per_row"][i])):
-            P, _, fp = oracle.row_dist(d["p"][i, j], w.temperature, w.top_k)
-            Q, _, fq = oracle.row_dist(d["q"][i, j], w.temperature, w.top_k)
+            P, _, fp = oracle.row_dist(d["p"][i, j], w.temperature, w.top_k, w.top_p)
+            Q, _, fq = oracle.row_dist(d["q"][i, j], w.tq, w.top_k, w.top_p)
             assert not (fp | fq) & oracle.FLAG_NONFINITE
             vals.append(np.minimum(P, Q).sum())
     return float(np.mean(vals))

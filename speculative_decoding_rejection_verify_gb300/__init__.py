@@ -6,14 +6,15 @@ no CPU fallback: without the compiled library every call raises.
 
 The C ABI is declared in ``include/spec_verify.h``; the names here mirror it:
 
-* ``verify(p, q, draft, k_per_row, u_accept, u_resample, temperature, top_k, stats=False)``
-  -> ``(tokens [B, K+1] int32, num_accepted [B] int32, stats dict | None)`` on device tensors;
-* ``verify_host(...)`` the same on host (numpy / CPU torch) arrays through ``spec_verify_host``;
+* ``verify(p, q, draft, k_per_row, u_accept, u_resample, temperature, top_k, stats=False,
+  draft_temperature=None, top_p=1.0)`` -> ``(tokens [B, K+1] int32, num_accepted [B] int32,
+  stats dict | None)`` on device tensors, through ``spec_verify_ex``;
+* ``verify_host(...)`` the same on host (numpy / CPU torch) arrays through ``spec_verify_host_ex``;
 * ``workspace_bytes(B, K, V, dtype, top_k)``.
 
 Logits are ``torch.float32`` or ``torch.bfloat16`` tensors ``p [B, K+1, V]`` and ``q [B, K, V]``
 (q may be None at temperature 0).  The verify rule (cf-1.com/news/5155685 §2.2,
-2kiu.com/news/5895634 §2.2, gsyq.cn/news/428210 §3.1-§3.3) is restated in the header.
+2kiu.com/news/5895634 §2.2 and §7, gsyq.cn/news/428210 §3.1-§3.3) is restated in the header.
 """
 from __future__ import annotations
 
@@ -41,8 +42,8 @@ MAX_K = 16
 MAX_V = 2097152
 MAX_TOPK = 256
 
-EXPORTS = ("spec_verify_workspace_bytes", "spec_verify", "spec_verify_host_staging_bytes",
-           "spec_verify_host", "spec_verify_static", "spec_verify_status_string")
+EXPORTS = ("spec_verify_workspace_bytes", "spec_verify", "spec_verify_ex", "spec_verify_host_staging_bytes",
+           "spec_verify_host", "spec_verify_host_ex", "spec_verify_static", "spec_verify_status_string")
 STATIC_SCRATCH_BYTES = 16 << 20
 
 
@@ -56,6 +57,16 @@ class StatsStruct(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("p_draft", "q_draft", "accept_margin", "sample_margin", "residual_mass", "row_lognorm", "flags",
                  "pass1_done")]
+
+
+class SamplingStruct(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_float), ("draft_temperature", ctypes.c_float),
+                ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float)]
+
+
+def _sampling(temperature, draft_temperature, top_k, top_p) -> SamplingStruct:
+    tq = temperature if draft_temperature is None else draft_temperature
+    return SamplingStruct(float(temperature), float(tq), int(top_k), float(top_p))
 
 
 _lib = None
@@ -85,10 +96,16 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
             lib.spec_verify.argtypes = [P, P, P, P, P, P, F, I, P, P, ctypes.POINTER(StatsStruct),
                                         I, I, I, I, P, Z, P]
             lib.spec_verify.restype = I
+            lib.spec_verify_ex.argtypes = [P, P, P, P, P, P, ctypes.POINTER(SamplingStruct), P, P,
+                                           ctypes.POINTER(StatsStruct), I, I, I, I, P, Z, P]
+            lib.spec_verify_ex.restype = I
             lib.spec_verify_host_staging_bytes.argtypes = [I, I, I, I, I, I]
             lib.spec_verify_host_staging_bytes.restype = Z
             lib.spec_verify_host.argtypes = [P, P, P, P, P, P, F, I, P, P, I, I, I, I, P, Z, P]
             lib.spec_verify_host.restype = I
+            lib.spec_verify_host_ex.argtypes = [P, P, P, P, P, P, ctypes.POINTER(SamplingStruct), P, P, I, I, I, I,
+                                                P, Z, P]
+            lib.spec_verify_host_ex.restype = I
             lib.spec_verify_static.argtypes = [P, P, P, P, P, P, F, I, P, P, ctypes.POINTER(StatsStruct),
                                                I, I, I, I, P]
             lib.spec_verify_static.restype = I
@@ -150,10 +167,11 @@ def _check(t, name, shape, dtype, device):
 
 def verify(p, q, draft, k_per_row=None, u_accept=None, u_resample=None, temperature: float = 1.0,
            top_k: int = 0, stats: bool = False, workspace_tensor=None, stream=None, out=None,
-           pass1_event=None):
-    """Run spec_verify on device tensors; returns (tokens, num_accepted, stats | None).
+           pass1_event=None, draft_temperature: Optional[float] = None, top_p: float = 1.0):
+    """Run spec_verify_ex on device tensors; returns (tokens, num_accepted, stats | None).
 
-    ``out``: optional (tokens, num_accepted) tensors to write into.  ``stream``: a
+    ``draft_temperature``: T_q of the q rows (None = ``temperature``); ``top_p``: nucleus mass
+    (1 = off).  ``out``: optional (tokens, num_accepted) tensors to write into.  ``stream``: a
     torch.cuda.Stream (default: the current stream).  ``pass1_event``: a torch.cuda.Event
     recorded between the streaming pass and the per-request pass.  The call is asynchronous."""
     torch = _torch()
@@ -200,12 +218,13 @@ def verify(p, q, draft, k_per_row=None, u_accept=None, u_resample=None, temperat
         sp.pass1_done = pass1_event.cuda_event
     nbytes = workspace_bytes(B, K, V, dt, top_k)
     ws = workspace_tensor if workspace_tensor is not None else workspace(nbytes, dev, handle)
-    rc = lib.spec_verify(_ptr(p), _ptr(q), _ptr(draft), _ptr(k_per_row), _ptr(u_accept), _ptr(u_resample),
-                         float(temperature), int(top_k), tokens.data_ptr(), nacc.data_ptr(),
-                         ctypes.byref(sp) if sp is not None else None, B, K, V, dt, ws.data_ptr(),
-                         ws.numel(), handle)
+    smp = _sampling(temperature, draft_temperature, top_k, top_p)
+    rc = lib.spec_verify_ex(_ptr(p), _ptr(q), _ptr(draft), _ptr(k_per_row), _ptr(u_accept), _ptr(u_resample),
+                            ctypes.byref(smp), tokens.data_ptr(), nacc.data_ptr(),
+                            ctypes.byref(sp) if sp is not None else None, B, K, V, dt, ws.data_ptr(),
+                            ws.numel(), handle)
     if rc != SPEC_OK:
-        raise SpecVerifyError(rc, "spec_verify")
+        raise SpecVerifyError(rc, "spec_verify_ex")
     return tokens, nacc, sd
 
 
@@ -220,7 +239,8 @@ def staging_bytes(B: int, K: int, V: int, dtype: int, top_k: int, ragged: bool) 
 
 
 def verify_host(p, q, draft, k_per_row=None, u_accept=None, u_resample=None, temperature: float = 1.0,
-                top_k: int = 0, staging=None, device=None, stream=None, out=None):
+                top_k: int = 0, staging=None, device=None, stream=None, out=None,
+                draft_temperature: Optional[float] = None, top_p: float = 1.0):
     """spec_verify_host on host arrays (numpy, or CPU torch tensors; pinned memory recommended).
 
     ``p``/``q``: float32 arrays or bf16 bits as uint16 (numpy) / torch.bfloat16 (CPU tensors).
@@ -270,8 +290,9 @@ def verify_host(p, q, draft, k_per_row=None, u_accept=None, u_resample=None, tem
         tp, npp = (tokens.ctypes.data, nacc.ctypes.data) if isinstance(tokens, np.ndarray) else \
             (tokens.data_ptr(), nacc.data_ptr())
     st = stream if stream is not None else torch.cuda.current_stream(dev)
-    rc = lib.spec_verify_host(pp, qp, dp, kp, ap, rp, float(temperature), int(top_k), tp, npp, B, K, V, dt,
-                              staging.data_ptr(), staging.numel(), st.cuda_stream)
+    smp = _sampling(temperature, draft_temperature, top_k, top_p)
+    rc = lib.spec_verify_host_ex(pp, qp, dp, kp, ap, rp, ctypes.byref(smp), tp, npp, B, K, V, dt,
+                                 staging.data_ptr(), staging.numel(), st.cuda_stream)
     if rc != SPEC_OK:
-        raise SpecVerifyError(rc, "spec_verify_host")
+        raise SpecVerifyError(rc, "spec_verify_host_ex")
     return tokens, nacc

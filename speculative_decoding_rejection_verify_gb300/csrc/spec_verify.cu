@@ -79,11 +79,15 @@ struct Params {
   int32_t* flags;
   void* pass1_done;               // optional cudaEvent_t recorded after the streaming pass
   int B, K, V, top_k, nchunk, R;  // R = padded rows per request (2K+1, or K+1 in greedy)
-  float c2;                       // log2(e) / T
+  float c2;                       // log2(e) / T of the target rows
   float invT;                     // 1 / T
+  float c2q;                      // log2(e) / T_q of the draft rows (T_q = T unless set apart)
+  float invTq;                    // 1 / T_q
+  float top_p;                    // nucleus mass of every row; >= 1 = off
   float2* partial;                // [B, R, nchunk, warps] (max, sum) or (max, argmax) per warp
   uint2* cmeta;                   // [B, R, nchunk] top-k: (k-th largest key of the chunk, count|flags)
   uint2* cand;                    // [B, R, nchunk, kCandCap] top-k: (key, token)
+  float2* rowstat;                // [B, R] top-p, sampling mode: (kept mass, cut) of each row
   const uint32_t* rowmap;         // ragged: [rows] (b << 6 | padded row); null = uniform layout
   const uint32_t* total_rows;     // ragged: number of valid rows
   uint32_t uniform_items;         // uniform layout: B * R * nchunk
@@ -301,6 +305,14 @@ struct Smem {
   float incl[kThreads];
   int y;
   float margin;
+  int nuc_digit;     // nucleus search: the bin of the cut at the current level
+  float nuc_above;   // mass of the bins above it
+  float nuc_bin;     // mass of the bin itself
+  uint32_t nuc_count;  // logits in it
+  float nuc_target;  // top_p * the row's kept mass
+  int nuc_n;         // logits gathered
+  uint32_t nuc_key;  // key of the cut
+  uint32_t red_cnt[32];
 };
 
 // ------------------------------------------------------------------------------------------------
@@ -309,16 +321,16 @@ struct Smem {
 // Sampling: each warp summarises its share of the chunk as (max, sum of 2^((z - max) * c2)) and
 // writes it to out[warp]; the request's tail merges the warps' and chunks' pairs per row.
 template <typename T>
-__device__ __forceinline__ void item_sample(const Params& P, const float (&v)[Cfg<T>::PER], float2* out) {
+__device__ __forceinline__ void item_sample(float c2, const float (&v)[Cfg<T>::PER], float2* out) {
   float m = -INFINITY;
 #pragma unroll
   for (int i = 0; i < Cfg<T>::PER; ++i) m = fmax_nan(m, v[i]);
   float s = 0.0f;
   if (m != -INFINITY) {
 #pragma unroll
-    for (int i = 0; i < Cfg<T>::PER; ++i) s += ex2((v[i] - m) * P.c2);
+    for (int i = 0; i < Cfg<T>::PER; ++i) s += ex2((v[i] - m) * c2);
   }
-  lse_warp(m, s, P.c2);
+  lse_warp(m, s, c2);
   if ((threadIdx.x & 31) == 0) out[threadIdx.x >> 5] = make_float2(m, s);
 }
 
@@ -642,15 +654,17 @@ __device__ __forceinline__ void load8(const T* __restrict__ row, int e0, int V, 
 // Weights of the inverse-CDF draw for 8 logits: the residual max(0, P - Q) when `resid`, else the
 // (unnormalised) target weights exp((z_p - M_p)/T) on the kept set.
 struct DrawRows {
-  float Lp, Tp;  // target row: log2 normaliser (max * c2 + log2 sum), top-k threshold
+  float Lp, Tp;  // target row: log2 normaliser (max * c2 + log2 sum), truncation threshold
   float Lq, Tq;  // draft row
   float Mp2;     // target row max * c2 (scale of the weights of a draw from p alone)
+  float c2q;     // the draft row's scale log2(e) / T_q
   bool resid;
 };
 
 // Weights of the inverse-CDF draw for 8 logits: the residual max(0, P - Q) with
-// P = 2^(z_p * c2 - Lp), Q = 2^(z_q * c2 - Lq) when `resid`, else the target weights
-// 2^(z_p * c2 - Mp2) relative to the row max.  Logits below a top-k threshold weigh 0 (MASK).
+// P = 2^(z_p * c2 - Lp), Q = 2^(z_q * c2q - Lq) when `resid`, else the target weights
+// 2^(z_p * c2 - Mp2) relative to the row max.  Logits below a row's truncation threshold
+// (top-k and / or top-p) weigh 0 (MASK).
 // Both passes of a draw compute them with these same instructions, so they agree bit for bit.
 template <bool MASK>
 __device__ __forceinline__ void weights_of(const float (&zp)[8], const float (&zq)[8], const DrawRows& d,
@@ -658,10 +672,11 @@ __device__ __forceinline__ void weights_of(const float (&zp)[8], const float (&z
   const float2 cc = make_float2(c2, c2);
   if (d.resid) {
     const float2 nlp = make_float2(-d.Lp, -d.Lp), nlq = make_float2(-d.Lq, -d.Lq);
+    const float2 ccq = make_float2(d.c2q, d.c2q);
 #pragma unroll
     for (int k = 0; k < 8; k += 2) {
       const float2 a = __ffma2_rn(make_float2(zp[k], zp[k + 1]), cc, nlp);
-      const float2 b = __ffma2_rn(make_float2(zq[k], zq[k + 1]), cc, nlq);
+      const float2 b = __ffma2_rn(make_float2(zq[k], zq[k + 1]), ccq, nlq);
       float pa = ex2(a.x), pb = ex2(a.y), qa = ex2(b.x), qb = ex2(b.y);
       if (MASK) {
         pa = zp[k] >= d.Tp ? pa : 0.0f;
@@ -949,6 +964,7 @@ __device__ float draw_range(const Params& P, const T* pr, const T* qr, const Dra
 template <typename T>
 __device__ bool topk_row_fast(const Params& P, int b, int rp, uint2* buf, float& M, float& S,
                               float& thr, int& flags) {
+  const float c2 = rp > P.K ? P.c2q : P.c2;
   const int lane = threadIdx.x & 31;
   const int nch = P.nchunk;
   const uint2* meta = P.cmeta + ((size_t)b * P.R + rp) * nch;
@@ -1044,7 +1060,7 @@ __device__ bool topk_row_fast(const Params& P, int b, int rp, uint2* buf, float&
   int kept = 0;
   for (int i = lane; i < n; i += 32) {
     if (buf[i].x >= kth) {
-      s += ex2((keyf(buf[i].x) - M) * P.c2);
+      s += ex2((keyf(buf[i].x) - M) * c2);
       ++kept;
     }
   }
@@ -1057,8 +1073,8 @@ __device__ bool topk_row_fast(const Params& P, int b, int rp, uint2* buf, float&
 
 // Exact top-k statistics of a whole row by radix selection over the row (whole CTA).
 template <typename T, bool VEC>
-__device__ void topk_row_exact(const Params& P, const T* row, uint32_t* hist, Smem& sm, float& M,
-                               float& S, float& thr, int& flags) {
+__device__ void topk_row_exact(const Params& P, const T* row, float c2, uint32_t* hist, Smem& sm,
+                               float& M, float& S, float& thr, int& flags) {
   const int t = threadIdx.x;
   const int V = P.V, k = P.top_k;
   uint32_t prefix = 0, mask = 0;
@@ -1107,7 +1123,7 @@ __device__ void topk_row_exact(const Params& P, const T* row, uint32_t* hist, Sm
   for (int e = t; e < V; e += kThreads) {
     float z = load1<T>(row + e);
     if (z >= thr) {
-      s += ex2((z - m) * P.c2);
+      s += ex2((z - m) * c2);
       ++kept;
     }
   }
@@ -1132,9 +1148,255 @@ __device__ void topk_row_exact(const Params& P, const T* row, uint32_t* hist, Sm
   __syncthreads();
 }
 
+// Nucleus (top-p) of one row, after its temperature and its top-k threshold `thr`: the smallest
+// set of most likely logits whose mass reaches top_p of the row's kept mass, with the whole tie
+// group at the cut (gsyq.cn §3.3 names top_p among the parameters both sides share).  Every
+// logit's weight w = 2^x, x = (z - M) * c2, is computed the same way in every pass, so all
+// passes agree on it.
+//   1. One pass bins the weights by u = -2x into 31 buckets of half a binade each plus a tail
+//      bucket (u >= 31), each thread in its own column of shared memory (no atomics), keeping
+//      mass and count; the tail (almost every logit of a long row) is only counted, its mass is
+//      the row's total S less the other buckets.  The bucket where the mass counted from the top
+//      first reaches top_p * S holds the cut.
+//   2. If that bucket holds at most kNucCap logits, one more pass gathers them (key, w) into
+//      shared memory; a bitonic sort by key and a scan from the top give the exact cut key.
+//   3. Otherwise the bucket is split by 4-bit digits of the key, most significant first, one
+//      pass per digit, until the part holding the cut is small enough to gather (or is a single
+//      key).
+// S is the row's kept mass relative to M (before top-p).  Returns the nucleus mass relative to M
+// and the cut as a logit value.  All threads of the block call it; `nbuf` is kNucBytes of shared
+// memory.
+constexpr int kNucBins = 32;
+constexpr int kNucCap = 4096;
+constexpr size_t kNucBytes = (size_t)kNucBins * kThreads * (sizeof(float) + sizeof(uint16_t));
+
+struct NucSel {     // which logits the current pass looks at
+  int bucket;       // level-0 bucket (-1: all kept logits)
+  uint32_t mask;    // key bits fixed by the digit levels so far
+  uint32_t prefix;  // their value
+};
+
+__device__ __forceinline__ int nuc_bucket(float x) { return (int)fminf(31.0f, floorf(-2.0f * x)); }
+
+// One pass over the row: per-thread bins (mass, count) of the selected logits, by level-0 bucket
+// (shift < 0) or by the key digit at `shift`; or, with `gather`, the selected logits themselves.
+template <typename T, bool VEC>
+__device__ __forceinline__ void nuc_pass(const Params& P, const T* row, float M, float c2, uint32_t kthr,
+                                         const NucSel& sel, int shift, bool gather, unsigned char* nbuf,
+                                         Smem& sm) {
+  const int t = threadIdx.x, lane = t & 31;
+  float* mass = reinterpret_cast<float*>(nbuf);
+  uint16_t* cnt = reinterpret_cast<uint16_t*>(nbuf + (size_t)kNucBins * kThreads * sizeof(float));
+  uint32_t* gk = reinterpret_cast<uint32_t*>(nbuf);
+  float* gw = reinterpret_cast<float*>(nbuf + (size_t)kNucCap * sizeof(uint32_t));
+  if (!gather) {
+#pragma unroll
+    for (int b = 0; b < kNucBins; ++b) {
+      mass[b * kThreads + t] = 0.0f;
+      cnt[b * kThreads + t] = 0;
+    }
+  } else if (t == 0) {
+    sm.nuc_n = 0;
+  }
+  const bool level0 = !gather && shift < 0;
+  uint32_t tail = 0;  // level 0: logits in the tail bucket, counted in a register
+  __syncthreads();
+  for (int c = 0; c < P.nchunk; ++c) {
+    const int v0 = c * Cfg<T>::CH;
+    float v[Cfg<T>::PER];
+    load_chunk<T, VEC>(row + v0, min(Cfg<T>::CH, P.V - v0), v);
+#pragma unroll
+    for (int i = 0; i < Cfg<T>::PER; ++i) {
+      const uint32_t k = fkey(v[i]);
+      const float x = (v[i] - M) * c2;
+      const int bk = nuc_bucket(x);
+      const bool in = v[i] > -INFINITY && k >= kthr && (sel.bucket < 0 || bk == sel.bucket) &&
+                      (k & sel.mask) == sel.prefix;
+      if (!gather) {
+        if (in && level0 && bk == kNucBins - 1) {
+          ++tail;
+        } else if (in) {
+          const int bin = level0 ? bk : (int)((k >> shift) & 15u);
+          mass[bin * kThreads + t] += ex2(x);
+          cnt[bin * kThreads + t] += 1;
+        }
+      } else {
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, in);
+        if (m) {
+          int base = 0;
+          if (lane == __ffs(m) - 1) base = atomicAdd(&sm.nuc_n, __popc(m));
+          base = __shfl_sync(0xFFFFFFFFu, base, __ffs(m) - 1);
+          const int idx = base + __popc(m & ((1u << lane) - 1u));
+          if (in && idx < kNucCap) {
+            gk[idx] = k;
+            gw[idx] = ex2(x);
+          }
+        }
+      }
+    }
+  }
+  if (level0) cnt[(kNucBins - 1) * kThreads + t] = (uint16_t)tail;
+  __syncthreads();
+}
+
+// Bins of the last pass summed over threads; warp 0 finds the bin where the mass counted from the
+// top (bin 0 first; for digits, the highest digit first) first reaches the target, or, if
+// rounding leaves the target unreached, the lowest bin with mass.  Results in sm.nuc_*.
+__device__ __forceinline__ void nuc_pick(unsigned char* nbuf, Smem& sm, int nbins, bool digits, float above,
+                                         bool level0, float top_p, float S) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const float* mass = reinterpret_cast<const float*>(nbuf);
+  const uint16_t* cnt = reinterpret_cast<const uint16_t*>(nbuf + (size_t)kNucBins * kThreads * sizeof(float));
+  for (int b = warp; b < nbins; b += kWarps) {
+    float s = 0.0f;
+    uint32_t n = 0;
+    for (int j = lane; j < kThreads; j += 32) {
+      s += mass[b * kThreads + j];
+      n += cnt[b * kThreads + j];
+    }
+    s = warp_sum(s);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xFFFFFFFFu, n, o);
+    if (lane == 0) {
+      sm.incl[b] = s;
+      sm.red_cnt[b] = n;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // lane l takes the l-th bin in order from the top
+    const int b = digits ? nbins - 1 - lane : lane;
+    float s = lane < nbins ? sm.incl[b] : 0.0f;
+    if (level0) {  // the tail's mass is what the other buckets leave of S
+      const float head = warp_sum(lane < kNucBins - 1 ? s : 0.0f);
+      if (lane == kNucBins - 1) s = fmaxf(S - head, 0.0f);
+      if (lane == 0) sm.nuc_target = top_p * S;
+    }
+    __syncwarp();
+    const float target = sm.nuc_target;
+    float incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const unsigned hit = __ballot_sync(0xFFFFFFFFu, lane < nbins && above + incl >= target);
+    const unsigned nz = __ballot_sync(0xFFFFFFFFu, s > 0.0f);
+    const int L = hit ? __ffs(hit) - 1 : (nz ? 31 - __clz(nz) : 0);
+    if (lane == L) {
+      sm.nuc_digit = b;
+      sm.nuc_above = above + incl - s;
+      sm.nuc_bin = s;
+      sm.nuc_count = sm.red_cnt[b];
+    }
+  }
+  __syncthreads();
+}
+
+template <typename T, bool VEC>
+__device__ __forceinline__ void nucleus_row(const Params& P, const T* row, float M, float c2, float thr, float S,
+                                            unsigned char* nbuf, Smem& sm, float& S_kept, float& cut) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const uint32_t kthr = thr == -INFINITY ? 0u : fkey(thr);  // keys below it are outside top-k
+  NucSel sel{-1, 0u, 0u};
+  nuc_pass<T, VEC>(P, row, M, c2, kthr, sel, -1, false, nbuf, sm);
+  nuc_pick(nbuf, sm, kNucBins, false, 0.0f, true, P.top_p, S);
+  sel.bucket = sm.nuc_digit;
+  float above = sm.nuc_above, binmass = sm.nuc_bin;
+  uint32_t count = sm.nuc_count;
+  bool exact_key = false;
+  for (int shift = 28; count > (uint32_t)kNucCap; shift -= 4) {
+    if (shift < 0) {  // every logit left has the same key: that key is the cut
+      exact_key = true;
+      break;
+    }
+    __syncthreads();
+    nuc_pass<T, VEC>(P, row, M, c2, kthr, sel, shift, false, nbuf, sm);
+    nuc_pick(nbuf, sm, 16, true, above, false, P.top_p, 0.0f);
+    sel.mask |= 15u << shift;
+    sel.prefix |= (uint32_t)sm.nuc_digit << shift;
+    above = sm.nuc_above;
+    binmass = sm.nuc_bin;
+    count = sm.nuc_count;
+  }
+  if (exact_key) {
+    S_kept = above + binmass;
+    cut = keyf(sel.prefix);
+    __syncthreads();
+    return;
+  }
+  __syncthreads();
+  nuc_pass<T, VEC>(P, row, M, c2, kthr, sel, 0, true, nbuf, sm);
+  const int n = min((int)count, sm.nuc_n);
+  uint32_t* gk = reinterpret_cast<uint32_t*>(nbuf);
+  float* gw = reinterpret_cast<float*>(nbuf + (size_t)kNucCap * sizeof(uint32_t));
+  int N = 32;
+  while (N < n) N <<= 1;
+  for (int i = n + t; i < N; i += kThreads) {
+    gk[i] = 0u;  // below every real key: sorts last
+    gw[i] = 0.0f;
+  }
+  __syncthreads();
+  // bitonic sort, descending by key (equal keys end up adjacent)
+  for (int k = 2; k <= N; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = t; i < N; i += kThreads) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const bool desc = (i & k) == 0;
+          const uint32_t a = gk[i], b = gk[ixj];
+          if (desc ? (a < b) : (a > b)) {
+            gk[i] = b;
+            gk[ixj] = a;
+            const float wa = gw[i];
+            gw[i] = gw[ixj];
+            gw[ixj] = wa;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  if (warp == 0) {
+    const float target = sm.nuc_target;
+    float cum = above;
+    int at = -1;
+    for (int base = 0; base < n && at < 0; base += 32) {
+      const int i = base + lane;
+      const float w = i < n ? gw[i] : 0.0f;
+      float incl = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned hit = __ballot_sync(0xFFFFFFFFu, i < n && cum + incl >= target);
+      if (hit) {
+        const int L = __ffs(hit) - 1;
+        at = base + L;
+        cum += __shfl_sync(0xFFFFFFFFu, incl, L);
+      } else {
+        cum += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      }
+    }
+    if (lane == 0) {
+      if (at < 0) at = n - 1;  // rounding left the target unreached: keep everything gathered
+      const uint32_t kc = gk[at];
+      for (int i = at + 1; i < n && gk[i] == kc; ++i) cum += gw[i];  // the rest of the tie group
+      sm.nuc_above = cum;
+      sm.nuc_key = kc;
+    }
+  }
+  __syncthreads();
+  S_kept = sm.nuc_above;
+  cut = keyf(sm.nuc_key);
+  __syncthreads();
+}
+
 // The per-request tail, run by the CTA that completed the request's last item.
-template <typename T, int MODE, bool VEC>
+template <typename T, int MODE, bool VEC, bool NUC>
 __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* dyn) {
+  constexpr bool MASK = MODE == kTopK || NUC;  // draws skip logits below a row threshold
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int K = P.K;
   // Warp 0 starts the loads of the ratio test right away (draft tokens, uniforms, the logits at
@@ -1165,13 +1427,14 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
     for (int r = warp; r < nrows; r += kWarps) {
       const int rp = r <= Kb ? r : K + 1 + (r - Kb - 1);
       const float2* part = P.partial + ((size_t)b * P.R + rp) * P.nchunk * kWarps;
+      const float c2 = r > Kb ? P.c2q : P.c2;
       float m = -INFINITY, s = 0.0f;
 #pragma unroll 4
       for (int c = lane; c < P.nchunk * kWarps; c += 32) {
         float2 pc = __ldg(part + c);
-        lse_merge(m, s, pc.x, pc.y, P.c2);
+        lse_merge(m, s, pc.x, pc.y, c2);
       }
-      lse_warp(m, s, P.c2);
+      lse_warp(m, s, c2);
       if (lane == 0) {
         sm.rowM[r] = m;
         sm.rowS[r] = s;
@@ -1226,8 +1489,9 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
         const int rp = r <= Kb ? r : K + 1 + (r - Kb - 1);
         float M, S, thr;
         int fl = 0;
-        topk_row_exact<T, VEC>(P, row_ptr<T>(P, b, rp), reinterpret_cast<uint32_t*>(dyn + (VEC ? (size_t)kDrawStages * kDrawStageBytes : 0)), sm, M, S,
-                               thr, fl);
+        topk_row_exact<T, VEC>(P, row_ptr<T>(P, b, rp), rp > K ? P.c2q : P.c2,
+                               reinterpret_cast<uint32_t*>(dyn + (VEC ? (size_t)kDrawStages * kDrawStageBytes : 0)),
+                               sm, M, S, thr, fl);
         if (t == 0) {
           sm.rowM[r] = M;
           sm.rowS[r] = S;
@@ -1239,6 +1503,31 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
     }
   }
   __syncthreads();
+  if (NUC && MODE == kSample) {  // top-p: the nucleus pass left each row's kept mass and cut
+    for (int r = t; r < nrows; r += kThreads) {
+      if (sm.rowFlag[r] & SPEC_FLAG_NONFINITE) continue;
+      const int rp = r <= Kb ? r : K + 1 + (r - Kb - 1);
+      const float2 ns = P.rowstat[(size_t)b * P.R + rp];
+      sm.rowS[r] = ns.x;
+      sm.rowT[r] = ns.y;
+    }
+    __syncthreads();
+  } else if (NUC) {  // top-p after top-k: cut every valid row's kept set down to its nucleus
+    unsigned char* nbuf = dyn + (VEC ? (size_t)kDrawStages * kDrawStageBytes : 0) +
+                          (MODE == kTopK ? (size_t)kWarps * kRowCap * sizeof(uint2) : 0);
+    for (int r = 0; r < nrows; ++r) {
+      if (sm.rowFlag[r] & SPEC_FLAG_NONFINITE) continue;  // uniform: every thread reads the same flag
+      const int rp = r <= Kb ? r : K + 1 + (r - Kb - 1);
+      float S, cut;
+      nucleus_row<T, VEC>(P, row_ptr<T>(P, b, rp), sm.rowM[r], r > Kb ? P.c2q : P.c2, sm.rowT[r], sm.rowS[r],
+                          nbuf, sm, S, cut);
+      if (t == 0) {
+        sm.rowS[r] = S;
+        sm.rowT[r] = cut;
+      }
+      __syncthreads();
+    }
+  }
   if (t == 0) {
     int f = 0;
     for (int r = 0; r < nrows; ++r) f |= sm.rowFlag[r];
@@ -1283,7 +1572,7 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
         if (!bad) {
           const int rq = Kb + 1 + lane;
           if (zpx >= sm.rowT[lane]) a = ex2((zpx - sm.rowM[lane]) * P.c2) / sm.rowS[lane];
-          if (zqx >= sm.rowT[rq]) cq = ex2((zqx - sm.rowM[rq]) * P.c2) / sm.rowS[rq];
+          if (zqx >= sm.rowT[rq]) cq = ex2((zqx - sm.rowM[rq]) * P.c2q) / sm.rowS[rq];
         }
         acc = uu * cq < a;
         am = cq > 0.0f ? fabsf(uu - a / cq) : INFINITY;
@@ -1315,7 +1604,8 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
     d.Mp2 = sm.rowM[js] * P.c2;
     d.Lp = d.Mp2 + log2f(sm.rowS[js]);
     d.Tp = sm.rowT[js];
-    d.Lq = d.resid ? sm.rowM[rq] * P.c2 + log2f(sm.rowS[rq]) : 0.0f;
+    d.Lq = d.resid ? sm.rowM[rq] * P.c2q + log2f(sm.rowS[rq]) : 0.0f;
+    d.c2q = P.c2q;
     d.Tq = d.resid ? sm.rowT[rq] : 0.0f;
     const T* pr = prow<T>(P, b, js);
     const T* qr = d.resid ? qrow<T>(P, b, js) : pr;
@@ -1325,7 +1615,7 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
     int clamp = 0;
     bool drawn = false;
     float R = 0.0f;
-    if (MODE == kSample && !d.resid) {
+    if (MODE == kSample && !NUC && !d.resid) {
       // Bonus draw: the chunk masses follow from the stored (max, sum) pairs, so only the chunk
       // holding u * S is read again.
       const int nch = P.nchunk;
@@ -1367,18 +1657,18 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
       const float tin = sm.tile_base, S = sm.total;
       __syncthreads();
       const int v0 = cs * Cfg<T>::CH;
-      const float rc = draw_range<T, VEC, MODE == kTopK>(P, pr, pr, d, v0, min(P.V, v0 + Cfg<T>::CH), false, u, tin, S,
-                                          wt, ring, sm, &clamp);
+      const float rc = draw_range<T, VEC, MASK>(P, pr, pr, d, v0, min(P.V, v0 + Cfg<T>::CH), false, u, tin, S,
+                                                wt, ring, sm, &clamp);
       drawn = rc > 0.0f;
       R = S;
     }
-    if (!drawn) R = draw_range<T, VEC, MODE == kTopK>(P, pr, qr, d, 0, P.V, true, u, 0.0f, 0.0f, wt, ring, sm, &clamp);
+    if (!drawn) R = draw_range<T, VEC, MASK>(P, pr, qr, d, 0, P.V, true, u, 0.0f, 0.0f, wt, ring, sm, &clamp);
     float resid_mass = d.resid ? R : 0.0f;
     if (!(R > 0.0f)) {
       // max(0, p - q) vanished through rounding: draw from p instead
       d.resid = false;
       if (t == 0) sm.flags |= SPEC_FLAG_RESIDUAL_ZERO;
-      R = draw_range<T, VEC, MODE == kTopK>(P, pr, pr, d, 0, P.V, true, u, 0.0f, 0.0f, wt, ring, sm, &clamp);
+      R = draw_range<T, VEC, MASK>(P, pr, pr, d, 0, P.V, true, u, 0.0f, 0.0f, wt, ring, sm, &clamp);
     }
     if (clamp) atomicOr(&sm.flags, SPEC_FLAG_CDF_CLAMP);
     __syncthreads();
@@ -1415,7 +1705,7 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
         int rr = -1;  // compact row index of padded row r
         if (r <= K) rr = r <= Kb ? r : -1;
         else rr = (r - K - 1) < Kb ? Kb + 1 + (r - K - 1) : -1;
-        if (rr >= 0) v = sm.rowM[rr] * P.invT + logf(sm.rowS[rr]);
+        if (rr >= 0) v = sm.rowM[rr] * (rr > Kb ? P.invTq : P.invT) + logf(sm.rowS[rr]);
       }
       P.lognorm[(size_t)b * R + r] = v;
     }
@@ -1499,7 +1789,7 @@ __device__ __forceinline__ uint32_t bmax2_nan(uint32_t a, uint32_t b) {
 // values, then 2^((z - max) * c2) in packed f32x2 arithmetic, then a warp max and a rescaled warp
 // sum.  Writes (max, sum) for the warp's share to out[warp].
 template <typename T>
-__device__ __forceinline__ void sample_vec(const Params& P, uint4 (&raw)[Cfg<T>::LOADS], int n, float2* out) {
+__device__ __forceinline__ void sample_vec(float c2, uint4 (&raw)[Cfg<T>::LOADS], int n, float2* out) {
   const int t = threadIdx.x;
   if (n < Cfg<T>::CH) {  // tail chunk: vectors at or past n hold no logits
 #pragma unroll
@@ -1531,7 +1821,7 @@ __device__ __forceinline__ void sample_vec(const Params& P, uint4 (&raw)[Cfg<T>:
   }
   float s = 0.0f;
   if (m != -INFINITY) {
-    const float2 negm = make_float2(-m, -m), cc = make_float2(P.c2, P.c2);
+    const float2 negm = make_float2(-m, -m), cc = make_float2(c2, c2);
     float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int l = 0; l < Cfg<T>::LOADS; ++l) {
@@ -1556,7 +1846,7 @@ __device__ __forceinline__ void sample_vec(const Params& P, uint4 (&raw)[Cfg<T>:
   float M = m;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmax_nan(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-  float sc = s == 0.0f ? 0.0f : s * ex2((m - M) * P.c2);
+  float sc = s == 0.0f ? 0.0f : s * ex2((m - M) * c2);
   sc = warp_sum(sc);
   if ((t & 31) == 0) out[t >> 5] = make_float2(M, sc);
 }
@@ -1639,7 +1929,7 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
     const int n = min(Cfg<T>::CH, P.V - v0);
     const size_t slot = ((size_t)k.b * P.R + k.rp) * P.nchunk + k.c;
     if (MODE == kSample)
-      item_sample<T>(P, v, P.partial + slot * kWarps);
+      item_sample<T>(k.rp > P.K ? P.c2q : P.c2, v, P.partial + slot * kWarps);
     else if (MODE == kGreedy)
       item_greedy<T, VEC>(v, n, v0, P.partial + slot * kWarps);
     else
@@ -1671,7 +1961,7 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
       const int n = min(Cfg<T>::CH, P.V - cc.c * Cfg<T>::CH);
       if (MODE == kSample) {
         const size_t slot = ((size_t)cc.b * P.R + cc.rp) * P.nchunk + cc.c;
-        sample_vec<T>(P, raw, n, P.partial + slot * kWarps);
+        sample_vec<T>(cc.rp > P.K ? P.c2q : P.c2, raw, n, P.partial + slot * kWarps);
       } else if (MODE == kGreedy) {
         const size_t slot = ((size_t)cc.b * P.R + cc.rp) * P.nchunk + cc.c;
         greedy_vec<T>(raw, n, cc.c * Cfg<T>::CH, P.partial + slot * kWarps);
@@ -1698,14 +1988,56 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
   }
 }
 
+// Top-p in sampling mode, between the two passes: one block per valid row merges the row's
+// chunk summaries into its (max, sum), exactly as the per-request pass does, finds the row's
+// nucleus and leaves (kept mass, cut) for the per-request pass.  Non-finite rows are left to the
+// per-request pass, which flags them.
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kThreads) nucleus_kernel(const Params P) {
+  extern __shared__ __align__(128) unsigned char dyn[];
+  __shared__ Smem sm;
+  const int t = threadIdx.x, lane = t & 31;
+  int b, rp;
+  if (P.rowmap) {
+    if (blockIdx.x >= __ldg(P.total_rows)) return;
+    const uint32_t e = __ldg(P.rowmap + blockIdx.x);
+    b = (int)(e >> 6);
+    rp = (int)(e & 63u);
+  } else {
+    b = (int)(blockIdx.x / (unsigned)P.R);
+    rp = (int)(blockIdx.x % (unsigned)P.R);
+  }
+  const float c2 = rp > P.K ? P.c2q : P.c2;
+  if (t < 32) {
+    const float2* part = P.partial + ((size_t)b * P.R + rp) * P.nchunk * kWarps;
+    float m = -INFINITY, s = 0.0f;
+#pragma unroll 4
+    for (int c = lane; c < P.nchunk * kWarps; c += 32) {
+      float2 pc = __ldg(part + c);
+      lse_merge(m, s, pc.x, pc.y, c2);
+    }
+    lse_warp(m, s, c2);
+    if (lane == 0) {
+      sm.rowM[0] = m;
+      sm.rowS[0] = s;
+      sm.rowFlag[0] = (!(s > 0.0f) || isinf(m) || isnan(s)) ? 1 : 0;
+    }
+  }
+  __syncthreads();
+  if (sm.rowFlag[0]) return;
+  float S, cut;
+  nucleus_row<T, VEC>(P, row_ptr<T>(P, b, rp), sm.rowM[0], c2, -INFINITY, sm.rowS[0], dyn, sm, S, cut);
+  if (t == 0) P.rowstat[(size_t)b * P.R + rp] = make_float2(S, cut);
+}
+
 // Pass 2: one block per request merges its rows' summaries, runs the ratio test and the
 // first-rejection scan, and draws the resampled or bonus token.
-template <typename T, int MODE, bool VEC>
+template <typename T, int MODE, bool VEC, bool NUC>
 __global__ void __launch_bounds__(kThreads) finish_kernel(const Params P) {
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ Smem sm;
   for (int b = blockIdx.x; b < P.B; b += gridDim.x) {
-    finish_request<T, MODE, VEC>(P, b, sm, dyn);
+    finish_request<T, MODE, VEC, NUC>(P, b, sm, dyn);
     __syncthreads();
   }
 }
@@ -1755,7 +2087,7 @@ __global__ void __launch_bounds__(1024) build_rowmap(const int32_t* __restrict__
 // host side
 // ------------------------------------------------------------------------------------------------
 struct Layout {
-  size_t partial, cmeta, cand, rowmap, total_rows, bytes;
+  size_t partial, cmeta, cand, rowstat, rowmap, total_rows, bytes;
   int R, nchunk;
   uint64_t rows_padded;
 };
@@ -1781,6 +2113,8 @@ static bool make_layout(int B, int K, int V, int es, int mode, bool ragged, Layo
     L->cand = o;
     o = align256(o + (size_t)items * kCandCap * sizeof(uint2));
   }
+  L->rowstat = o;
+  if (mode != kGreedy) o = align256(o + (size_t)L->rows_padded * sizeof(float2));
   L->rowmap = o;
   L->total_rows = o;
   if (ragged) {
@@ -1801,10 +2135,11 @@ static int mode_of(float temperature, int top_k, int V) {
 static size_t stats_smem(int mode, bool vec) {
   return (vec ? (size_t)kStages * kChunkBytes : 0) + (mode == kTopK ? (size_t)2 * kSegCap * sizeof(uint2) : 0);
 }
-static size_t finish_smem(int mode, int V, int es, bool vec) {
+static size_t finish_smem(int mode, int V, int es, bool vec, bool nuc) {
   const int ntile = (V + kTile - 1) / kTile;
   const int nch = (V + kChunkBytes / es - 1) / (kChunkBytes / es);
   size_t bytes = (size_t)(ntile > nch ? ntile : nch) * sizeof(float);  // tile / chunk sums
+  if (nuc && mode == kTopK && bytes < kNucBytes) bytes = kNucBytes;  // the nucleus bins / gathered logits
   if (mode == kGreedy) return 16;
   if (mode == kTopK) bytes += (size_t)kWarps * kRowCap * sizeof(uint2);
   if (vec) bytes += (size_t)kDrawStages * kDrawStageBytes;  // cp.async ring of the CDF pass
@@ -1820,9 +2155,10 @@ static cudaError_t prepare(K kern, size_t dsm) {
 template <typename T, int MODE, bool VEC>
 static cudaError_t launch_t(const Params& P, uint32_t items, cudaStream_t st) {
   const int es = (int)sizeof(T);
+  const bool nuc = MODE != kGreedy && P.top_p < 1.0f;
   auto k1 = stats_kernel<T, MODE, VEC>;
-  auto k2 = finish_kernel<T, MODE, VEC>;
-  const size_t d1 = stats_smem(MODE, VEC), d2 = finish_smem(MODE, P.V, es, VEC);
+  auto k2 = nuc ? finish_kernel<T, MODE, VEC, MODE != kGreedy> : finish_kernel<T, MODE, VEC, false>;
+  const size_t d1 = stats_smem(MODE, VEC), d2 = finish_smem(MODE, P.V, es, VEC, nuc);
   cudaError_t e = prepare(k1, d1);
   if (e == cudaSuccess) e = prepare(k2, d2);
   int dev = 0, sms = 0, occ = 0;
@@ -1837,6 +2173,14 @@ static cudaError_t launch_t(const Params& P, uint32_t items, cudaStream_t st) {
   e = cudaGetLastError();
   if (e == cudaSuccess && P.pass1_done) e = cudaEventRecord(static_cast<cudaEvent_t>(P.pass1_done), st);
   if (e != cudaSuccess) return e;
+  if (nuc && MODE == kSample) {
+    auto kn = nucleus_kernel<T, VEC>;
+    e = prepare(kn, kNucBytes);
+    if (e != cudaSuccess) return e;
+    kn<<<(unsigned)((uint64_t)P.B * P.R), kThreads, kNucBytes, st>>>(P);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   k2<<<(unsigned)P.B, kThreads, d2, st>>>(P);
   return cudaGetLastError();
 }
@@ -1872,14 +2216,19 @@ size_t spec_verify_workspace_bytes(int32_t B, int32_t K_max, int32_t V, spec_dty
   return a.bytes > b.bytes ? a.bytes : b.bytes;
 }
 
-spec_status_t spec_verify(const void* p_logits, const void* q_logits, const int32_t* draft_tokens,
-                          const int32_t* k_per_row, const float* u_accept, const float* u_resample,
-                          float temperature, int32_t top_k, int32_t* out_tokens,
-                          int32_t* out_num_accepted, const spec_verify_stats_t* out_stats, int32_t B,
-                          int32_t K_max, int32_t V, spec_dtype_t dtype, void* workspace,
-                          size_t workspace_bytes, void* stream) {
-  if (B < 0 || K_max < 0 || V <= 0) return SPEC_ERR_INVALID_ARG;
+spec_status_t spec_verify_ex(const void* p_logits, const void* q_logits, const int32_t* draft_tokens,
+                             const int32_t* k_per_row, const float* u_accept, const float* u_resample,
+                             const spec_sampling_t* sampling, int32_t* out_tokens,
+                             int32_t* out_num_accepted, const spec_verify_stats_t* out_stats, int32_t B,
+                             int32_t K_max, int32_t V, spec_dtype_t dtype, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (B < 0 || K_max < 0 || V <= 0 || !sampling) return SPEC_ERR_INVALID_ARG;
+  const float temperature = sampling->temperature, tq = sampling->draft_temperature;
+  const int32_t top_k = sampling->top_k;
+  const float top_p = sampling->top_p;
   if (!(temperature >= 0.0f) || isinf(temperature) || top_k < 0) return SPEC_ERR_INVALID_ARG;
+  if (temperature > 0.0f && (!(tq > 0.0f) || isinf(tq))) return SPEC_ERR_INVALID_ARG;
+  if (!(top_p > 0.0f)) return SPEC_ERR_INVALID_ARG;
   if (K_max > SPEC_MAX_K || V > SPEC_MAX_V) return SPEC_ERR_UNSUPPORTED;
   if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED;
   const int mode = mode_of(temperature, top_k, V);
@@ -1923,12 +2272,16 @@ spec_status_t spec_verify(const void* p_logits, const void* q_logits, const int3
   P.top_k = top_k;
   P.nchunk = L.nchunk;
   P.R = L.R;
-  const double T = temperature;
+  const double T = temperature, Tq = tq;
   P.c2 = mode == kGreedy ? 0.0f : (float)(1.4426950408889634 / T);
   P.invT = mode == kGreedy ? 0.0f : (float)(1.0 / T);
+  P.c2q = mode == kGreedy ? 0.0f : (float)(1.4426950408889634 / Tq);
+  P.invTq = mode == kGreedy ? 0.0f : (float)(1.0 / Tq);
+  P.top_p = top_p >= 1.0f ? 1.0f : top_p;
   P.partial = reinterpret_cast<float2*>(ws + L.partial);
   P.cmeta = reinterpret_cast<uint2*>(ws + L.cmeta);
   P.cand = reinterpret_cast<uint2*>(ws + L.cand);
+  P.rowstat = reinterpret_cast<float2*>(ws + L.rowstat);
   P.rowmap = ragged ? reinterpret_cast<const uint32_t*>(ws + L.rowmap) : nullptr;
   P.total_rows = ragged ? reinterpret_cast<const uint32_t*>(ws + L.total_rows) : nullptr;
   P.uniform_items = (uint32_t)(L.rows_padded * (uint64_t)L.nchunk);
@@ -1944,6 +2297,17 @@ spec_status_t spec_verify(const void* p_logits, const void* q_logits, const int3
   cudaError_t e = dtype == SPEC_DTYPE_BF16 ? launch_mode<uint16_t>(mode, vec, P, items, s)
                                            : launch_mode<float>(mode, vec, P, items, s);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status_t spec_verify(const void* p_logits, const void* q_logits, const int32_t* draft_tokens,
+                          const int32_t* k_per_row, const float* u_accept, const float* u_resample,
+                          float temperature, int32_t top_k, int32_t* out_tokens,
+                          int32_t* out_num_accepted, const spec_verify_stats_t* out_stats, int32_t B,
+                          int32_t K_max, int32_t V, spec_dtype_t dtype, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  const spec_sampling_t sp = {temperature, temperature, top_k, 1.0f};
+  return spec_verify_ex(p_logits, q_logits, draft_tokens, k_per_row, u_accept, u_resample, &sp, out_tokens,
+                        out_num_accepted, out_stats, B, K_max, V, dtype, workspace, workspace_bytes, stream);
 }
 
 size_t spec_verify_host_staging_bytes(int32_t B, int32_t K_max, int32_t V, spec_dtype_t dtype,
@@ -1963,12 +2327,15 @@ size_t spec_verify_host_staging_bytes(int32_t B, int32_t K_max, int32_t V, spec_
   return o + ws;
 }
 
-spec_status_t spec_verify_host(const void* p_logits, const void* q_logits,
-                               const int32_t* draft_tokens, const int32_t* k_per_row,
-                               const float* u_accept, const float* u_resample, float temperature,
-                               int32_t top_k, int32_t* out_tokens, int32_t* out_num_accepted,
-                               int32_t B, int32_t K_max, int32_t V, spec_dtype_t dtype,
-                               void* staging, size_t staging_bytes, void* stream) {
+spec_status_t spec_verify_host_ex(const void* p_logits, const void* q_logits,
+                                  const int32_t* draft_tokens, const int32_t* k_per_row,
+                                  const float* u_accept, const float* u_resample,
+                                  const spec_sampling_t* sampling, int32_t* out_tokens,
+                                  int32_t* out_num_accepted, int32_t B, int32_t K_max, int32_t V,
+                                  spec_dtype_t dtype, void* staging, size_t staging_bytes, void* stream) {
+  if (!sampling) return SPEC_ERR_INVALID_ARG;
+  const float temperature = sampling->temperature;
+  const int32_t top_k = sampling->top_k;
   if (B < 0 || K_max < 0 || V <= 0 || K_max > SPEC_MAX_K || V > SPEC_MAX_V) return SPEC_ERR_INVALID_ARG;
   if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED;
   const size_t need = spec_verify_host_staging_bytes(B, K_max, V, dtype, top_k, k_per_row != nullptr);
@@ -2003,16 +2370,28 @@ spec_status_t spec_verify_host(const void* p_logits, const void* q_logits,
   if (e == cudaSuccess && !greedy && u_accept && K_max) e = cudaMemcpyAsync(dua, u_accept, (size_t)B * K_max * 4, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess && !greedy && u_resample) e = cudaMemcpyAsync(dur, u_resample, (size_t)B * 4, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return SPEC_ERR_CUDA;
-  spec_status_t r = spec_verify(dp, greedy ? nullptr : (q_logits ? dq : nullptr), draft_tokens ? (const int32_t*)dx : nullptr,
-                                k_per_row ? (const int32_t*)dk : nullptr, greedy ? nullptr : (u_accept ? (const float*)dua : nullptr),
-                                greedy ? nullptr : (u_resample ? (const float*)dur : nullptr), temperature, top_k,
-                                (int32_t*)dtok, (int32_t*)dn, nullptr, B, K_max, V, dtype, dws,
-                                staging_bytes - (size_t)(dws - d), stream);
+  spec_status_t r = spec_verify_ex(dp, greedy ? nullptr : (q_logits ? dq : nullptr),
+                                   draft_tokens ? (const int32_t*)dx : nullptr, k_per_row ? (const int32_t*)dk : nullptr,
+                                   greedy ? nullptr : (u_accept ? (const float*)dua : nullptr),
+                                   greedy ? nullptr : (u_resample ? (const float*)dur : nullptr), sampling,
+                                   (int32_t*)dtok, (int32_t*)dn, nullptr, B, K_max, V, dtype, dws,
+                                   staging_bytes - (size_t)(dws - d), stream);
   if (r != SPEC_OK) return r;
   e = cudaMemcpyAsync(out_tokens, dtok, (size_t)B * (K_max + 1) * 4, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(out_num_accepted, dn, (size_t)B * 4, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status_t spec_verify_host(const void* p_logits, const void* q_logits,
+                               const int32_t* draft_tokens, const int32_t* k_per_row,
+                               const float* u_accept, const float* u_resample, float temperature,
+                               int32_t top_k, int32_t* out_tokens, int32_t* out_num_accepted,
+                               int32_t B, int32_t K_max, int32_t V, spec_dtype_t dtype,
+                               void* staging, size_t staging_bytes, void* stream) {
+  const spec_sampling_t sp = {temperature, temperature, top_k, 1.0f};
+  return spec_verify_host_ex(p_logits, q_logits, draft_tokens, k_per_row, u_accept, u_resample, &sp,
+                             out_tokens, out_num_accepted, B, K_max, V, dtype, staging, staging_bytes, stream);
 }
 
 const char* spec_verify_status_string(spec_status_t status) {

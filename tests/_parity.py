@@ -8,7 +8,9 @@ Acceptance criteria (the tolerances the verify step is held to):
 * p_j(x_j) and q_j(x_j) within 1e-5 relative; each row's log-normaliser within 1e-5 absolute
   (= 1e-5 relative on every probability of the row); the residual mass within 1e-5;
 * the data flags (bad token, bad k, non-finite, top-k tie) identical; the rounding flags
-  (zero residual, CDF clamp) are free to differ.
+  (zero residual, CDF clamp) are free to differ;
+* with top-p, a request any of whose rows has its nucleus cut within 1e-5 of top_p (the
+  oracle's nucleus margin) is counted as low-margin and only its output form is checked.
 """
 from __future__ import annotations
 
@@ -37,6 +39,8 @@ def run_gpu(d, dev="cuda:0", stats=True, k_per_row="auto", **kw):
         k_per_row = kpr if (w is None or w.ragged is not None) else None
     T = d["temperature"]
     greedy = T == 0.0
+    kw.setdefault("draft_temperature", d.get("draft_temperature"))
+    kw.setdefault("top_p", d.get("top_p", 1.0))
     tok, n, st = sv.verify(to_dev(d["p"], dev), None if greedy else to_dev(d["q"], dev),
                            to_dev(d["draft"], dev), to_dev(k_per_row, dev),
                            None if greedy else to_dev(d["ua"], dev), None if greedy else to_dev(d["ur"], dev),
@@ -56,7 +60,8 @@ def run_oracle(d, nthreads=0, k_per_row="auto"):
     if isinstance(k_per_row, str):
         k_per_row = kpr if (w is None or w.ragged is not None) else None
     return oracle.verify(d["p"], d["q"], d["draft"], k_per_row, d["ua"], d["ur"], d["temperature"],
-                         d["top_k"], nthreads=nthreads or (os.cpu_count() or 1))
+                         d["top_k"], nthreads=nthreads or (os.cpu_count() or 1),
+                         draft_temperature=d.get("draft_temperature"), top_p=d.get("top_p", 1.0))
 
 
 def compare(g, o, K, kb=None, check_stats=True):
@@ -75,6 +80,20 @@ def compare(g, o, K, kb=None, check_stats=True):
         no, ng = int(o["n_acc"][b]), int(g["n_acc"][b])
         to, tg = o["tokens"][b], g["tokens"][b]
         assert 0 <= ng <= kb[b], f"b={b}: n_acc {ng} outside [0, {kb[b]}]"
+        nm = o.get("nucleus_margin")
+        Kmax = (len(o["row_lognorm"][b]) - 1) // 2
+        loose = np.zeros(2 * Kmax + 1, bool)  # rows whose top-p cut is within rounding of top_p
+        if nm is not None:
+            loose = nm[b] < MARGIN
+            used = np.zeros_like(loose)
+            used[: no + 1] = True                     # p rows 0..n_acc
+            used[Kmax + 1: Kmax + 1 + min(no + 1, int(kb[b]))] = True  # q rows 0..n_acc (< K_b)
+            if (loose & used).any():
+                # a row the decision used has its cut within rounding of top_p: either kept set
+                # is correct, so only the form of the result is checked
+                low_margin += 1
+                assert (tg[ng + 1:] == -1).all() and 0 <= tg[ng] < 1 << 30
+                continue
         if no == ng and (to == tg).all():
             exact += 1
         else:
@@ -99,7 +118,8 @@ def compare(g, o, K, kb=None, check_stats=True):
         ln_o, ln_g = o["row_lognorm"][b], g["row_lognorm"][b]
         fin = np.isfinite(ln_o)
         assert (np.isfinite(ln_g) == fin).all(), f"b={b}: lognorm validity {ln_g} vs {ln_o}"
-        np.testing.assert_allclose(ln_g[fin], ln_o[fin], rtol=0, atol=RTOL, err_msg=f"b={b} lognorm")
+        cmp = fin & ~loose
+        np.testing.assert_allclose(ln_g[cmp], ln_o[cmp], rtol=0, atol=RTOL, err_msg=f"b={b} lognorm")
         if no == ng:
             np.testing.assert_allclose(g["residual_mass"][b], o["residual_mass"][b], rtol=0, atol=RTOL)
     return dict(exact=exact, low_margin=low_margin, requests=B)

@@ -81,6 +81,27 @@ def test_host_side_validation(lib):
     assert _call(lib, B=0, T=0.0, q=0, ua=0, ur=0) == 0
 
 
+def _call_ex(lib, sampling, B=1, K=4, V=100, wsb=1 << 20):
+    P = ctypes.c_void_p
+    return lib.spec_verify_ex(P(1), P(1), P(1), None, P(1), P(1),
+                              ctypes.byref(sampling) if sampling is not None else None, P(1), P(1), None,
+                              B, K, V, 0, P(256), wsb, None)
+
+
+def test_sampling_parameter_validation(lib):
+    S = sv.SamplingStruct
+    assert _call_ex(lib, None) == 1
+    assert _call_ex(lib, S(1.0, 0.0, 0, 1.0)) == 1            # draft temperature 0 under T > 0
+    assert _call_ex(lib, S(1.0, -1.0, 0, 1.0)) == 1
+    assert _call_ex(lib, S(1.0, float("inf"), 0, 1.0)) == 1
+    assert _call_ex(lib, S(1.0, 0.5, 0, 0.0)) == 1            # top_p must be > 0
+    assert _call_ex(lib, S(1.0, 0.5, 0, float("nan"))) == 1
+    assert _call_ex(lib, S(1.0, 0.5, -2, 0.9)) == 1
+    assert _call_ex(lib, S(1.0, 0.5, 0, 0.9), B=0) == 0       # valid parameters, empty batch
+    assert _call_ex(lib, S(0.0, 0.0, 0, 0.9), B=0) == 0       # greedy ignores T_q
+    assert _call_ex(lib, S(1.0, 0.5, 0, 1.7), B=0) == 0       # top_p >= 1 is off
+
+
 def test_status_strings(lib):
     for code in range(6):
         assert lib.spec_verify_status_string(code)

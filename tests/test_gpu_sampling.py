@@ -1,0 +1,134 @@
+"""GPU parity of the sampling-parameter variants against the fp64 oracle: a draft temperature of
+its own (2kiu.com §7) and top-p / nucleus truncation (gsyq.cn §3.3), alone and with top-k, at
+small sizes and at the full size of the largest batch (every request compared), plus the limits
+(top_p = 1 and T_q = T reproduce spec_verify bit for bit; a vanishing top_p keeps the maximal
+logits; greedy ignores both) and exact ties in bf16."""
+import numpy as np
+import pytest
+
+import workloads as W
+from _parity import compare, run_gpu, run_oracle, to_dev
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def _nucleus_valid(d, g, o, tol=1e-5):
+    """Every valid row's kept mass, as the GPU's log-normaliser implies it, is a correct nucleus
+    up to rounding: it reaches top_p, and it passes the oracle's only where the oracle's cut
+    reached top_p by less than the tolerance.  Holds for low-margin rows too."""
+    import oracle
+    w = d["workload"]
+    top_p = float(np.float32(d["top_p"]))
+    if top_p >= 1.0:
+        return
+    K = w.K
+    for b in range(d["p"].shape[0]):
+        if o["flags"][b] & 16:
+            continue
+        kb = int(d["k_per_row"][b])
+        rows = [(d["p"][b, j], d["temperature"], j) for j in range(kb + 1)] + \
+               [(d["q"][b, j], d["draft_temperature"], K + 1 + j) for j in range(kb)]
+        for z, T, r in rows:
+            full = oracle.row_dist(z, T, d["top_k"], 1.0)[1]["lognorm"]
+            fg = np.exp(g["row_lognorm"][b, r] - full)
+            fo = np.exp(o["row_lognorm"][b, r] - full)
+            assert fg >= top_p - tol, (b, r, fg, top_p)
+            assert fg <= fo + tol or fo - top_p < tol, (b, r, fg, fo, top_p)
+
+
+def _check(d, **kw):
+    """Element-by-element parity.  A top-p cut within 1e-5 of top_p on any row a request uses
+    makes it low-margin (either kept set is right; the nucleus of every row is still checked)."""
+    kw.setdefault("stats", True)
+    g = run_gpu(d, **kw)
+    o = run_oracle(d)
+    w = d["workload"]
+    res = compare(g, o, w.K, d["k_per_row"])
+    _nucleus_valid(d, g, o)
+    if d.get("top_p", 1.0) < 0.99:
+        assert res["exact"] >= (res["requests"] + 1) // 2, res
+    return res, g, o
+
+
+@pytest.mark.parametrize("name,over", [("c5_topp0.9", dict(B=16)), ("c5_tq0.5", dict(B=16)),
+                                       ("c5_topp0.9", dict(B=8, dtype="f32")),
+                                       ("c5_tq0.5", dict(B=8, dtype="f32"))],
+                         ids=["topp_bf16", "tq_bf16", "topp_f32", "tq_f32"])
+def test_variant_small(name, over):
+    _check(W.generate(W.get(name, **over)))
+
+
+@pytest.mark.parametrize("top_p", [1e-6, 0.3, 0.7, 0.95, 0.999])
+@pytest.mark.parametrize("tq", [None, 0.6])
+def test_topp_sweep(top_p, tq):
+    w = W.get("c2", B=8, top_p=top_p, draft_temperature=tq, tau=0.6)
+    _check(W.generate(w))
+
+
+def test_topp_with_topk_ragged():
+    w = W.get("c4", B=8, top_p=0.8, draft_temperature=0.5, tau=0.6)
+    _check(W.generate(w))
+
+
+def test_topp_exact_ties_bf16():
+    """Logits on a coarse grid: many equal values straddle every nucleus cut."""
+    w = W.get("c2", B=8, top_p=0.6, tau=0.6)
+    d = W.generate(w)
+    for key in ("p", "q"):
+        f = W.bf16_bits_to_f32(d[key])
+        d[key] = W.to_bf16_bits(np.round(f * 2) / 2)
+    _check(d)
+
+
+def test_tiny_topp_keeps_the_maximum():
+    w = W.get("c1", top_p=1e-6)
+    d = W.generate(w)
+    res, g, o = _check(d)
+    # with only the argmax group kept, every draft that is not the argmax is rejected and the
+    # resample / bonus draw returns the argmax of the row
+    p = W.as_f32(d["p"])[0]
+    n = int(g["n_acc"][0])
+    assert g["tokens"][0, n] == int(np.argmax(p[n]))
+
+
+def test_limits_match_spec_verify_bit_for_bit():
+    import speculative_decoding_rejection_verify_gb300 as sv
+    d = W.generate(W.get("c5_a0.8", B=16))
+    a = run_gpu(d, top_p=1.0, draft_temperature=None)
+    dev = "cuda:0"
+    args = (to_dev(d["p"], dev), to_dev(d["q"], dev), to_dev(d["draft"], dev), None, to_dev(d["ua"], dev),
+            to_dev(d["ur"], dev), 1.0, 0)
+    b = sv.verify(*args, stats=True, top_p=1.5, draft_temperature=1.0)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(a["tokens"], b[0].cpu().numpy())
+    np.testing.assert_array_equal(a["row_lognorm"], b[2]["row_lognorm"].cpu().numpy())
+
+
+def test_greedy_ignores_sampling_parameters():
+    d = W.generate(W.get("c5_greedy", B=16))
+    a = run_gpu(d)
+    b = run_gpu(d, top_p=0.5, draft_temperature=0.3)
+    np.testing.assert_array_equal(a["tokens"], b["tokens"])
+    np.testing.assert_array_equal(a["n_acc"], b["n_acc"])
+
+
+@pytest.mark.parametrize("name", ["c5_topp0.9", "c5_tq0.5"])
+def test_variant_full(name):
+    """The full batch in the launch configuration the benchmark times; every request compared."""
+    d = W.generate(W.get(name))
+    g = run_gpu(d, stats=True)
+    o = run_oracle(d)
+    res = compare(g, o, d["workload"].K, d["k_per_row"])
+    assert res["requests"] == 1024 and res["exact"] >= 512, res
+
+
+def test_host_entry_with_sampling():
+    import speculative_decoding_rejection_verify_gb300 as sv
+    d = W.generate(W.get("c5_topp0.9", B=8))
+    g = run_gpu(d, stats=False)
+    tok, n = sv.verify_host(d["p"], d["q"], d["draft"], None, d["ua"], d["ur"], d["temperature"], d["top_k"],
+                            top_p=d["top_p"], draft_temperature=d["draft_temperature"])
+    np.testing.assert_array_equal(tok, g["tokens"])
+    np.testing.assert_array_equal(n, g["n_acc"])

@@ -47,6 +47,9 @@ def test_topp_hand_example(lib=None):
     # margin = distance of top_p to the cumulative masses around the cut (0.5 | 0.75 for 0.6)
     _, info, _ = oracle.row_dist(z, 1.0, 0, 0.6, lib=lib)
     assert abs(info["nucleus_margin"] - 0.1) < 1e-6
+    # a cut at the first group: the mass before it is exactly 0, so only the far side counts
+    _, info, _ = oracle.row_dist(z, 1.0, 0, 0.1, lib=lib)
+    assert abs(info["nucleus_margin"] - 0.4) < 1e-6
 
 
 def _brute_nucleus(z, T, top_k, top_p):

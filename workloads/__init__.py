@@ -1,16 +1,19 @@
 """Seeded synthetic inputs for the speculative-sampling verify step.
 
 This module serves the tests, the benchmark and the oracle alike, and holds none of the
-verify step's arithmetic (no softmax, no ratio test, no residual, no inverse CDF).  It plays
-the part of the two models around the verify step:
+verify step's arithmetic (no normaliser, no ratio test, no residual, no inverse CDF; the one
+weighting in it is the draft sampler's own nucleus cut, made with numpy's cumulative sum).
+It plays the part of the two models around the verify step:
 
 * the draft model's logits: z_q = 3 * N(0, 1) - 1.1 * ln(rank_v), with rank a seeded
   permutation of 1..V shared by every row of a workload (a Zipf-like bias);
 * the target model's logits: z_p = z_q + tau * N(0, 1) at the draft positions, and a fresh
   base row plus noise at the bonus position j = K_b;
 * the draft model's own sampling of the draft tokens, by the Gumbel-max trick
-  (argmax_v z_q[v] / T + G_v over the top-k kept set; plain argmax when T == 0).  Gumbel-max
-  draws exactly from softmax(z_q / T), the law the verify step assumes the draft used;
+  (argmax_v z_q[v] / T_q + G_v over the kept set; plain argmax when T == 0).  Gumbel-max
+  draws exactly from softmax(z_q / T_q) on that set, the law the verify step assumes the draft
+  used.  The kept set is the draft sampler's own truncation: top-k, then, when the workload sets
+  top_p < 1, the most likely tokens up to mass top_p (the tied group at the cut whole);
 * the uniforms the verify step consumes, on the grid k * 2^-24 so both sides see identical
   float32 values.
 
@@ -60,10 +63,21 @@ class Workload:
     tau: Optional[float] = None  # target-noise scale; None = look up tau.json
     ragged: Optional[tuple] = None  # (lo, hi) inclusive range of K_b, or None for K_b = K
     greedy: bool = False          # draft tokens by argmax, verified at T = 0
+    draft_temperature: Optional[float] = None  # T_q of the draft; None = temperature
+    top_p: float = 1.0            # nucleus mass of both sides; 1 = off
+
+    @property
+    def tq(self) -> float:
+        return self.temperature if self.draft_temperature is None else self.draft_temperature
 
     @property
     def key(self) -> str:
+        """Name of the tuned tau (a greedy batch shares the tau of its sampled twin)."""
         return self.name if self.alpha is None or self.name != "c5" else f"c5_a{self.alpha:g}"
+
+    @property
+    def label(self) -> str:
+        return "c5_greedy" if self.greedy else self.key
 
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
@@ -83,6 +97,12 @@ for _a, _s in ((0.4, 1051), (0.6, 1052), (0.8, 1053), (0.9, 1054)):
     WORKLOADS[f"c5_a{_a:g}"] = Workload("c5", B=1024, K=4, V=128256, dtype="bf16", temperature=1.0,
                                         top_k=0, seed=_s, alpha=_a)
 WORKLOADS["c5_greedy"] = WORKLOADS["c5_a0.8"].with_(temperature=0.0, greedy=True)
+# Sampling-parameter variants of the largest batch: nucleus truncation on both sides, and a
+# draft that samples at its own, lower temperature (T_q = 0.5 under a target at T = 1).
+WORKLOADS["c5_topp0.9"] = Workload("c5_topp0.9", B=1024, K=4, V=128256, dtype="bf16", temperature=1.0,
+                                   top_k=0, seed=1061, alpha=0.8, top_p=0.9)
+WORKLOADS["c5_tq0.5"] = Workload("c5_tq0.5", B=1024, K=4, V=128256, dtype="bf16", temperature=1.0,
+                                 top_k=0, seed=1062, alpha=0.45, draft_temperature=0.5)
 
 
 def get(name: str, **overrides) -> Workload:
@@ -139,7 +159,8 @@ def k_per_row(w: Workload, requests: Optional[Sequence[int]] = None) -> np.ndarr
     return np.array([_rng(w.seed, _S_KB, int(b)).integers(lo, hi + 1) for b in reqs], np.int32)
 
 
-def _draft_token(zq: np.ndarray, T: float, top_k: int, greedy: bool, g: np.random.Generator) -> int:
+def _draft_token(zq: np.ndarray, T: float, top_k: int, greedy: bool, g: np.random.Generator,
+                 top_p: float = 1.0) -> int:
     """The draft model's own sample from its row (Gumbel-max; argmax when greedy)."""
     z = zq.astype(np.float64)
     if greedy:
@@ -147,6 +168,12 @@ def _draft_token(zq: np.ndarray, T: float, top_k: int, greedy: bool, g: np.rando
     if 0 < top_k < z.shape[0]:
         kth = np.partition(z, z.shape[0] - top_k)[z.shape[0] - top_k]
         z = np.where(z >= kth, z, -np.inf)
+    if top_p < 1.0:  # the draft sampler's nucleus: most likely tokens up to mass top_p
+        w = np.exp((z - z.max()) / T)
+        order = np.argsort(-z, kind="stable")
+        cum = np.cumsum(w[order]) / w.sum()
+        cut = z[order[min(int(np.searchsorted(cum, np.float32(top_p))), len(z) - 1)]]
+        z = np.where(z >= cut, z, -np.inf)
     u = g.random(z.shape[0])
     gumbel = -np.log(-np.log(np.clip(u, 1e-300, None)))
     return int(np.argmax(z / T + gumbel))
@@ -176,7 +203,7 @@ def _request(w: Workload, tau: float, bias_v: np.ndarray, Kb: int, b: int, p_out
     x_out[:] = 0
     for j in range(Kb):
         zq = bf16_bits_to_f32(q_out[j]) if bf else q_out[j]
-        x_out[j] = _draft_token(zq, w.temperature, w.top_k, w.greedy, g)
+        x_out[j] = _draft_token(zq, w.tq, w.top_k, w.greedy, g, w.top_p)
 
 
 def uniforms(w: Workload, requests: Sequence[int]):
@@ -195,7 +222,8 @@ def generate(w: Workload, requests: Optional[Sequence[int]] = None, threads: int
     """Materialise a workload (or the listed requests of it) as host arrays.
 
     Returns dict(p [n, K+1, V], q [n, K, V] (float32, or uint16 bf16 bits), draft [n, K] int32,
-    k_per_row [n] int32, ua [n, K] f32, ur [n] f32, temperature, top_k, workload)."""
+    k_per_row [n] int32, ua [n, K] f32, ur [n] f32, temperature, draft_temperature, top_k, top_p,
+    workload)."""
     tau = tau_of(w) if tau is None else tau
     reqs = np.arange(w.B) if requests is None else np.asarray(requests, np.int64)
     n = len(reqs)
@@ -218,7 +246,8 @@ def generate(w: Workload, requests: Optional[Sequence[int]] = None, threads: int
             one(i)
     ua, ur = uniforms(w, reqs)
     return dict(p=p, q=q, draft=x, k_per_row=kb.astype(np.int32), ua=ua, ur=ur,
-                temperature=float(w.temperature), top_k=int(w.top_k), workload=w)
+                temperature=float(w.temperature), draft_temperature=float(w.tq), top_k=int(w.top_k),
+                top_p=float(w.top_p), workload=w)
 
 
 def algorithmic_bytes(w: Workload, kb: np.ndarray) -> int:
