@@ -22,6 +22,7 @@
 // the final draw L2-resident.  There is no tensor-core work: nothing here is a contraction.
 
 #include <cuda_runtime.h>
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 
@@ -252,6 +253,17 @@ __device__ __forceinline__ void load_chunk(const T* __restrict__ base, int n, fl
       const int e = i * kThreads + t;
       v[i] = e < n ? load1<T>(base + e) : -INFINITY;
     }
+  }
+}
+
+// The thread's 16-byte vectors of the chunk at `base` (16-byte aligned), not yet unpacked;
+// vectors at or past n read nothing.
+template <typename T>
+__device__ __forceinline__ void load_raw(const T* __restrict__ base, int n, uint4 (&raw)[Cfg<T>::LOADS]) {
+#pragma unroll
+  for (int l = 0; l < Cfg<T>::LOADS; ++l) {
+    const int e0 = (l * kThreads + threadIdx.x) * Cfg<T>::VW;
+    raw[l] = e0 < n ? ldg_stream(base + e0) : make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
@@ -1149,26 +1161,27 @@ __device__ void topk_row_exact(const Params& P, const T* row, float c2, uint32_t
 }
 
 // Nucleus (top-p) of one row, after its temperature and its top-k threshold `thr`: the smallest
-// set of most likely logits whose mass reaches top_p of the row's kept mass, with the whole tie
+// set of most likely logits whose mass reaches top_p of the row's kept mass S, with the whole tie
 // group at the cut (gsyq.cn §3.3 names top_p among the parameters both sides share).  Every
-// logit's weight w = 2^x, x = (z - M) * c2, is computed the same way in every pass, so all
-// passes agree on it.
-//   1. One pass bins the weights by u = -2x into 31 buckets of half a binade each plus a tail
-//      bucket (u >= 31), each thread in its own column of shared memory (no atomics), keeping
-//      mass and count; the tail (almost every logit of a long row) is only counted, its mass is
-//      the row's total S less the other buckets.  The bucket where the mass counted from the top
-//      first reaches top_p * S holds the cut.
-//   2. If that bucket holds at most kNucCap logits, one more pass gathers them (key, w) into
-//      shared memory; a bitonic sort by key and a scan from the top give the exact cut key.
-//   3. Otherwise the bucket is split by 4-bit digits of the key, most significant first, one
-//      pass per digit, until the part holding the cut is small enough to gather (or is a single
-//      key).
-// S is the row's kept mass relative to M (before top-p).  Returns the nucleus mass relative to M
-// and the cut as a logit value.  All threads of the block call it; `nbuf` is kNucBytes of shared
-// memory.
+// logit's weight w = 2^x, x = (z - M) * c2, and its bucket, floor(-2x) capped at 31 (half a
+// binade per bucket; bucket 31 is the tail, w < 2^-15.5), are computed the same way everywhere,
+// so all steps agree on them.  The tail's mass is S less the other buckets.
+//   Common path (nucleus_row): one read of the row lists the head logits (buckets 0..30, a few
+//   percent of a long row) in shared memory; their buckets give the one holding the cut; its
+//   logits, sorted by key, give the exact cut (nuc_select).
+//   Multi-pass path, when the head does not fit, the cut lies in the tail, or its bucket holds
+//   more than kNucCap logits: one pass bins every logit by bucket, each thread in its own column
+//   of shared memory (no atomics); then the bucket holding the cut is split by 4-bit digits of
+//   the key, one pass per digit, until the part holding the cut fits kNucCap (or is one key);
+//   a last pass gathers it for nuc_select.
 constexpr int kNucBins = 32;
-constexpr int kNucCap = 4096;
+constexpr int kNucCap = 2048;
 constexpr size_t kNucBytes = (size_t)kNucBins * kThreads * (sizeof(float) + sizeof(uint16_t));
+
+// The bucket of a logit: floor(-2x), x = (z - M) * c2 <= 0, capped at the tail bucket.
+__device__ __forceinline__ int nuc_bucket_of(float z, float M, float c2) {
+  return min(kNucBins - 1, __float2int_rd(-2.0f * ((z - M) * c2)));  // z <= M: never negative
+}
 
 struct NucSel {     // which logits the current pass looks at
   int bucket;       // level-0 bucket (-1: all kept logits)
@@ -1176,7 +1189,6 @@ struct NucSel {     // which logits the current pass looks at
   uint32_t prefix;  // their value
 };
 
-__device__ __forceinline__ int nuc_bucket(float x) { return (int)fminf(31.0f, floorf(-2.0f * x)); }
 
 // One pass over the row: per-thread bins (mass, count) of the selected logits, by level-0 bucket
 // (shift < 0) or by the key digit at `shift`; or, with `gather`, the selected logits themselves.
@@ -1209,7 +1221,7 @@ __device__ __forceinline__ void nuc_pass(const Params& P, const T* row, float M,
     for (int i = 0; i < Cfg<T>::PER; ++i) {
       const uint32_t k = fkey(v[i]);
       const float x = (v[i] - M) * c2;
-      const int bk = nuc_bucket(x);
+      const int bk = nuc_bucket_of(v[i], M, c2);
       const bool in = v[i] > -INFINITY && k >= kthr && (sel.bucket < 0 || bk == sel.bucket) &&
                       (k & sel.mask) == sel.prefix;
       if (!gather) {
@@ -1293,10 +1305,237 @@ __device__ __forceinline__ void nuc_pick(unsigned char* nbuf, Smem& sm, int nbin
   __syncthreads();
 }
 
+// Exact cut among n gathered logits (keys gk, weights gw, n <= kNucCap) that hold the cut, with
+// `above` the mass of every kept logit above them: a bitonic sort by key, descending, then a scan
+// from the top to the first tie group where the mass reaches the target.  Leaves the nucleus mass
+// in sm.nuc_above and the cut key in sm.nuc_key.
+__device__ __forceinline__ void nuc_select(uint32_t* gk, float* gw, int n, float above, float target, Smem& sm) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  int N = 32;
+  while (N < n) N <<= 1;
+  for (int i = n + t; i < N; i += kThreads) {
+    gk[i] = 0u;  // below every real key: sorts last
+    gw[i] = 0.0f;
+  }
+  __syncthreads();
+  for (int k = 2; k <= N; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = t; i < N; i += kThreads) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const bool desc = (i & k) == 0;
+          const uint32_t a = gk[i], b = gk[ixj];
+          if (desc ? (a < b) : (a > b)) {
+            gk[i] = b;
+            gk[ixj] = a;
+            const float wa = gw[i];
+            gw[i] = gw[ixj];
+            gw[ixj] = wa;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  if (warp == 0) {
+    float cum = above;
+    int at = -1;
+    for (int base = 0; base < n && at < 0; base += 32) {
+      const int i = base + lane;
+      const float w = i < n ? gw[i] : 0.0f;
+      float incl = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned hit = __ballot_sync(0xFFFFFFFFu, i < n && cum + incl >= target);
+      if (hit) {
+        const int L = __ffs(hit) - 1;
+        at = base + L;
+        cum += __shfl_sync(0xFFFFFFFFu, incl, L);
+      } else {
+        cum += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      }
+    }
+    if (lane == 0) {
+      if (at < 0) at = n - 1;  // rounding left the target unreached: keep everything gathered
+      const uint32_t kc = gk[at];
+      for (int i = at + 1; i < n && gk[i] == kc; ++i) cum += gw[i];  // the rest of the tie group
+      sm.nuc_above = cum;
+      sm.nuc_key = kc;
+    }
+  }
+  __syncthreads();
+}
+
+// Shared-memory layout of the nucleus search (kNucBufBytes): the common path keeps the row's head
+// logits in per-thread columns (entry i of thread t at i * kThreads + t, in the row's own type)
+// followed by per-thread bins that later hold the sort area; the multi-pass path reuses the same
+// bytes for its bins and gathers.  The common path's buckets are whole binades of the weight:
+// hb = floor(-x) capped at 15 (the tail, w < 2^-15), then 16 sub-buckets of the chosen one.
+constexpr int kHeadBins = 16;
+constexpr size_t kNucListBytes = 49152;
+constexpr size_t kNucBinBytes = (size_t)kHeadBins * kThreads * sizeof(float);
+constexpr size_t kNucBufBytes = kNucListBytes + kNucBinBytes;
+static_assert(kNucBufBytes >= kNucBytes, "nucleus buffer");
+static_assert(kNucBinBytes >= (size_t)kNucCap * (sizeof(uint32_t) + sizeof(float)), "nucleus sort area");
+
+// Per-thread bins (column t of `bins`, nbins <= 32) summed over the block; warp 0 walks them from
+// bin 0 (the heaviest weights) and picks the bin where `above` plus the mass so far first reaches
+// the target.  With `tail_from_S`, the last bin's mass is S less the others.  Results in sm.nuc_*.
+__device__ __forceinline__ void nuc_walk_bins(const float* bins, int nbins, Smem& sm, float above, float target,
+                                              bool tail_from_S, float S) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  for (int b = warp; b < nbins; b += kWarps) {
+    float s = 0.0f;
+#pragma unroll
+    for (int j = lane; j < kThreads; j += 32) s += bins[b * kThreads + j];
+    s = warp_sum(s);
+    if (lane == 0) sm.incl[b] = s;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float s = lane < nbins ? sm.incl[lane] : 0.0f;
+    if (tail_from_S) {
+      const float head = warp_sum(lane < nbins - 1 ? s : 0.0f);
+      if (lane == nbins - 1) s = fmaxf(S - head, 0.0f);
+    }
+    float incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const unsigned hit = __ballot_sync(0xFFFFFFFFu, lane < nbins && above + incl >= target);
+    const unsigned nz = __ballot_sync(0xFFFFFFFFu, s > 0.0f);
+    const int L = hit ? __ffs(hit) - 1 : (nz ? 31 - __clz(nz) : 0);
+    if (lane == L) {
+      sm.nuc_digit = L;
+      sm.nuc_above = above + incl - s;
+      sm.nuc_bin = s;
+    }
+    if (lane == 0) sm.nuc_n = 0;
+  }
+  __syncthreads();
+}
+
+// S is the row's kept mass relative to M (before top-p).  Returns the nucleus mass relative to M
+// and the cut as a logit value.  All threads of the block call it; `nbuf` is kNucBufBytes of
+// shared memory.
 template <typename T, bool VEC>
 __device__ __forceinline__ void nucleus_row(const Params& P, const T* row, float M, float c2, float thr, float S,
                                             unsigned char* nbuf, Smem& sm, float& S_kept, float& cut) {
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int t = threadIdx.x;
+  const float target = P.top_p * S;
+  // ---- common path: one read of the row lists the head logits in per-thread columns ----
+  constexpr int kCap = (int)(kNucListBytes / sizeof(T) / kThreads);
+  float* bins = reinterpret_cast<float*>(nbuf + kNucListBytes);
+  // Every head logit (hb < 15) lies above zcut: the bound M - 15 / c2, widened by a relative
+  // 1e-4 against rounding, or the top-k threshold if that is higher.  A listed logit whose bucket
+  // turns out to be the tail is ignored below.
+  const float zcut = fmaxf(M - (15.0f / c2) * 1.0001f, thr == -INFINITY ? -FLT_MAX : nextafterf(thr, -INFINITY));
+  int cnt = 0;
+  auto scan = [&](const float (&v)[Cfg<T>::PER]) {
+#pragma unroll
+    for (int i = 0; i < Cfg<T>::PER; ++i) {
+      // an overflowing column keeps rewriting its last slot and sends the row to the multi-pass path
+      const bool in = v[i] > zcut;
+      const int slot = min(cnt, kCap - 1) * kThreads + t;
+      if (in) {
+        if (sizeof(T) == 2)
+          reinterpret_cast<uint16_t*>(nbuf)[slot] = (uint16_t)(__float_as_uint(v[i]) >> 16);
+        else
+          reinterpret_cast<float*>(nbuf)[slot] = v[i];
+      }
+      cnt += in;
+    }
+  };
+  if (VEC) {  // two chunks' loads in flight ahead of the one being scanned
+    uint4 r0[Cfg<T>::LOADS], r1[Cfg<T>::LOADS];
+    load_raw<T>(row, min(Cfg<T>::CH, P.V), r0);
+    if (P.nchunk > 1) load_raw<T>(row + Cfg<T>::CH, min(Cfg<T>::CH, P.V - Cfg<T>::CH), r1);
+    for (int c = 0; c < P.nchunk; ++c) {
+      const int v0 = c * Cfg<T>::CH;
+      float v[Cfg<T>::PER];
+      unpack<T>(r0, min(Cfg<T>::CH, P.V - v0), v);
+#pragma unroll
+      for (int l = 0; l < Cfg<T>::LOADS; ++l) r0[l] = r1[l];
+      if (c + 2 < P.nchunk) load_raw<T>(row + v0 + 2 * Cfg<T>::CH, min(Cfg<T>::CH, P.V - v0 - 2 * Cfg<T>::CH), r1);
+      scan(v);
+    }
+  } else {
+    for (int c = 0; c < P.nchunk; ++c) {
+      const int v0 = c * Cfg<T>::CH;
+      float v[Cfg<T>::PER];
+      load_chunk<T, VEC>(row + v0, min(Cfg<T>::CH, P.V - v0), v);
+      scan(v);
+    }
+  }
+  auto entry = [&](int i) -> float {
+    return sizeof(T) == 2 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(nbuf)[i * kThreads + t] << 16)
+                          : reinterpret_cast<const float*>(nbuf)[i * kThreads + t];
+  };
+  // the binade and sub-bucket of a listed logit, from -x exactly as its weight 2^x is formed
+  auto hbin = [&](float nx) { return min(kHeadBins - 1, __float2int_rd(nx)); };
+  auto sbin = [&](float nx, int hb) { return min(kHeadBins - 1, __float2int_rd((nx - (float)hb) * 16.0f)); };
+  const bool overflow = __syncthreads_or(cnt > kCap);
+  bool done = false;
+  if (!overflow) {
+#pragma unroll
+    for (int b = 0; b < kHeadBins; ++b) bins[b * kThreads + t] = 0.0f;
+    for (int i = 0; i < cnt; ++i) {
+      const float z = entry(i);
+      const float x = (z - M) * c2;
+      const int hb = hbin(-x);
+      if (hb < kHeadBins - 1) bins[hb * kThreads + t] += ex2(x);
+    }
+    __syncthreads();
+    nuc_walk_bins(bins, kHeadBins, sm, 0.0f, target, true, S);
+    const int bsel = sm.nuc_digit;
+    if (bsel < kHeadBins - 1) {
+      const float above1 = sm.nuc_above;
+#pragma unroll
+      for (int b = 0; b < kHeadBins; ++b) bins[b * kThreads + t] = 0.0f;
+      for (int i = 0; i < cnt; ++i) {
+        const float z = entry(i);
+        const float x = (z - M) * c2;
+        if (hbin(-x) == bsel) bins[sbin(-x, bsel) * kThreads + t] += ex2(x);
+      }
+      __syncthreads();
+      nuc_walk_bins(bins, kHeadBins, sm, above1, target, false, 0.0f);
+      const int ssel = sm.nuc_digit;
+      const float above2 = sm.nuc_above;
+      // gather the chosen sub-bucket into the sort area (the bins are consumed)
+      uint32_t* sk = reinterpret_cast<uint32_t*>(bins);
+      float* sw = bins + kNucCap;
+      for (int i = 0; i < cnt; ++i) {
+        const float z = entry(i);
+        const float x = (z - M) * c2;
+        if (hbin(-x) == bsel && sbin(-x, bsel) == ssel) {
+          const int idx = atomicAdd(&sm.nuc_n, 1);
+          if (idx < kNucCap) {
+            sk[idx] = fkey(z);
+            sw[idx] = ex2(x);
+          }
+        }
+      }
+      __syncthreads();
+      const int n = sm.nuc_n;
+      if (n <= kNucCap) {
+        nuc_select(sk, sw, n, above2, target, sm);
+        done = true;
+      }
+    }
+  }
+  if (done) {
+    S_kept = sm.nuc_above;
+    cut = keyf(sm.nuc_key);
+    __syncthreads();
+    return;
+  }
+  __syncthreads();
+  // ---- multi-pass path: a crowded head, a cut in the tail, or a large boundary bucket ----
   const uint32_t kthr = thr == -INFINITY ? 0u : fkey(thr);  // keys below it are outside top-k
   NucSel sel{-1, 0u, 0u};
   nuc_pass<T, VEC>(P, row, M, c2, kthr, sel, -1, false, nbuf, sm);
@@ -1328,66 +1567,8 @@ __device__ __forceinline__ void nucleus_row(const Params& P, const T* row, float
   __syncthreads();
   nuc_pass<T, VEC>(P, row, M, c2, kthr, sel, 0, true, nbuf, sm);
   const int n = min((int)count, sm.nuc_n);
-  uint32_t* gk = reinterpret_cast<uint32_t*>(nbuf);
-  float* gw = reinterpret_cast<float*>(nbuf + (size_t)kNucCap * sizeof(uint32_t));
-  int N = 32;
-  while (N < n) N <<= 1;
-  for (int i = n + t; i < N; i += kThreads) {
-    gk[i] = 0u;  // below every real key: sorts last
-    gw[i] = 0.0f;
-  }
-  __syncthreads();
-  // bitonic sort, descending by key (equal keys end up adjacent)
-  for (int k = 2; k <= N; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = t; i < N; i += kThreads) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const bool desc = (i & k) == 0;
-          const uint32_t a = gk[i], b = gk[ixj];
-          if (desc ? (a < b) : (a > b)) {
-            gk[i] = b;
-            gk[ixj] = a;
-            const float wa = gw[i];
-            gw[i] = gw[ixj];
-            gw[ixj] = wa;
-          }
-        }
-      }
-      __syncthreads();
-    }
-  }
-  if (warp == 0) {
-    const float target = sm.nuc_target;
-    float cum = above;
-    int at = -1;
-    for (int base = 0; base < n && at < 0; base += 32) {
-      const int i = base + lane;
-      const float w = i < n ? gw[i] : 0.0f;
-      float incl = w;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const unsigned hit = __ballot_sync(0xFFFFFFFFu, i < n && cum + incl >= target);
-      if (hit) {
-        const int L = __ffs(hit) - 1;
-        at = base + L;
-        cum += __shfl_sync(0xFFFFFFFFu, incl, L);
-      } else {
-        cum += __shfl_sync(0xFFFFFFFFu, incl, 31);
-      }
-    }
-    if (lane == 0) {
-      if (at < 0) at = n - 1;  // rounding left the target unreached: keep everything gathered
-      const uint32_t kc = gk[at];
-      for (int i = at + 1; i < n && gk[i] == kc; ++i) cum += gw[i];  // the rest of the tie group
-      sm.nuc_above = cum;
-      sm.nuc_key = kc;
-    }
-  }
-  __syncthreads();
+  nuc_select(reinterpret_cast<uint32_t*>(nbuf), reinterpret_cast<float*>(nbuf + (size_t)kNucCap * sizeof(uint32_t)),
+             n, above, sm.nuc_target, sm);
   S_kept = sm.nuc_above;
   cut = keyf(sm.nuc_key);
   __syncthreads();
@@ -2139,7 +2320,7 @@ static size_t finish_smem(int mode, int V, int es, bool vec, bool nuc) {
   const int ntile = (V + kTile - 1) / kTile;
   const int nch = (V + kChunkBytes / es - 1) / (kChunkBytes / es);
   size_t bytes = (size_t)(ntile > nch ? ntile : nch) * sizeof(float);  // tile / chunk sums
-  if (nuc && mode == kTopK && bytes < kNucBytes) bytes = kNucBytes;  // the nucleus bins / gathered logits
+  if (nuc && mode == kTopK && bytes < kNucBufBytes) bytes = kNucBufBytes;  // the nucleus search
   if (mode == kGreedy) return 16;
   if (mode == kTopK) bytes += (size_t)kWarps * kRowCap * sizeof(uint2);
   if (vec) bytes += (size_t)kDrawStages * kDrawStageBytes;  // cp.async ring of the CDF pass
@@ -2175,9 +2356,9 @@ static cudaError_t launch_t(const Params& P, uint32_t items, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (nuc && MODE == kSample) {
     auto kn = nucleus_kernel<T, VEC>;
-    e = prepare(kn, kNucBytes);
+    e = prepare(kn, kNucBufBytes);
     if (e != cudaSuccess) return e;
-    kn<<<(unsigned)((uint64_t)P.B * P.R), kThreads, kNucBytes, st>>>(P);
+    kn<<<(unsigned)((uint64_t)P.B * P.R), kThreads, kNucBufBytes, st>>>(P);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
