@@ -10,7 +10,9 @@ The C ABI is declared in ``include/spec_verify.h``; the names here mirror it:
   draft_temperature=None, top_p=1.0)`` -> ``(tokens [B, K+1] int32, num_accepted [B] int32,
   stats dict | None)`` on device tensors, through ``spec_verify_ex``;
 * ``verify_host(...)`` the same on host (numpy / CPU torch) arrays through ``spec_verify_host_ex``;
-* ``workspace_bytes(B, K, V, dtype, top_k)``.
+* ``workspace_bytes(B, K, V, dtype, top_k)``;
+* ``Controller(...)``: the host-side draft-length controller of ``include/spec_control.h``
+  (2kiu.com/news/5895634 §4.4 and §7), fed with each batch's ``num_accepted``.
 
 Logits are ``torch.float32`` or ``torch.bfloat16`` tensors ``p [B, K+1, V]`` and ``q [B, K, V]``
 (q may be None at temperature 0).  The verify rule (cf-1.com/news/5155685 §2.2,
@@ -44,6 +46,9 @@ MAX_TOPK = 256
 
 EXPORTS = ("spec_verify_workspace_bytes", "spec_verify", "spec_verify_ex", "spec_verify_host_staging_bytes",
            "spec_verify_host", "spec_verify_host_ex", "spec_verify_static", "spec_verify_status_string")
+CONTROL_EXPORTS = ("spec_ctrl_default_config", "spec_ctrl_create", "spec_ctrl_destroy", "spec_ctrl_update",
+                   "spec_ctrl_skip", "spec_ctrl_k", "spec_ctrl_window_mean", "spec_ctrl_window_fill",
+                   "spec_ctrl_totals")
 STATIC_SCRATCH_BYTES = 16 << 20
 
 
@@ -67,6 +72,12 @@ class SamplingStruct(ctypes.Structure):
 def _sampling(temperature, draft_temperature, top_k, top_p) -> SamplingStruct:
     tq = temperature if draft_temperature is None else draft_temperature
     return SamplingStruct(float(temperature), float(tq), int(top_k), float(top_p))
+
+
+class ControlConfig(ctypes.Structure):
+    _fields_ = [("k_init", ctypes.c_int32), ("k_min", ctypes.c_int32), ("k_max", ctypes.c_int32),
+                ("window", ctypes.c_int32), ("raise_above", ctypes.c_float), ("lower_below", ctypes.c_float),
+                ("disable_below", ctypes.c_float), ("probe_after", ctypes.c_int32)]
 
 
 _lib = None
@@ -111,6 +122,26 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
             lib.spec_verify_static.restype = I
             lib.spec_verify_status_string.argtypes = [I]
             lib.spec_verify_status_string.restype = ctypes.c_char_p
+            CP = ctypes.POINTER(ControlConfig)
+            lib.spec_ctrl_default_config.argtypes = [CP]
+            lib.spec_ctrl_default_config.restype = None
+            lib.spec_ctrl_create.argtypes = [CP]
+            lib.spec_ctrl_create.restype = P
+            lib.spec_ctrl_destroy.argtypes = [P]
+            lib.spec_ctrl_destroy.restype = None
+            lib.spec_ctrl_update.argtypes = [P, P, P, I, I]
+            lib.spec_ctrl_update.restype = I
+            lib.spec_ctrl_skip.argtypes = [P]
+            lib.spec_ctrl_skip.restype = I
+            lib.spec_ctrl_k.argtypes = [P]
+            lib.spec_ctrl_k.restype = I
+            lib.spec_ctrl_window_mean.argtypes = [P]
+            lib.spec_ctrl_window_mean.restype = ctypes.c_double
+            lib.spec_ctrl_window_fill.argtypes = [P]
+            lib.spec_ctrl_window_fill.restype = I
+            L = ctypes.POINTER(ctypes.c_int64)
+            lib.spec_ctrl_totals.argtypes = [P, L, L, L]
+            lib.spec_ctrl_totals.restype = None
             _lib = lib
     return _lib
 
@@ -296,3 +327,67 @@ def verify_host(p, q, draft, k_per_row=None, u_accept=None, u_resample=None, tem
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_verify_host_ex")
     return tokens, nacc
+
+
+class Controller:
+    """The draft-length controller (``include/spec_control.h``): record each verified batch's
+    ``num_accepted`` with :meth:`update` (or a batch decoded without drafts with :meth:`skip`);
+    both return the K for the next batch, 0 meaning speculation is off.  Host-side; keyword
+    arguments override the pages' defaults (k_init 4, k in [2, 10], window 100, raise above 0.8,
+    lower below 0.6, switch off below 0.5, probe again after 100 batches)."""
+
+    def __init__(self, **overrides):
+        lib = load()
+        cfg = ControlConfig()
+        lib.spec_ctrl_default_config(ctypes.byref(cfg))
+        for k, v in overrides.items():
+            if not hasattr(cfg, k):
+                raise TypeError(f"unknown controller setting {k}")
+            setattr(cfg, k, v)
+        self.config = cfg
+        self._lib = lib
+        self._h = lib.spec_ctrl_create(ctypes.byref(cfg))
+        if not self._h:
+            raise ValueError("controller settings out of range")
+
+    def __del__(self):
+        h, self._h = getattr(self, "_h", None), None
+        if h:
+            self._lib.spec_ctrl_destroy(h)
+
+    def update(self, num_accepted, k_per_row=None, K_used: Optional[int] = None) -> int:
+        """Record one verified batch (host arrays or tensors; copied to the host if needed)."""
+        n = np.ascontiguousarray(_host_i32(num_accepted))
+        kp = None if k_per_row is None else np.ascontiguousarray(_host_i32(k_per_row))
+        K = self.k if K_used is None else int(K_used)
+        r = self._lib.spec_ctrl_update(self._h, n.ctypes.data, None if kp is None else kp.ctypes.data,
+                                       int(n.shape[0]), K)
+        if r < 0:
+            raise ValueError("spec_ctrl_update rejected its arguments")
+        return r
+
+    def skip(self) -> int:
+        return self._lib.spec_ctrl_skip(self._h)
+
+    @property
+    def k(self) -> int:
+        return self._lib.spec_ctrl_k(self._h)
+
+    @property
+    def window_mean(self) -> float:
+        return self._lib.spec_ctrl_window_mean(self._h)
+
+    @property
+    def window_fill(self) -> int:
+        return self._lib.spec_ctrl_window_fill(self._h)
+
+    def totals(self) -> Tuple[int, int, int]:
+        a, p, b = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        self._lib.spec_ctrl_totals(self._h, ctypes.byref(a), ctypes.byref(p), ctypes.byref(b))
+        return a.value, p.value, b.value
+
+
+def _host_i32(a) -> np.ndarray:
+    if hasattr(a, "detach"):  # a torch tensor
+        a = a.detach().cpu().numpy()
+    return np.asarray(a, dtype=np.int32)

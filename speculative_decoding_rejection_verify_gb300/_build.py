@@ -8,7 +8,9 @@ import sys
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 SRC = os.path.join(PKG, "csrc", "spec_verify.cu")
+SRC_CTRL = os.path.join(PKG, "csrc", "spec_control.cpp")
 HDR = os.path.join(ROOT, "include", "spec_verify.h")
+HDR_CTRL = os.path.join(ROOT, "include", "spec_control.h")
 LIB = os.path.join(PKG, "libspecverify.so")
 
 NVCC_FLAGS = [
@@ -28,7 +30,7 @@ def stale() -> bool:
     if not os.path.exists(LIB):
         return True
     t = os.path.getmtime(LIB)
-    return any(os.path.getmtime(f) > t for f in (SRC, HDR, __file__))
+    return any(os.path.getmtime(f) > t for f in (SRC, SRC_CTRL, HDR, HDR_CTRL, __file__))
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
@@ -36,7 +38,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if not force and not stale():
         return LIB
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"), SRC, "-o", tmp]
+    cmd = [nvcc(), *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"), SRC, SRC_CTRL, "-o", tmp]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     subprocess.run(cmd, check=True)

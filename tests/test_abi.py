@@ -9,7 +9,9 @@ import pytest
 import speculative_decoding_rejection_verify_gb300 as sv
 from speculative_decoding_rejection_verify_gb300 import _build
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "spec_verify.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+HEADER = os.path.join(INCLUDE, "spec_verify.h")
+HEADERS = [os.path.join(INCLUDE, f) for f in sorted(os.listdir(INCLUDE)) if f.endswith(".h")]
 
 
 @pytest.fixture(scope="module")
@@ -18,15 +20,17 @@ def lib():
     return sv.load()
 
 
-def declared_functions():
-    src = open(HEADER).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(spec_\w+)\s*\(", src, flags=re.M)))
+def declared_functions(path=None):
+    names = set()
+    for h in ([path] if path else HEADERS):
+        src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(spec_\w+)\s*\(", src, flags=re.M))
+    return sorted(names)
 
 
 def test_header_declares_the_entry_points():
-    names = declared_functions()
-    assert set(names) == set(sv.EXPORTS), names
+    assert set(declared_functions(HEADER)) == set(sv.EXPORTS)
+    assert set(declared_functions(os.path.join(INCLUDE, "spec_control.h"))) == set(sv.CONTROL_EXPORTS)
 
 
 def test_library_exports_every_declared_symbol(lib):
