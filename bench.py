@@ -175,6 +175,17 @@ def describe(w: W.Workload) -> str:
         (f" alpha~{w.alpha:g}" if w.alpha is not None and not w.greedy else "")
 
 
+def launches_per_step(w: W.Workload) -> int:
+    """Kernels of one step: the streaming pass and the per-request pass, plus the ragged row
+    table, the nucleus pass (top-p without top-k) and, for sampling, the q(x) kernel."""
+    n = 2 + (w.ragged is not None)
+    if w.temperature > 0 and w.top_p < 1.0 and not (0 < w.top_k < w.V):
+        n += 1
+    if w.K == 0 and w.temperature >= 0:
+        n += 1
+    return n
+
+
 def cpu_baseline(w: W.Workload, budget_requests: int, seconds: float = 10.0):
     """The oracle, as it stands, on the host cores over a bounded sample of the workload: the
     first `budget_requests` requests, verified repeatedly until about `seconds` have passed."""
@@ -281,8 +292,20 @@ def run_gpu(args, w: W.Workload):
     nacc = torch.empty((B,), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    sampling = K == 0  # draft-token sampling: one draw per row through spec_sample
+    if sampling:
+        for c in copies:
+            c["rows"] = c["p"][:, 0, :].contiguous()
+        sws = torch.zeros(sv.load().spec_sample_workspace_bytes(B, V, dt_code, w.top_k), dtype=torch.uint8,
+                          device=dev)
+        sprob = torch.empty((B,), dtype=torch.float32, device=dev)
+
     def launch(i, st, mid=None):
         c = copies[i & 1]
+        if sampling:
+            sv.sample(c["rows"], c["ur"], w.temperature, w.top_k, w.top_p, workspace_tensor=sws, stream=st,
+                      out=(nacc, sprob))
+            return
         sv.verify(c["p"], c["q"], c["x"], c["k"], c["ua"], c["ur"], w.temperature, w.top_k,
                   workspace_tensor=ws, stream=st, out=(tok, nacc), pass1_event=mid,
                   draft_temperature=w.tq, top_p=w.top_p)
@@ -327,25 +350,25 @@ def run_gpu(args, w: W.Workload):
         t_start.record(stream)
         for i in range(args.steps):
             ev[i][0].record(stream)
-            step(i, None if graphs else ev[i][1])
+            step(i, None if (graphs or sampling) else ev[i][1])
             ev[i][2].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
         barrier(world)
     total_ms = t_start.elapsed_time(t_end)
-    if graphs is None:
+    if graphs is None and not sampling:
         pass1_ms = statistics.mean(a.elapsed_time(m) for a, m, _ in ev)
         pass2_ms = statistics.mean(m.elapsed_time(z) for _, m, z in ev)
     else:  # no event between the passes inside a graph: the whole step stands for the pass
         pass1_ms = statistics.mean(a.elapsed_time(z) for a, _, z in ev)
         pass2_ms = None
     step_ms = max_over_ranks(total_ms / args.steps, world, dev)
-    all_positions = sum_over_ranks(positions, world, dev)
+    all_positions = sum_over_ranks(B if sampling else positions, world, dev)
     value = all_positions / (step_ms * 1e-3)
 
     # end to end: host buffers through spec_verify_host (H2D + verify + D2H, synchronous)
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and not sampling:
         pin = lambda a: None if a is None else torch.from_numpy(a).pin_memory().numpy()  # noqa: E731
         hp = dict(p=pin(d["p"]), q=None if greedy else pin(d["q"]), x=pin(d["draft"]), k=pin(kb) if ragged else None,
                   ua=None if greedy else pin(d["ua"]), ur=None if greedy else pin(d["ur"]))
@@ -379,7 +402,8 @@ def run_gpu(args, w: W.Workload):
     else:
         l2_note = f"hot L2: both input copies ({2 * in_bytes / 1e6:.2f} MB) fit in L2 ({l2_bytes / 1e6:.0f} MB)"
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": "sampled tokens/s and logits GB/s" if sampling else METRIC, "value": value,
+        "unit": "tokens/s" if sampling else UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded generator; no dataset)",
         "config": {"workload": describe(w), "B_per_gpu": B, "K": K, "V": V, "temperature": w.temperature,
@@ -391,11 +415,12 @@ def run_gpu(args, w: W.Workload):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": traffic_for(w.label),
-                     "kernel": "stats_kernel (streaming pass)" if graphs is None else "whole step (graph replay)",
+                     "kernel": ("stats_kernel (streaming pass)" if graphs is None and not sampling else
+                                "whole step" + (" (graph replay)" if graphs else "")),
                      "per_launch_ms": pass1_ms,
                      "step_frac": logits_bytes / (step_ms * 1e-3) / 1e9 / peak,
                      "pass2_ms": pass2_ms},
-        "gpu_launches": args.steps * (3 if ragged else 2),
+        "gpu_launches": args.steps * launches_per_step(w),
         "clocks": clk.summary(),
     }
     if e2e is not None:

@@ -195,6 +195,26 @@ spec_status_t spec_verify_host_ex(const void* p_logits, const void* q_logits,
                                   int32_t* out_num_accepted, int32_t B, int32_t K_max, int32_t V,
                                   spec_dtype_t dtype, void* staging, size_t staging_bytes, void* stream);
 
+/*
+ * Draft-token sampling, the step before verification (gsyq.cn/news/428210 §3.1: the draft model
+ * proposes its tokens by sampling its own distribution): one token per row of `logits`, drawn
+ * from the row's distribution after temperature, top-k and top-p by the same inverse CDF as the
+ * verify step's bonus draw: x = the smallest v with u * S < C_v, C_v cumulative in ascending
+ * token id over the kept set (greedy argmax, lowest index, at temperature 0).  It is
+ * spec_verify_ex on a batch of `rows` requests with no drafts.
+ *   logits [rows, V] dtype (device); u [rows] float in [0, 1) (device; NULL iff temperature == 0);
+ *   sampling: temperature, top_k, top_p (draft_temperature is not used);
+ *   out_tokens [rows] int32 (device): the drawn token, -1 for a row with NaN / +inf logits;
+ *   out_prob [rows] float (device) or NULL: the drawn token's probability q(x) under that
+ *       distribution (1 in greedy mode, NaN where out_tokens is -1);
+ *   workspace: spec_sample_workspace_bytes(...) bytes of device memory, 256-B aligned.
+ * Errors as for spec_verify_ex.
+ */
+size_t spec_sample_workspace_bytes(int32_t rows, int32_t V, spec_dtype_t dtype, int32_t top_k);
+spec_status_t spec_sample(const void* logits, const float* u, const spec_sampling_t* sampling, int32_t* out_tokens,
+                          float* out_prob, int32_t rows, int32_t V, spec_dtype_t dtype, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
 /* Size of the fixed device array behind spec_verify_static (16 MiB). */
 #define SPEC_STATIC_SCRATCH_BYTES (16u << 20)
 

@@ -45,7 +45,8 @@ MAX_V = 2097152
 MAX_TOPK = 256
 
 EXPORTS = ("spec_verify_workspace_bytes", "spec_verify", "spec_verify_ex", "spec_verify_host_staging_bytes",
-           "spec_verify_host", "spec_verify_host_ex", "spec_verify_static", "spec_verify_status_string")
+           "spec_verify_host", "spec_verify_host_ex", "spec_verify_static", "spec_verify_status_string",
+           "spec_sample_workspace_bytes", "spec_sample")
 CONTROL_EXPORTS = ("spec_ctrl_default_config", "spec_ctrl_create", "spec_ctrl_destroy", "spec_ctrl_update",
                    "spec_ctrl_skip", "spec_ctrl_k", "spec_ctrl_window_mean", "spec_ctrl_window_fill",
                    "spec_ctrl_totals")
@@ -122,6 +123,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
             lib.spec_verify_static.restype = I
             lib.spec_verify_status_string.argtypes = [I]
             lib.spec_verify_status_string.restype = ctypes.c_char_p
+            lib.spec_sample_workspace_bytes.argtypes = [I, I, I, I]
+            lib.spec_sample_workspace_bytes.restype = Z
+            lib.spec_sample.argtypes = [P, P, ctypes.POINTER(SamplingStruct), P, P, I, I, I, P, Z, P]
+            lib.spec_sample.restype = I
             CP = ctypes.POINTER(ControlConfig)
             lib.spec_ctrl_default_config.argtypes = [CP]
             lib.spec_ctrl_default_config.restype = None
@@ -257,6 +262,39 @@ def verify(p, q, draft, k_per_row=None, u_accept=None, u_resample=None, temperat
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_verify_ex")
     return tokens, nacc, sd
+
+
+def sample(logits, u=None, temperature: float = 1.0, top_k: int = 0, top_p: float = 1.0, prob: bool = True,
+           workspace_tensor=None, stream=None, out=None):
+    """Draw one token per row of ``logits`` [rows, V] (device) with the uniforms ``u`` [rows]
+    through ``spec_sample``; returns (tokens [rows] int32, q(x) [rows] float32 | None)."""
+    torch = _torch()
+    lib = load()
+    if logits.dim() != 2:
+        raise ValueError("logits must be [rows, V]")
+    rows, V = logits.shape
+    dev = logits.device
+    dt = _dtype_code(logits)
+    _check(logits, "logits", (rows, V), logits.dtype, dev)
+    if u is not None:
+        _check(u, "u", (rows,), torch.float32, dev)
+    st = stream if stream is not None else torch.cuda.current_stream(dev)
+    if out is None:
+        tokens = torch.empty((rows,), dtype=torch.int32, device=dev)
+        pr = torch.empty((rows,), dtype=torch.float32, device=dev) if prob else None
+    else:
+        tokens, pr = out
+    nbytes = lib.spec_sample_workspace_bytes(rows, V, dt, int(top_k))
+    if nbytes == 0:
+        raise SpecVerifyError(1, "spec_sample_workspace_bytes")
+    ws = workspace_tensor if workspace_tensor is not None else workspace(nbytes, dev, st.cuda_stream)
+    smp = SamplingStruct(float(temperature), float(temperature), int(top_k), float(top_p))
+    rc = lib.spec_sample(_ptr(logits), _ptr(u), ctypes.byref(smp), tokens.data_ptr(),
+                         None if pr is None else pr.data_ptr(), rows, V, dt, ws.data_ptr(), ws.numel(),
+                         st.cuda_stream)
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_sample")
+    return tokens, pr
 
 
 _stage_cache: Dict[int, object] = {}

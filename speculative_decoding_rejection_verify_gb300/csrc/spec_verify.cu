@@ -2223,6 +2223,20 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const Params P) {
   }
 }
 
+// Sampling: q(x) of each drawn token, exp(z_x / T - the row's log-normaliser over its kept set);
+// 1 in greedy mode (the draft's one-hot); NaN for a row without a result.
+template <typename T>
+__global__ void __launch_bounds__(256) sample_prob_kernel(const T* __restrict__ logits, const int32_t* __restrict__ tok,
+                                                          const float* __restrict__ lognorm, float invT, int rows,
+                                                          int V, float* __restrict__ out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= rows) return;
+  const int y = tok[i];
+  float pr = NAN;
+  if (y >= 0 && y < V) pr = invT == 0.0f ? 1.0f : expf(load1<T>(logits + (size_t)i * V + y) * invT - lognorm[i]);
+  out[i] = pr;
+}
+
 // Ragged batches: a table of valid rows in request-major order, so no item is spent on padding.
 __global__ void __launch_bounds__(1024) build_rowmap(const int32_t* __restrict__ kpr, int B, int K,
                                                      int greedy, uint32_t* rowmap,
@@ -2573,6 +2587,45 @@ spec_status_t spec_verify_host(const void* p_logits, const void* q_logits,
   const spec_sampling_t sp = {temperature, temperature, top_k, 1.0f};
   return spec_verify_host_ex(p_logits, q_logits, draft_tokens, k_per_row, u_accept, u_resample, &sp,
                              out_tokens, out_num_accepted, B, K_max, V, dtype, staging, staging_bytes, stream);
+}
+
+size_t spec_sample_workspace_bytes(int32_t rows, int32_t V, spec_dtype_t dtype, int32_t top_k) {
+  const size_t ws = spec_verify_workspace_bytes(rows, 0, V, dtype, top_k);
+  if (ws == 0) return 0;
+  return ws + 2 * align256((size_t)rows * sizeof(int32_t));  // + accepted counts and normalisers
+}
+
+spec_status_t spec_sample(const void* logits, const float* u, const spec_sampling_t* sampling, int32_t* out_tokens,
+                          float* out_prob, int32_t rows, int32_t V, spec_dtype_t dtype, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  if (rows < 0 || V <= 0 || !sampling) return SPEC_ERR_INVALID_ARG;
+  if (V > SPEC_MAX_V) return SPEC_ERR_UNSUPPORTED;
+  if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED;
+  spec_sampling_t sp = *sampling;
+  sp.draft_temperature = sp.temperature > 0.0f ? sp.temperature : 1.0f;  // there are no q rows
+  const size_t base = spec_verify_workspace_bytes(rows, 0, V, dtype, sp.top_k > 0 ? sp.top_k : 0);
+  if (base == 0) return SPEC_ERR_INVALID_ARG;
+  const size_t need = spec_sample_workspace_bytes(rows, V, dtype, sp.top_k > 0 ? sp.top_k : 0);
+  char* ws = static_cast<char*>(workspace);
+  if (rows > 0 && (!ws || ((uintptr_t)ws & 255u) || workspace_bytes < need)) return SPEC_ERR_WORKSPACE;
+  int32_t* nacc = rows > 0 ? reinterpret_cast<int32_t*>(ws + base) : nullptr;
+  float* ln = rows > 0 ? reinterpret_cast<float*>(ws + base + align256((size_t)rows * sizeof(int32_t))) : nullptr;
+  spec_verify_stats_t st = {};
+  st.row_lognorm = out_prob ? ln : nullptr;
+  // a request with no drafts: its one token is the draw from p at position 0 (the bonus draw)
+  spec_status_t r = spec_verify_ex(logits, nullptr, nullptr, nullptr, nullptr, u, &sp, out_tokens, nacc, &st, rows, 0,
+                                   V, dtype, ws, base, stream);
+  if (r != SPEC_OK || rows == 0 || !out_prob) return r;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const float invT = sp.temperature > 0.0f ? (float)(1.0 / (double)sp.temperature) : 0.0f;
+  const unsigned grid = (unsigned)((rows + 255) / 256);
+  if (dtype == SPEC_DTYPE_BF16)
+    sample_prob_kernel<uint16_t><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(logits), out_tokens, ln, invT,
+                                                      rows, V, out_prob);
+  else
+    sample_prob_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(logits), out_tokens, ln, invT, rows, V,
+                                                   out_prob);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 const char* spec_verify_status_string(spec_status_t status) {

@@ -103,6 +103,10 @@ WORKLOADS["c5_topp0.9"] = Workload("c5_topp0.9", B=1024, K=4, V=128256, dtype="b
                                    top_k=0, seed=1061, alpha=0.8, top_p=0.9)
 WORKLOADS["c5_tq0.5"] = Workload("c5_tq0.5", B=1024, K=4, V=128256, dtype="bf16", temperature=1.0,
                                  top_k=0, seed=1062, alpha=0.45, draft_temperature=0.5)
+# Draft-token sampling (the step before verification): 1024 rows of 128256 bf16 logits, one draw
+# each; a batch of requests with no drafts, whose one row is the row sampled from.
+WORKLOADS["sample_c5"] = Workload("sample_c5", B=1024, K=0, V=128256, dtype="bf16", temperature=1.0,
+                                  top_k=0, seed=1071, alpha=None, tau=0.5)
 
 
 def get(name: str, **overrides) -> Workload:
