@@ -313,6 +313,7 @@ struct Smem {
   int rowFlag[kMaxRows];
   int Kb, jstar, flags, nonfinite;
   int tile, seg_first, found;
+  int rowListed[kMaxRows];  // top-k: the row's kept set is complete in its chunk lists
   float tile_base, total;
   float incl[kThreads];
   int y;
@@ -1574,6 +1575,137 @@ __device__ __forceinline__ void nucleus_row(const Params& P, const T* row, float
   __syncthreads();
 }
 
+// Top-k draws over the kept set: p's kept tokens (key >= the row's threshold) are prefixes of row
+// js's sorted chunk lists; their weights are those of draw_range (the residual max(0, P - Q), Q
+// read at each token, or the target weights for a draw from p alone), and the inverse CDF runs
+// over them sorted by token id, so it draws what the full-row pass draws (only the summation
+// order differs).  Returns false (nothing drawn) if the kept set exceeds the list buffer
+// (kWarps * kRowCap pairs); otherwise sets sm.y, sm.margin and *R_out.  Whole block.
+template <typename T>
+__device__ bool draw_list(const Params& P, int b, int js, const T* qr, const DrawRows& d, float u, uint2* lst,
+                          Smem& sm, int* clamp, float* R_out) {
+  constexpr int kCap = kWarps * kRowCap;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int nch = P.nchunk;
+  const uint2* meta = P.cmeta + ((size_t)b * P.R + js) * nch;
+  const uint2* cand = P.cand + ((size_t)b * P.R + js) * nch * (size_t)kCandCap;
+  const uint32_t kt = fkey(d.Tp);
+  if (warp == 0) {  // gather the prefixes of the chunk lists at or above the threshold
+    int n = 0;
+    for (int c0 = 0; c0 < nch; c0 += 32) {
+      const int c = c0 + lane;
+      const int cnt = c < nch ? (int)(__ldcg(&meta[c].y) & kMetaCount) : 0;
+      const uint2* src = cand + (size_t)(c < nch ? c : 0) * kCandCap;
+      int take = 0;
+      while (take < cnt && __ldcg(&src[take].x) >= kt) ++take;
+      int off = take;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, off, o);
+        if (lane >= o) off += y;
+      }
+      const int base = n + off - take;
+      for (int i = 0; i < take; ++i)
+        if (base + i < kCap) lst[base + i] = __ldcg(src + i);
+      n += __shfl_sync(0xFFFFFFFFu, off, 31);
+    }
+    if (lane == 0) sm.found = n;
+  }
+  __syncthreads();
+  const int n = sm.found;
+  if (n > kCap || n == 0) {
+    __syncthreads();
+    return false;
+  }
+  // weights, as (token, weight bits)
+  for (int i = t; i < n; i += kThreads) {
+    const uint2 e = lst[i];
+    const float zp = keyf(e.x);
+    float w;
+    if (d.resid) {
+      const float pa = ex2(fmaf(zp, P.c2, -d.Lp));
+      const float zq = load1<T>(qr + e.y);
+      const float qa = zq >= d.Tq ? ex2(fmaf(zq, d.c2q, -d.Lq)) : 0.0f;
+      w = fmaxf(pa - qa, 0.0f);
+    } else {
+      w = ex2(fmaf(zp, P.c2, -d.Mp2));
+    }
+    lst[i] = make_uint2(e.y, __float_as_uint(w));
+  }
+  int N = 32;
+  while (N < n) N <<= 1;
+  for (int i = n + t; i < N; i += kThreads) lst[i] = make_uint2(0xFFFFFFFFu, 0u);  // sorts last
+  __syncthreads();
+  for (int k = 2; k <= N; k <<= 1) {  // bitonic sort by token id, ascending
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = t; i < N; i += kThreads) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const uint2 a = lst[i], c = lst[ixj];
+          if (((i & k) == 0) ? (a.x > c.x) : (a.x < c.x)) {
+            lst[i] = c;
+            lst[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // cumulative sums in token order: each thread owns a run of consecutive entries
+  constexpr int kPer = kCap / kThreads;
+  const int i0 = t * kPer;
+  float run = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j)
+    if (i0 + j < n) run += __uint_as_float(lst[i0 + j].y);
+  float incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sm.red_s[warp] = incl;
+  if (t == 0) {
+    sm.y = -1;
+    sm.margin = 0.0f;
+  }
+  __syncthreads();
+  float before = incl - run, R = 0.0f;
+  for (int w = 0; w < kWarps; ++w) {
+    if (w < warp) before += sm.red_s[w];
+    R += sm.red_s[w];
+  }
+  const float target = u * R;
+  float C = before;
+  int last = -1;
+  for (int j = 0; j < kPer; ++j) {
+    const int i = i0 + j;
+    if (i >= n) break;
+    const float w = __uint_as_float(lst[i].y);
+    const float prev = C;
+    C += w;
+    if (w > 0.0f) last = i;
+    if (w > 0.0f && target >= prev && target < C) {
+      sm.y = (int)lst[i].x;
+      sm.margin = fminf(u - prev / R, C / R - u);
+    }
+  }
+  // rounding put u * R at or past the total: the last token with weight, flagged
+  __syncthreads();
+  if (t == 0) sm.found = -1;
+  __syncthreads();
+  if (last >= 0) atomicMax(&sm.found, last);
+  __syncthreads();
+  if (t == 0 && sm.y < 0 && sm.found >= 0) {
+    sm.y = (int)lst[sm.found].x;
+    sm.margin = 0.0f;
+    *clamp = 1;
+  }
+  __syncthreads();
+  *R_out = R;
+  return true;
+}
+
 // The per-request tail, run by the CTA that completed the request's last item.
 template <typename T, int MODE, bool VEC, bool NUC>
 __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* dyn) {
@@ -1661,6 +1793,7 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
         if (!ok && !(fl & SPEC_FLAG_NONFINITE)) fl |= 0x40000000;  // needs the exact path
         if (ok && (!(S > 0.0f) || isinf(M) || isnan(S))) fl |= SPEC_FLAG_NONFINITE;
         sm.rowFlag[r] = fl;
+        sm.rowListed[r] = ok;
       }
       __syncwarp();
     }
@@ -1843,13 +1976,19 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
       drawn = rc > 0.0f;
       R = S;
     }
+    // after top-k, p's kept set (at most a few hundred tokens) is complete in row js's chunk lists
+    // unless that row took the exact path: the draw runs over it instead of over the whole row
+    uint2* klist = reinterpret_cast<uint2*>(dyn + (VEC ? (size_t)kDrawStages * kDrawStageBytes : 0));
+    const bool listed = MODE == kTopK && sm.rowListed[js];
+    if (listed && !drawn) drawn = draw_list<T>(P, b, js, qr, d, u, klist, sm, &clamp, &R);
     if (!drawn) R = draw_range<T, VEC, MASK>(P, pr, qr, d, 0, P.V, true, u, 0.0f, 0.0f, wt, ring, sm, &clamp);
     float resid_mass = d.resid ? R : 0.0f;
     if (!(R > 0.0f)) {
       // max(0, p - q) vanished through rounding: draw from p instead
       d.resid = false;
       if (t == 0) sm.flags |= SPEC_FLAG_RESIDUAL_ZERO;
-      R = draw_range<T, VEC, MASK>(P, pr, pr, d, 0, P.V, true, u, 0.0f, 0.0f, wt, ring, sm, &clamp);
+      if (!(listed && draw_list<T>(P, b, js, pr, d, u, klist, sm, &clamp, &R)))
+        R = draw_range<T, VEC, MASK>(P, pr, pr, d, 0, P.V, true, u, 0.0f, 0.0f, wt, ring, sm, &clamp);
     }
     if (clamp) atomicOr(&sm.flags, SPEC_FLAG_CDF_CLAMP);
     __syncthreads();
