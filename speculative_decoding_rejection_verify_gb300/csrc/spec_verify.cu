@@ -36,6 +36,8 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kChunkBytes = 16384;      // bytes of logits per work item (16 B per thread x 4)
 constexpr int kStages = 4;               // work items in flight per CTA (cp.async ring)
+constexpr int kStagesTopK = 3;           // top-k: a shallower ring leaves room for 3 blocks per SM
+__host__ __device__ constexpr int stages_of(int mode) { return mode == 1 ? kStagesTopK : kStages; }
 constexpr int kTile = 256;               // inverse-CDF tile: 32 lanes x 8 logits
 constexpr int kCandCap = 256;            // top-k candidates stored per chunk
 constexpr int kSegCap = 1024;            // running top-k candidates of a row segment (per buffer)
@@ -458,22 +460,13 @@ __device__ void seg_filter(const float (&v)[Cfg<T>::PER], int n, int v0, uint32_
       if (elem_of<T, VEC>(i, t) < n) mx = fmax_nan(mx, v[i]);
   }
   if (__any_sync(0xFFFFFFFFu, mx != mx) && lane == 0) atomicOr(&sm.seg_flags, (int)kMetaNaN);
-  if (!__any_sync(0xFFFFFFFFu, mx >= tf)) return;
+  if (!(mx >= tf)) return;
+  // a lane with survivors reserves its own slots (survivors are few once the bound is tight)
   int cnt = 0;
-  if (mx >= tf) {
 #pragma unroll
-    for (int i = 0; i < Cfg<T>::PER; ++i) cnt += (full || elem_of<T, VEC>(i, t) < n) && v[i] >= tf;
-  }
-  int incl = cnt;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  int base = 0;
-  if (lane == 31) base = atomicAdd(&sm.seg_n, incl);
-  base = __shfl_sync(0xFFFFFFFFu, base, 31) + incl - cnt;
-  if (cnt) {
+  for (int i = 0; i < Cfg<T>::PER; ++i) cnt += (full || elem_of<T, VEC>(i, t) < n) && v[i] >= tf;
+  int base = atomicAdd(&sm.seg_n, cnt);
+  {
 #pragma unroll
     for (int i = 0; i < Cfg<T>::PER; ++i) {
       const int e = elem_of<T, VEC>(i, t);
@@ -584,9 +577,11 @@ __device__ void seg_compact(int k, bool sorted, uint2* bufs, Smem& sm) {
 // One chunk of a top-k row in the streaming pass.
 template <typename T, bool VEC>
 __device__ void topk_chunk(const Params& P, const float (&v)[Cfg<T>::PER], int n, int b, int rp, int c,
-                           bool seg_start, bool seg_end, uint2* bufs, Smem& sm) {
+                           bool seg_start, bool seg_end, uint2* bufs, Smem& sm, int& seg_next, int& seg_m) {
   const int k = P.top_k;
   if (seg_start) {
+    seg_next = 0;  // the block's check schedule: identical registers in every thread
+    seg_m = 0;
     if (threadIdx.x == 0) {
       sm.seg_n = 0;
       sm.seg_theta = 0;
@@ -601,11 +596,21 @@ __device__ void topk_chunk(const Params& P, const float (&v)[Cfg<T>::PER], int n
   if (!sm.seg_tight) theta = max(theta, chunk_bound<T, VEC>(v, n, k, sm));
   const bool tight = sm.seg_tight;
   seg_filter<T, VEC>(v, n, c * Cfg<T>::CH, theta, bufs + (size_t)sm.seg_cur * kSegCap, sm);
-  // Once theta is tight a chunk adds few candidates, so the block meets (and maybe compacts) only
-  // every 4th chunk; the buffer's headroom above kSegCompact absorbs the chunks in between.
-  if (seg_end || !tight || ((c - sm.seg_c0) & 3) == 3) {
+  // The block meets (and maybe compacts) only on its check schedule.  A bound refreshed over m
+  // chunks lets about k / m survivors through per chunk; the next check comes when twice that
+  // rate would fill the buffer's free room (after 1..16 chunks).  Every thread derives the same
+  // schedule from values it reads between two barriers, so all of them meet at the same chunks.
+  const int dc = c - sm.seg_c0;
+  if (seg_end || !tight || dc >= seg_next) {
     __syncthreads();
-    if (seg_end || sm.seg_n > kSegCompact || (!tight && sm.seg_n >= k)) seg_compact(k, seg_end, bufs, sm);
+    if (seg_end || sm.seg_n > kSegCompact || (!tight && sm.seg_n >= k)) {
+      seg_compact(k, seg_end, bufs, sm);
+      seg_m = dc + 1;
+    }
+    const int fill = min(sm.seg_n, kSegCap);
+    __syncthreads();  // nobody adds to the set before every thread has read its size
+    const int gap = ((kSegCap - fill) * max(seg_m, 1)) / (2 * k);
+    seg_next = dc + min(16, max(1, gap));
   }
   const size_t row_slot = ((size_t)b * P.R + rp) * P.nchunk;
   if (threadIdx.x == 0 && c != sm.seg_c0) P.cmeta[row_slot + c] = make_uint2(0u, 0u);
@@ -2240,10 +2245,12 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
   const uint32_t hi = (uint32_t)(((uint64_t)total * (blockIdx.x + 1)) / gridDim.x);
   if (lo >= hi) return;
   uint4* stages = reinterpret_cast<uint4*>(dyn);
-  uint2* surv = reinterpret_cast<uint2*>(dyn + (VEC ? (size_t)kStages * kChunkBytes : 0));
+  constexpr int ST = stages_of(MODE);
+  uint2* surv = reinterpret_cast<uint2*>(dyn + (VEC ? (size_t)ST * kChunkBytes : 0));
   Cursor cc;
   cursor_at<T>(P, lo, cc);
   bool seg_start = true, seg_end = false;  // row segments of the top-k path
+  int seg_next = 0, seg_m = 0;
   auto summarise_f = [&](const Cursor& k, const float (&v)[Cfg<T>::PER]) {
     const int v0 = k.c * Cfg<T>::CH;
     const int n = min(Cfg<T>::CH, P.V - v0);
@@ -2253,12 +2260,12 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
     else if (MODE == kGreedy)
       item_greedy<T, VEC>(v, n, v0, P.partial + slot * kWarps);
     else
-      topk_chunk<T, VEC>(P, v, n, k.b, k.rp, k.c, seg_start, seg_end, surv, sm);
+      topk_chunk<T, VEC>(P, v, n, k.b, k.rp, k.c, seg_start, seg_end, surv, sm, seg_next, seg_m);
   };
   if (VEC) {
     Cursor ic = cc;
 #pragma unroll
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < ST; ++s) {
       if (lo + s < hi) {
         issue_at<T>(P, ic, stages + (size_t)s * (kChunkBytes / 16));
         cursor_next<T>(P, ic);
@@ -2268,11 +2275,11 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
     int s = 0;
     for (uint32_t it = lo; it < hi; ++it) {
       uint4* st = stages + (size_t)s * (kChunkBytes / 16);
-      cp_async_wait<kStages - 1>();  // this thread's copies of this item have landed
+      cp_async_wait<ST - 1>();  // this thread's copies of this item have landed
       uint4 raw[Cfg<T>::LOADS];
 #pragma unroll
       for (int l = 0; l < Cfg<T>::LOADS; ++l) raw[l] = st[l * kThreads + threadIdx.x];
-      if (it + kStages < hi) {  // the stage's bytes are in registers: refill it
+      if (it + ST < hi) {  // the stage's bytes are in registers: refill it
         issue_at<T>(P, ic, st);
         cursor_next<T>(P, ic);
       }
@@ -2292,7 +2299,7 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
       }
       seg_start = seg_end;
       cursor_next<T>(P, cc);
-      s = s + 1 == kStages ? 0 : s + 1;
+      s = s + 1 == ST ? 0 : s + 1;
     }
     cp_async_wait<0>();
   } else {
@@ -2467,7 +2474,7 @@ static int mode_of(float temperature, int top_k, int V) {
 
 // dynamic shared memory of the two passes
 static size_t stats_smem(int mode, bool vec) {
-  return (vec ? (size_t)kStages * kChunkBytes : 0) + (mode == kTopK ? (size_t)2 * kSegCap * sizeof(uint2) : 0);
+  return (vec ? (size_t)stages_of(mode) * kChunkBytes : 0) + (mode == kTopK ? (size_t)2 * kSegCap * sizeof(uint2) : 0);
 }
 static size_t finish_smem(int mode, int V, int es, bool vec, bool nuc) {
   const int ntile = (V + kTile - 1) / kTile;
