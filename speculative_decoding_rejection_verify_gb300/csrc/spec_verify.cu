@@ -21,6 +21,7 @@
 // A request-major item order keeps only a few requests in flight, which is what keeps the rows of
 // the final draw L2-resident.  There is no tensor-core work: nothing here is a contraction.
 
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <float.h>
 #include <math.h>
@@ -36,6 +37,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kChunkBytes = 16384;      // bytes of logits per work item (16 B per thread x 4)
 constexpr int kStages = 4;               // work items in flight per CTA (cp.async ring)
+constexpr int kCluster = 8;              // blocks sharing one request's draw when requests are few
 constexpr int kStagesTopK = 3;           // top-k: a shallower ring leaves room for 3 blocks per SM
 __host__ __device__ constexpr int stages_of(int mode) { return mode == 1 ? kStagesTopK : kStages; }
 constexpr int kTile = 256;               // inverse-CDF tile: 32 lanes x 8 logits
@@ -320,6 +322,8 @@ struct Smem {
   float incl[kThreads];
   int y;
   float margin;
+  float cl_total, cl_base, cl_R;  // cluster draw: this block's range total; the owner's offset, R
+  int cl_owner;
   int nuc_digit;     // nucleus search: the bin of the cut at the current level
   float nuc_above;   // mass of the bins above it
   float nuc_bin;     // mass of the bin itself
@@ -739,15 +743,18 @@ __device__ __forceinline__ void weights8(const T* pr, const T* qr, int e0, int V
 // tile, tiles by segments per thread).  With `full`, the range is the whole row and
 // target = u * (its total), which is also the margin scale; otherwise `target` is the mass the
 // draw must pass inside the range and `Rm` the margin scale.  Returns the range total; sets
-// sm.y, sm.margin and the clamp flag.
+// sm.y, sm.margin and the clamp flag.  `phase` splits the work for a cluster of blocks sharing
+// one row: 1 = only the tile sums and the range total (kept in wt / sm for a later phase 2),
+// 2 = only the search, over the sums a phase-1 call on the same range left; 0 = both.
 template <typename T, bool VEC, bool MASK>
 __device__ float draw_range(const Params& P, const T* pr, const T* qr, const DrawRows& d, int v0,
                             int vend, bool full, float u, float target_in, float Rm, float* wt,
-                            uint4* ring, Smem& sm, int* clamp) {
+                            uint4* ring, Smem& sm, int* clamp, int phase = 0) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int V = vend;
   const int ntile = (vend - v0 + kTile - 1) / kTile;
   // pass A: tile sums
+  if (phase != 2) {
   if constexpr (VEC) {
     // Aligned rows stream through a cp.async ring: stage k holds elements [v0 + k*SE, + SE) of the
     // p row and of the q row (the q half is not read for a draw from p alone).  Each thread copies
@@ -847,29 +854,36 @@ __device__ float draw_range(const Params& P, const T* pr, const T* qr, const Dra
       }
     }
   }
+  }  // phase != 2
   __syncthreads();  // every tile sum written
   // segments of tiles per thread, then a block inclusive scan of the segment sums
   const int L = (ntile + kThreads - 1) / kThreads;
   const int s0 = t * L, s1 = min(s0 + L, ntile);
-  float seg = 0.0f;
-  for (int i = s0; i < s1; ++i) seg += wt[i];
-  float x = seg;
+  float incl;
+  if (phase != 2) {
+    float seg = 0.0f;
+    for (int i = s0; i < s1; ++i) seg += wt[i];
+    float x = seg;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    float y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-    if (lane >= o) x += y;
+    for (int o = 1; o < 32; o <<= 1) {
+      float y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) sm.red_s[warp] = x;
+    if (t == 0) sm.seg_first = kThreads;
+    __syncthreads();
+    float off = 0.0f;
+    for (int w = 0; w < warp; ++w) off += sm.red_s[w];
+    incl = x + off;
+    sm.incl[t] = incl;
+    if (t == kThreads - 1) sm.total = incl;
+  } else {
+    incl = sm.incl[t];
+    if (t == 0) sm.seg_first = kThreads;
   }
-  if (lane == 31) sm.red_s[warp] = x;
-  if (t == 0) sm.seg_first = kThreads;
-  __syncthreads();
-  float off = 0.0f;
-  for (int w = 0; w < warp; ++w) off += sm.red_s[w];
-  const float incl = x + off;
-  sm.incl[t] = incl;
-  if (t == kThreads - 1) sm.total = incl;
   __syncthreads();
   const float total = sm.total;
-  if (!(total > 0.0f)) return total;  // caller handles an empty residual
+  if (!(total > 0.0f) || phase == 1) return total;  // caller handles an empty residual
   const float R = full ? total : Rm;
   const float target = full ? u * total : target_in;
   if (target < incl) atomicMin(&sm.seg_first, t);
@@ -1711,10 +1725,76 @@ __device__ bool draw_list(const Params& P, int b, int js, const T* qr, const Dra
   return true;
 }
 
+// A draw over the whole row split across the CL blocks of a cluster: each block sums its share
+// of the row's tiles (draw_range phase 1), the shares' totals are read from every block's shared
+// memory in rank order (so every block forms the same R, target and owner), and the block whose
+// share holds u * R searches its own tile sums (phase 2) and hands the token to rank 0.  Every
+// block of the cluster calls it; returns R.
+template <typename T, bool VEC, bool MASK, int CL>
+__device__ float cluster_draw(const Params& P, const T* pr, const T* qr, const DrawRows& d, float u, float* wt,
+                              uint4* ring, Smem& sm, int* clamp) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = (int)cl.block_rank();
+  const int ntile = (P.V + kTile - 1) / kTile;
+  const int per = (ntile + CL - 1) / CL;
+  const int v0 = min(P.V, rank * per * kTile), v1 = min(P.V, v0 + per * kTile);
+  const float Rr = v1 > v0 ? draw_range<T, VEC, MASK>(P, pr, qr, d, v0, v1, false, u, 0.0f, 0.0f, wt, ring, sm, clamp, 1)
+                           : 0.0f;
+  if (threadIdx.x == 0) sm.cl_total = Rr;
+  cl.sync();
+  if (threadIdx.x == 0) {
+    float tot[CL], R = 0.0f;
+#pragma unroll
+    for (int r = 0; r < CL; ++r) {
+      tot[r] = *cl.map_shared_rank(&sm.cl_total, r);
+      R += tot[r];
+    }
+    const float target = u * R;
+    int owner = -1, last = -1;
+    float cum = 0.0f, base = 0.0f, base_last = 0.0f;
+    for (int r = 0; r < CL; ++r) {
+      if (tot[r] > 0.0f) {
+        if (owner < 0 && target < cum + tot[r]) {
+          owner = r;
+          base = cum;
+        }
+        last = r;
+        base_last = cum;
+      }
+      cum += tot[r];
+    }
+    if (owner < 0) {  // rounding: the last share with mass searches (and clamps)
+      owner = last;
+      base = base_last;
+    }
+    sm.cl_owner = owner;
+    sm.cl_base = base;
+    sm.cl_R = R;
+  }
+  __syncthreads();
+  const float R = sm.cl_R;
+  if (R > 0.0f && rank == sm.cl_owner) {
+    draw_range<T, VEC, MASK>(P, pr, qr, d, v0, v1, false, u, u * R - sm.cl_base, R, wt, ring, sm, clamp, 2);
+    Smem* lead = cl.map_shared_rank(&sm, 0);
+    if (threadIdx.x == 0) {
+      lead->y = sm.y;
+      lead->margin = sm.margin;
+    }
+    if (*clamp) atomicOr(&lead->flags, SPEC_FLAG_CDF_CLAMP);
+    *clamp = 0;
+  }
+  cl.sync();  // rank 0 holds the token; no block leaves while another may still write to it
+  return R;
+}
+
 // The per-request tail, run by the CTA that completed the request's last item.
-template <typename T, int MODE, bool VEC, bool NUC>
+template <typename T, int MODE, bool VEC, bool NUC, int CL = 1>
 __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* dyn) {
   constexpr bool MASK = MODE == kTopK || NUC;  // draws skip logits below a row threshold
+  // With CL > 1 the CL blocks of a cluster all run the request's decision (identically) and share
+  // its full-row draw; only rank 0 writes results.
+  const bool lead = CL == 1 || cooperative_groups::this_cluster().block_rank() == 0;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int K = P.K;
   // Warp 0 starts the loads of the ratio test right away (draft tokens, uniforms, the logits at
@@ -1900,13 +1980,13 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
       jstar = rej ? __ffs(rej) - 1 : Kb;
       unsigned badm = __ballot_sync(0xFFFFFFFFu, bad);
       examined_bad = jstar < Kb && ((badm >> jstar) & 1u);
-      if (lane < K) {
+      if (lane < K && lead) {
         const bool ex = lane <= jstar && lane < Kb;
         if (P.p_draft) P.p_draft[(size_t)b * K + lane] = ex ? a : NAN;
         if (P.q_draft) P.q_draft[(size_t)b * K + lane] = ex ? cq : NAN;
         if (P.acc_margin) P.acc_margin[(size_t)b * K + lane] = ex ? am : NAN;
       }
-      if (lane <= K) tok[lane] = lane < jstar ? x : -1;
+      if (lane <= K && lead) tok[lane] = lane < jstar ? x : -1;
       if (lane == 0) sm.jstar = jstar;
     }
     if (lane == 0 && examined_bad) sm.flags |= SPEC_FLAG_BAD_TOKEN;
@@ -1934,7 +2014,10 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
     int clamp = 0;
     bool drawn = false;
     float R = 0.0f;
-    if (MODE == kSample && !NUC && !d.resid) {
+    if (MODE == kSample && !NUC && !d.resid && !lead) {
+      drawn = true;  // a bonus draw reads one chunk: rank 0 does it alone
+      R = 1.0f;
+    } else if (MODE == kSample && !NUC && !d.resid) {
       // Bonus draw: the chunk masses follow from the stored (max, sum) pairs, so only the chunk
       // holding u * S is read again.
       const int nch = P.nchunk;
@@ -1986,18 +2069,27 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
     uint2* klist = reinterpret_cast<uint2*>(dyn + (VEC ? (size_t)kDrawStages * kDrawStageBytes : 0));
     const bool listed = MODE == kTopK && sm.rowListed[js];
     if (listed && !drawn) drawn = draw_list<T>(P, b, js, qr, d, u, klist, sm, &clamp, &R);
-    if (!drawn) R = draw_range<T, VEC, MASK>(P, pr, qr, d, 0, P.V, true, u, 0.0f, 0.0f, wt, ring, sm, &clamp);
+    if (!drawn) {
+      if (CL > 1 && d.resid)
+        R = cluster_draw<T, VEC, MASK, CL>(P, pr, qr, d, u, wt, ring, sm, &clamp);
+      else
+        R = draw_range<T, VEC, MASK>(P, pr, qr, d, 0, P.V, true, u, 0.0f, 0.0f, wt, ring, sm, &clamp);
+    }
     float resid_mass = d.resid ? R : 0.0f;
     if (!(R > 0.0f)) {
-      // max(0, p - q) vanished through rounding: draw from p instead
+      // max(0, p - q) vanished through rounding: draw from p instead (R is the same in every
+      // block of a cluster, so they all take this branch together)
+      const bool was_resid = d.resid;
       d.resid = false;
       if (t == 0) sm.flags |= SPEC_FLAG_RESIDUAL_ZERO;
-      if (!(listed && draw_list<T>(P, b, js, pr, d, u, klist, sm, &clamp, &R)))
+      if (CL > 1 && was_resid)
+        R = cluster_draw<T, VEC, MASK, CL>(P, pr, pr, d, u, wt, ring, sm, &clamp);
+      else if (!(listed && draw_list<T>(P, b, js, pr, d, u, klist, sm, &clamp, &R)))
         R = draw_range<T, VEC, MASK>(P, pr, pr, d, 0, P.V, true, u, 0.0f, 0.0f, wt, ring, sm, &clamp);
     }
     if (clamp) atomicOr(&sm.flags, SPEC_FLAG_CDF_CLAMP);
     __syncthreads();
-    if (t == 0) {
+    if (t == 0 && lead) {
       tok[js] = sm.y;
       if (P.resid_mass) P.resid_mass[b] = resid_mass;
       if (P.samp_margin) P.samp_margin[b] = sm.margin;
@@ -2018,6 +2110,7 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
     }
   }
   __syncthreads();
+  if (!lead) return;
   if (t == 0) {
     P.out_nacc[b] = sm.jstar;
     if (P.flags) P.flags[b] = sm.flags;
@@ -2383,6 +2476,15 @@ __global__ void __launch_bounds__(256) sample_prob_kernel(const T* __restrict__ 
   out[i] = pr;
 }
 
+// Pass 2 for batches of fewer requests than SMs (sampling mode): a cluster of kCluster blocks per
+// request, which share the full-row residual draw (cluster_draw).
+template <typename T, bool VEC>
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) finish_cluster_kernel(const Params P) {
+  extern __shared__ __align__(128) unsigned char dyn[];
+  __shared__ Smem sm;
+  finish_request<T, kSample, VEC, false, kCluster>(P, (int)(blockIdx.x / kCluster), sm, dyn);
+}
+
 // Ragged batches: a table of valid rows in request-major order, so no item is spent on padding.
 __global__ void __launch_bounds__(1024) build_rowmap(const int32_t* __restrict__ kpr, int B, int K,
                                                      int greedy, uint32_t* rowmap,
@@ -2521,6 +2623,14 @@ static cudaError_t launch_t(const Params& P, uint32_t items, cudaStream_t st) {
     kn<<<(unsigned)((uint64_t)P.B * P.R), kThreads, kNucBufBytes, st>>>(P);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+  }
+  if (MODE == kSample && !nuc && P.B <= sms && P.V >= 16384) {
+    // few requests: a cluster per request spreads each full-row draw over kCluster SMs
+    auto kc = finish_cluster_kernel<T, VEC>;
+    e = prepare(kc, d2);
+    if (e != cudaSuccess) return e;
+    kc<<<(unsigned)P.B * kCluster, kThreads, d2, st>>>(P);
+    return cudaGetLastError();
   }
   k2<<<(unsigned)P.B, kThreads, d2, st>>>(P);
   return cudaGetLastError();
