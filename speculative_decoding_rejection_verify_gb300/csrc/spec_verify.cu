@@ -2239,7 +2239,8 @@ __device__ __forceinline__ void sample_vec(float c2, uint4 (&raw)[Cfg<T>::LOADS]
   }
   float s = 0.0f;
   if (m != -INFINITY) {
-    const float2 negm = make_float2(-m, -m), cc = make_float2(c2, c2);
+    // 2^((z - m) * c2) as 2^(z * c2 - m * c2): one packed FMA per pair of logits
+    const float2 negmc = make_float2(-m * c2, -m * c2), cc = make_float2(c2, c2);
     float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int l = 0; l < Cfg<T>::LOADS; ++l) {
@@ -2247,13 +2248,13 @@ __device__ __forceinline__ void sample_vec(float c2, uint4 (&raw)[Cfg<T>::LOADS]
       if (sizeof(T) == 2) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          float2 d = __fmul2_rn(__fadd2_rn(make_float2(bf16_lo(w[k]), bf16_hi(w[k])), negm), cc);
+          const float2 d = __ffma2_rn(make_float2(bf16_lo(w[k]), bf16_hi(w[k])), cc, negmc);
           acc = __fadd2_rn(acc, make_float2(ex2(d.x), ex2(d.y)));
         }
       } else {
 #pragma unroll
         for (int k = 0; k < 4; k += 2) {
-          float2 d = __fmul2_rn(__fadd2_rn(make_float2(__uint_as_float(w[k]), __uint_as_float(w[k + 1])), negm), cc);
+          const float2 d = __ffma2_rn(make_float2(__uint_as_float(w[k]), __uint_as_float(w[k + 1])), cc, negmc);
           acc = __fadd2_rn(acc, make_float2(ex2(d.x), ex2(d.y)));
         }
       }
