@@ -214,3 +214,31 @@ def test_errors_are_reported():
     with pytest.raises(sv.SpecVerifyError):
         sv.verify(to_dev(d["p"], dev), to_dev(d["q"], dev), to_dev(d["draft"], dev), None, to_dev(d["ua"], dev),
                   to_dev(d["ur"], dev), 1.0, 300)  # top-k above the supported bound
+
+
+# ------------------------------------------------------------------------------------------------
+# the small-batch tail (an 8-block cluster per request) and the one-block tail, at their switch
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("extra", [0, 1])
+def test_cluster_tail_switch(extra):
+    """B = the SM count takes the cluster tail, B = SMs + 1 the one-block tail; both must agree
+    with the oracle (V = 16392 is just past the cluster tail's vocabulary threshold and leaves a
+    ragged last tile in every cluster share)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    d = _gen("c2", B=sms + extra, V=16392, tau=0.9)
+    res, _, _ = _check(d)
+    assert res["requests"] == sms + extra
+
+
+def test_cluster_tail_f32_and_zero_residual_fallback():
+    # fp32 rows through the cluster tail, and p == q rows with u = 1 - 2^-24: the ratio test
+    # accepts (u * q < p with p = q), and where rounding makes it reject, the residual is ~0 and
+    # every block of the cluster must take the zero-residual fallback together
+    d = _gen("c3", B=6, dtype="f32", V=40000)
+    _check(d)
+    d = _gen("c3", B=4, V=40000)
+    d["p"][:, :6] = d["q"]
+    d["ua"][:] = np.float32(1.0 - 2.0 ** -24)
+    g = run_gpu(d)
+    o = run_oracle(d)
+    compare(g, o, d["workload"].K, d["k_per_row"])
