@@ -130,6 +130,12 @@ __device__ __forceinline__ float ex2(float x) {
   return r;
 }
 
+// Programmatic dependent launch: a kernel lets the next kernel of the stream start launching
+// (its blocks then wait in pdl_wait until this grid has finished and its writes are visible).
+// Both are no-ops when the kernels are launched the ordinary way.
+__device__ __forceinline__ void pdl_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Total order on floats as unsigned keys (-0 is folded into +0; NaN handled by callers).
 __device__ __forceinline__ uint32_t fkey(float f) {
   uint32_t u = __float_as_uint(f + 0.0f);
@@ -2334,6 +2340,7 @@ template <typename T, int MODE, bool VEC>
 __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ Smem sm;
+  pdl_launch_next();  // the next pass may launch now; it waits for this grid before reading
   const uint32_t total = P.rowmap ? __ldg(P.total_rows) * (uint32_t)P.nchunk : P.uniform_items;
   const uint32_t lo = (uint32_t)(((uint64_t)total * blockIdx.x) / gridDim.x);
   const uint32_t hi = (uint32_t)(((uint64_t)total * (blockIdx.x + 1)) / gridDim.x);
@@ -2417,6 +2424,8 @@ template <typename T, bool VEC>
 __global__ void __launch_bounds__(kThreads) nucleus_kernel(const Params P) {
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ Smem sm;
+  pdl_wait();
+  pdl_launch_next();
   const int t = threadIdx.x, lane = t & 31;
   int b, rp;
   if (P.rowmap) {
@@ -2457,6 +2466,8 @@ template <typename T, int MODE, bool VEC, bool NUC>
 __global__ void __launch_bounds__(kThreads) finish_kernel(const Params P) {
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ Smem sm;
+  pdl_wait();
+  pdl_launch_next();
   for (int b = blockIdx.x; b < P.B; b += gridDim.x) {
     finish_request<T, MODE, VEC, NUC>(P, b, sm, dyn);
     __syncthreads();
@@ -2469,6 +2480,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) sample_prob_kernel(const T* __restrict__ logits, const int32_t* __restrict__ tok,
                                                           const float* __restrict__ lognorm, float invT, int rows,
                                                           int V, float* __restrict__ out) {
+  pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= rows) return;
   const int y = tok[i];
@@ -2483,6 +2495,8 @@ template <typename T, bool VEC>
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) finish_cluster_kernel(const Params P) {
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ Smem sm;
+  pdl_wait();
+  pdl_launch_next();
   finish_request<T, kSample, VEC, false, kCluster>(P, (int)(blockIdx.x / kCluster), sm, dyn);
 }
 
@@ -2596,6 +2610,24 @@ static cudaError_t prepare(K kern, size_t dsm) {
   return cudaSuccess;
 }
 
+// Launches a pass after the previous kernel of the stream; with `pdl` it may start launching while
+// that kernel drains (programmatic stream serialization; the kernel waits in pdl_wait).
+template <typename... A>
+static cudaError_t launch_after(void (*kern)(A...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                                A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <typename T, int MODE, bool VEC>
 static cudaError_t launch_t(const Params& P, uint32_t items, cudaStream_t st) {
   const int es = (int)sizeof(T);
@@ -2617,24 +2649,25 @@ static cudaError_t launch_t(const Params& P, uint32_t items, cudaStream_t st) {
   e = cudaGetLastError();
   if (e == cudaSuccess && P.pass1_done) e = cudaEventRecord(static_cast<cudaEvent_t>(P.pass1_done), st);
   if (e != cudaSuccess) return e;
+  // the kernel after the streaming pass overlaps its launch with the pass's tail, unless an event
+  // is recorded between them
+  const bool pdl = P.pass1_done == nullptr;
   if (nuc && MODE == kSample) {
     auto kn = nucleus_kernel<T, VEC>;
     e = prepare(kn, kNucBufBytes);
-    if (e != cudaSuccess) return e;
-    kn<<<(unsigned)((uint64_t)P.B * P.R), kThreads, kNucBufBytes, st>>>(P);
-    e = cudaGetLastError();
+    if (e == cudaSuccess)
+      e = launch_after(kn, dim3((unsigned)((uint64_t)P.B * P.R)), dim3(kThreads), kNucBufBytes, st, pdl, P);
     if (e != cudaSuccess) return e;
   }
+  const bool pdl2 = pdl || (nuc && MODE == kSample);
   if (MODE == kSample && !nuc && P.B <= sms && P.V >= 16384) {
     // few requests: a cluster per request spreads each full-row draw over kCluster SMs
     auto kc = finish_cluster_kernel<T, VEC>;
     e = prepare(kc, d2);
-    if (e != cudaSuccess) return e;
-    kc<<<(unsigned)P.B * kCluster, kThreads, d2, st>>>(P);
-    return cudaGetLastError();
+    if (e == cudaSuccess) e = launch_after(kc, dim3((unsigned)P.B * kCluster), dim3(kThreads), d2, st, pdl2, P);
+    return e;
   }
-  k2<<<(unsigned)P.B, kThreads, d2, st>>>(P);
-  return cudaGetLastError();
+  return launch_after(k2, dim3((unsigned)P.B), dim3(kThreads), d2, st, pdl2, P);
 }
 
 template <typename T>
@@ -2876,13 +2909,15 @@ spec_status_t spec_sample(const void* logits, const float* u, const spec_samplin
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const float invT = sp.temperature > 0.0f ? (float)(1.0 / (double)sp.temperature) : 0.0f;
   const unsigned grid = (unsigned)((rows + 255) / 256);
+  cudaError_t e;
   if (dtype == SPEC_DTYPE_BF16)
-    sample_prob_kernel<uint16_t><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(logits), out_tokens, ln, invT,
-                                                      rows, V, out_prob);
+    e = launch_after(sample_prob_kernel<uint16_t>, dim3(grid), dim3(256), 0, s, true,
+                     static_cast<const uint16_t*>(logits), (const int32_t*)out_tokens, (const float*)ln, invT, rows, V,
+                     out_prob);
   else
-    sample_prob_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(logits), out_tokens, ln, invT, rows, V,
-                                                   out_prob);
-  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+    e = launch_after(sample_prob_kernel<float>, dim3(grid), dim3(256), 0, s, true, static_cast<const float*>(logits),
+                     (const int32_t*)out_tokens, (const float*)ln, invT, rows, V, out_prob);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 const char* spec_verify_status_string(spec_status_t status) {
