@@ -242,3 +242,38 @@ def test_cluster_tail_f32_and_zero_residual_fallback():
     g = run_gpu(d)
     o = run_oracle(d)
     compare(g, o, d["workload"].K, d["k_per_row"])
+
+
+@pytest.mark.parametrize("name,over", [("c2", {}), ("c5_a0.8", dict(B=200)), ("c5_topp0.9", dict(B=8))],
+                         ids=["cluster_tail", "one_block_tail", "nucleus"])
+def test_cuda_graph_replay_matches_direct_calls(name, over):
+    """The step (dependent launches between its kernels, cluster tail, nucleus pass) captured in
+    a CUDA graph replays to the results of direct calls."""
+    import speculative_decoding_rejection_verify_gb300 as sv
+    d = W.generate(W.get(name, **over))
+    dev = "cuda:0"
+    args = (to_dev(d["p"], dev), to_dev(d["q"], dev), to_dev(d["draft"], dev), None, to_dev(d["ua"], dev),
+            to_dev(d["ur"], dev), d["temperature"], d["top_k"])
+    kw = dict(top_p=d["top_p"], draft_temperature=d["draft_temperature"])
+    ref_tok, ref_n, _ = sv.verify(*args, **kw)
+    torch.cuda.synchronize()
+    B, K1 = ref_tok.shape
+    tok = torch.full((B, K1), -7, dtype=torch.int32, device=dev)
+    n = torch.full((B,), -7, dtype=torch.int32, device=dev)
+    ws = torch.zeros(sv.workspace_bytes(B, K1 - 1, d["p"].shape[-1], sv.DTYPE_BF16, d["top_k"]), dtype=torch.uint8,
+                     device=dev)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):  # first call outside capture (kernel attributes)
+        sv.verify(*args, **kw, workspace_tensor=ws, stream=s, out=(tok, n))
+    torch.cuda.synchronize()
+    tok.fill_(-7)
+    n.fill_(-7)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sv.verify(*args, **kw, workspace_tensor=ws, stream=torch.cuda.current_stream(), out=(tok, n))
+    for _ in range(2):
+        tok.fill_(-7)
+        n.fill_(-7)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(tok, ref_tok) and torch.equal(n, ref_n)
