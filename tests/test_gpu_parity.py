@@ -277,3 +277,24 @@ def test_cuda_graph_replay_matches_direct_calls(name, over):
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(tok, ref_tok) and torch.equal(n, ref_n)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_maximum_sizes(dtype):
+    """K_max = 16 drafts over the largest supported vocabulary, 2^21 (SPEC_MAX_K, SPEC_MAX_V):
+    rows of 4 (bf16) or 8 (f32) MB, 256 / 512 chunks each."""
+    import speculative_decoding_rejection_verify_gb300 as sv
+    d = W.generate(W.get("c5_a0.8", B=2, K=sv.MAX_K, V=sv.MAX_V, dtype=dtype))
+    res, _, _ = _check(d)
+    assert res["requests"] == 2
+
+
+def test_maximum_k_with_topk_and_topp():
+    import speculative_decoding_rejection_verify_gb300 as sv
+    d = W.generate(W.get("c4", B=3, K=sv.MAX_K, ragged=None, V=60000, top_k=sv.MAX_TOPK, tau=0.6))
+    _check(d)
+    d = W.generate(W.get("c5_topp0.9", B=3, K=sv.MAX_K, V=60000, tau=0.6))
+    g = run_gpu(d)
+    o = run_oracle(d)
+    res = compare(g, o, d["workload"].K, d["k_per_row"])
+    assert res["requests"] == 3
