@@ -1063,7 +1063,13 @@ __device__ bool topk_row_fast(const Params& P, int b, int rp, uint2* buf, float&
     const int cnt = c < nch ? (int)(__ldcg(&meta[c].y) & kMetaCount) : 0;
     const uint2* lst = cand + (size_t)(c < nch ? c : 0) * kCandCap;
     int take = 0;
-    while (take < cnt && __ldcg(&lst[take].x) >= Lk) ++take;
+    for (int i = 0; i < cnt; i += 2) {  // two entries per 16-byte load
+      const uint4 v = __ldcg(reinterpret_cast<const uint4*>(lst) + (i >> 1));
+      if (v.x < Lk) break;
+      take = i + 1;
+      if (i + 1 >= cnt || v.z < Lk) break;
+      take = i + 2;
+    }
     int off = take;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -1615,33 +1621,47 @@ __device__ bool draw_list(const Params& P, int b, int js, const T* qr, const Dra
   const uint2* meta = P.cmeta + ((size_t)b * P.R + js) * nch;
   const uint2* cand = P.cand + ((size_t)b * P.R + js) * nch * (size_t)kCandCap;
   const uint32_t kt = fkey(d.Tp);
-  if (warp == 0) {  // gather the prefixes of the chunk lists at or above the threshold
-    int n = 0;
-    for (int c0 = 0; c0 < nch; c0 += 32) {
-      const int c = c0 + lane;
-      const int cnt = c < nch ? (int)(__ldcg(&meta[c].y) & kMetaCount) : 0;
-      const uint2* src = cand + (size_t)(c < nch ? c : 0) * kCandCap;
-      int take = 0;
-      while (take < cnt && __ldcg(&src[take].x) >= kt) ++take;
-      int off = take;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, off, o);
-        if (lane >= o) off += y;
-      }
-      const int base = n + off - take;
-      for (int i = 0; i < take; ++i)
-        if (base + i < kCap) lst[base + i] = __ldcg(src + i);
-      n += __shfl_sync(0xFFFFFFFFu, off, 31);
+  // the length of a sorted list's prefix at or above the threshold, two entries per 16-byte load
+  auto prefix = [&](int c) {
+    const int cnt = (int)(__ldcg(&meta[c].y) & kMetaCount);
+    const uint4* src = reinterpret_cast<const uint4*>(cand + (size_t)c * kCandCap);
+    int take = 0;
+    for (int i = 0; i < cnt; i += 2) {
+      const uint4 v = __ldcg(src + (i >> 1));
+      if (v.x < kt) break;
+      take = i + 1;
+      if (i + 1 >= cnt || v.z < kt) break;
+      take = i + 2;
     }
-    if (lane == 0) sm.found = n;
+    return take;
+  };
+  // gather: every thread takes chunk lists t, t + 256, ...; a block scan of the counts places them
+  int mine = 0;
+  for (int c = t; c < nch; c += kThreads) mine += prefix(c);
+  int cincl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, cincl, o);
+    if (lane >= o) cincl += y;
   }
+  if (lane == 31) sm.red_i[warp] = cincl;
   __syncthreads();
-  const int n = sm.found;
+  int base = cincl - mine, n = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    if (w < warp) base += sm.red_i[w];
+    n += sm.red_i[w];
+  }
   if (n > kCap || n == 0) {
     __syncthreads();
     return false;
   }
+  for (int c = t; c < nch; c += kThreads) {
+    const int take = prefix(c);
+    const uint2* src = cand + (size_t)c * kCandCap;
+    for (int i = 0; i < take; ++i) lst[base + i] = __ldcg(src + i);
+    base += take;
+  }
+  __syncthreads();
   // weights, as (token, weight bits)
   for (int i = t; i < n; i += kThreads) {
     const uint2 e = lst[i];
@@ -1657,23 +1677,38 @@ __device__ bool draw_list(const Params& P, int b, int js, const T* qr, const Dra
     }
     lst[i] = make_uint2(e.y, __float_as_uint(w));
   }
-  int N = 32;
-  while (N < n) N <<= 1;
-  for (int i = n + t; i < N; i += kThreads) lst[i] = make_uint2(0xFFFFFFFFu, 0u);  // sorts last
   __syncthreads();
-  for (int k = 2; k <= N; k <<= 1) {  // bitonic sort by token id, ascending
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = t; i < N; i += kThreads) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const uint2 a = lst[i], c = lst[ixj];
-          if (((i & k) == 0) ? (a.x > c.x) : (a.x < c.x)) {
-            lst[i] = c;
-            lst[ixj] = a;
+  // order by token id: tokens are distinct, so each entry's place is the number of smaller ones
+  // (up to kCap / 2 entries, into the buffer's upper half); a bitonic sort for more
+  uint2* srt = lst;
+  if (n <= kCap / 2) {
+    srt = lst + kCap / 2;
+    for (int i = t; i < n; i += kThreads) {
+      const uint2 e = lst[i];
+      int pos = 0;
+      for (int j = 0; j < n; ++j) pos += lst[j].x < e.x;
+      srt[pos] = e;
+    }
+    __syncthreads();
+  } else {
+    int N = 32;
+    while (N < n) N <<= 1;
+    for (int i = n + t; i < N; i += kThreads) lst[i] = make_uint2(0xFFFFFFFFu, 0u);  // sorts last
+    __syncthreads();
+    for (int k = 2; k <= N; k <<= 1) {  // bitonic sort by token id, ascending
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        for (int i = t; i < N; i += kThreads) {
+          const int ixj = i ^ j;
+          if (ixj > i) {
+            const uint2 a = lst[i], c = lst[ixj];
+            if (((i & k) == 0) ? (a.x > c.x) : (a.x < c.x)) {
+              lst[i] = c;
+              lst[ixj] = a;
+            }
           }
         }
+        __syncthreads();
       }
-      __syncthreads();
     }
   }
   // cumulative sums in token order: each thread owns a run of consecutive entries
@@ -1682,7 +1717,7 @@ __device__ bool draw_list(const Params& P, int b, int js, const T* qr, const Dra
   float run = 0.0f;
 #pragma unroll
   for (int j = 0; j < kPer; ++j)
-    if (i0 + j < n) run += __uint_as_float(lst[i0 + j].y);
+    if (i0 + j < n) run += __uint_as_float(srt[i0 + j].y);
   float incl = run;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -1706,12 +1741,12 @@ __device__ bool draw_list(const Params& P, int b, int js, const T* qr, const Dra
   for (int j = 0; j < kPer; ++j) {
     const int i = i0 + j;
     if (i >= n) break;
-    const float w = __uint_as_float(lst[i].y);
+    const float w = __uint_as_float(srt[i].y);
     const float prev = C;
     C += w;
     if (w > 0.0f) last = i;
     if (w > 0.0f && target >= prev && target < C) {
-      sm.y = (int)lst[i].x;
+      sm.y = (int)srt[i].x;
       sm.margin = fminf(u - prev / R, C / R - u);
     }
   }
@@ -1722,7 +1757,7 @@ __device__ bool draw_list(const Params& P, int b, int js, const T* qr, const Dra
   if (last >= 0) atomicMax(&sm.found, last);
   __syncthreads();
   if (t == 0 && sm.y < 0 && sm.found >= 0) {
-    sm.y = (int)lst[sm.found].x;
+    sm.y = (int)srt[sm.found].x;
     sm.margin = 0.0f;
     *clamp = 1;
   }
