@@ -38,9 +38,12 @@ def _nucleus_valid(d, g, o, tol=1e-5):
             assert fg <= fo + tol or fo - top_p < tol, (b, r, fg, fo, top_p)
 
 
-def _check(d, **kw):
+def _check(d, min_exact=0.5, **kw):
     """Element-by-element parity.  A top-p cut within 1e-5 of top_p on any row a request uses
-    makes it low-margin (either kept set is right; the nucleus of every row is still checked)."""
+    makes it low-margin (either kept set is right; the nucleus of every row is still checked).
+    At least the fraction `min_exact` of the requests must be compared exactly.  (An fp32 row's
+    boundary token carries ~1e-4 of the mass, so about one row in ten has a cut within 1e-5 of
+    top_p, and a request uses up to 2 K + 1 rows.)"""
     kw.setdefault("stats", True)
     g = run_gpu(d, **kw)
     o = run_oracle(d)
@@ -48,7 +51,7 @@ def _check(d, **kw):
     res = compare(g, o, w.K, d["k_per_row"])
     _nucleus_valid(d, g, o)
     if d.get("top_p", 1.0) < 0.99:
-        assert res["exact"] >= (res["requests"] + 1) // 2, res
+        assert res["exact"] >= int(np.ceil(res["requests"] * min_exact)), res
     return res, g, o
 
 
@@ -132,3 +135,46 @@ def test_host_entry_with_sampling():
                             top_p=d["top_p"], draft_temperature=d["draft_temperature"])
     np.testing.assert_array_equal(tok, g["tokens"])
     np.testing.assert_array_equal(n, g["n_acc"])
+
+
+# ---------------------------------------------------------------------------------------------
+# the nucleus pass (top-p without top-k) on layouts and rows its common path does not settle
+# ---------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_topp_both_dtypes(dtype):
+    _check(W.generate(W.get("c5_topp0.9", B=12, dtype=dtype)), min_exact=0.25)
+
+
+def test_topp_ragged_sampling_mode():
+    """Ragged K_b with top-p and no top-k: the nucleus pass takes its rows from the row table
+    (rows past K_b are never read), with a draft temperature of its own."""
+    w = W.get("c5_topp0.9", B=16, ragged=(0, 4), draft_temperature=0.7)
+    _check(W.generate(w))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_topp_rows_off_the_common_path(dtype):
+    """Rows the one-read common path cannot settle, mixed with ordinary ones in one batch:
+    ascending rows (a crowded head), constant rows (every logit tied) and a row whose cut lies in
+    the tail, below 2^-15 of the max's weight.  They take the multi-pass search and must come out
+    exactly as the oracle has them."""
+    w = W.get("c5_topp0.9", B=6, dtype=dtype)
+    d = W.generate(w)
+    V = w.V
+    rng = np.random.default_rng(7)
+    rows = {}
+    ramp = np.linspace(-20.0, 10.0, V, dtype=np.float32)
+    rows[(0, 0)] = ramp                                   # ascending p row
+    rows[(1, 1)] = ramp + rng.normal(0, 0.05, V).astype(np.float32)
+    rows[(2, 0)] = np.full(V, 1.5, np.float32)            # constant row
+    # one spike over a low tail (each tail weight below 2^-15 of the spike's) that holds most of
+    # the mass, so the cut lies in the tail
+    tail = (-8.0 + rng.normal(0, 0.3, V)).astype(np.float32)
+    tail[rng.integers(V)] = 3.0
+    rows[(3, 2)] = tail
+    for (b, j), z in rows.items():
+        for key in ("p", "q"):
+            if key == "q" and j >= w.K:
+                continue
+            d[key][b, j] = W.to_bf16_bits(z) if dtype == "bf16" else z
+    _check(d, min_exact=0.25)
