@@ -151,6 +151,26 @@ def test_topk_variants():
         _check(d)
 
 
+@pytest.mark.parametrize("top_k", [32, 64, 65])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_topk_with_crowded_rows(top_k, dtype):
+    """Rows that crowd the streaming pass's running candidate set, mixed with ordinary rows: a
+    constant row (every logit tied, so the set overflows and the row takes the exact path) and an
+    ascending row (every chunk raises the bound)."""
+    w = W.get("c4", B=6, V=40000, tau=0.6, top_k=top_k, dtype=dtype)
+    d = W.generate(w)
+    V = w.V
+    special = {(0, 0): np.full(V, 2.0, np.float32), (1, 1): np.linspace(-8.0, 8.0, V, dtype=np.float32)}
+    for (b, j), z in special.items():
+        if j > int(d["k_per_row"][b]):
+            continue
+        for key in ("p", "q"):
+            if key == "q" and j >= int(d["k_per_row"][b]):
+                continue
+            d[key][b, j] = W.to_bf16_bits(z) if dtype == "bf16" else z
+    _check(d)
+
+
 def test_p_equals_q_accepts_everything():
     d = _gen("c2", B=8, V=5000, tau=0.0)
     d["p"][:, : d["q"].shape[1]] = d["q"]
