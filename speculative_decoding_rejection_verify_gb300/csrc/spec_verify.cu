@@ -1338,11 +1338,49 @@ __device__ __forceinline__ void nuc_pick(unsigned char* nbuf, Smem& sm, int nbin
 }
 
 // Exact cut among n gathered logits (keys gk, weights gw, n <= kNucCap) that hold the cut, with
-// `above` the mass of every kept logit above them: a bitonic sort by key, descending, then a scan
-// from the top to the first tie group where the mass reaches the target.  Leaves the nucleus mass
-// in sm.nuc_above and the cut key in sm.nuc_key.
+// `above` the mass of every kept logit above them: a bitonic sort by key, descending (in warp 0's
+// registers when n <= 32, the usual size of a boundary sub-bucket), then a scan from the top to the
+// first tie group where the mass reaches the target.  Leaves the nucleus mass in sm.nuc_above and
+// the cut key in sm.nuc_key.
 __device__ __forceinline__ void nuc_select(uint32_t* gk, float* gw, int n, float above, float target, Smem& sm) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  if (n <= 32) {  // one logit per lane of warp 0: a bitonic sort by shuffles, no block barrier
+    if (warp == 0) {
+      uint32_t k = lane < n ? gk[lane] : 0u;  // key 0: below every real key, sorts last
+      float w = lane < n ? gw[lane] : 0.0f;
+#pragma unroll
+      for (int kk = 2; kk <= 32; kk <<= 1) {
+#pragma unroll
+        for (int j = kk >> 1; j > 0; j >>= 1) {
+          const uint32_t ok = __shfl_xor_sync(0xFFFFFFFFu, k, j);
+          const float ow = __shfl_xor_sync(0xFFFFFFFFu, w, j);
+          const bool take_max = ((lane & kk) == 0) == ((lane & j) == 0);  // descending overall
+          if (take_max ? ok > k : ok < k) {
+            k = ok;
+            w = ow;
+          }
+        }
+      }
+      float incl = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned hit = __ballot_sync(0xFFFFFFFFu, lane < n && above + incl >= target);
+      // rounding left the target unreached: keep everything gathered
+      const int at = hit ? __ffs(hit) - 1 : n - 1;
+      const uint32_t kc = __shfl_sync(0xFFFFFFFFu, k, at);
+      // the nucleus mass: everything above, and every gathered logit down to the whole tie group
+      const float kept = warp_sum(lane < n && k >= kc ? w : 0.0f);
+      if (lane == 0) {
+        sm.nuc_above = above + kept;
+        sm.nuc_key = kc;
+      }
+    }
+    __syncthreads();
+    return;
+  }
   int N = 32;
   while (N < n) N <<= 1;
   for (int i = n + t; i < N; i += kThreads) {
@@ -1467,20 +1505,30 @@ __device__ __forceinline__ void nucleus_row(const Params& P, const T* row, float
   // 1e-4 against rounding, or the top-k threshold if that is higher.  A listed logit whose bucket
   // turns out to be the tail is ignored below.
   const float zcut = fmaxf(M - (15.0f / c2) * 1.0001f, thr == -INFINITY ? -FLT_MAX : nextafterf(thr, -INFINITY));
-  int cnt = 0;
+  // Each thread appends to its own column (entry i at byte (i * kThreads + t) * sizeof(T)) through a
+  // running offset.  A chunk adds at most PER entries, so a column found full before a chunk is
+  // wound back to its last entry and can only run on into the bins behind the list (free until
+  // the list has been read), by less than PER rows of the columns; its row takes the multi-pass
+  // path.
+  constexpr uint32_t kStride = kThreads * sizeof(T);
+  static_assert((size_t)Cfg<T>::PER * kStride <= kNucBinBytes, "a chunk's overrun stays in the bins");
+  const uint32_t col0 = t * (uint32_t)sizeof(T), col_end = col0 + (uint32_t)kCap * kStride;
+  uint32_t wp = col0;
+  bool crowded = false;
   auto scan = [&](const float (&v)[Cfg<T>::PER]) {
+    if (wp >= col_end) {
+      crowded = true;
+      wp = col_end - kStride;
+    }
 #pragma unroll
     for (int i = 0; i < Cfg<T>::PER; ++i) {
-      // an overflowing column keeps rewriting its last slot and sends the row to the multi-pass path
-      const bool in = v[i] > zcut;
-      const int slot = min(cnt, kCap - 1) * kThreads + t;
-      if (in) {
+      if (v[i] > zcut) {
         if (sizeof(T) == 2)
-          reinterpret_cast<uint16_t*>(nbuf)[slot] = (uint16_t)(__float_as_uint(v[i]) >> 16);
+          *reinterpret_cast<uint16_t*>(nbuf + wp) = (uint16_t)(__float_as_uint(v[i]) >> 16);
         else
-          reinterpret_cast<float*>(nbuf)[slot] = v[i];
+          *reinterpret_cast<float*>(nbuf + wp) = v[i];
+        wp += kStride;
       }
-      cnt += in;
     }
   };
   if (VEC) {  // two chunks' loads in flight ahead of the one being scanned
@@ -1511,6 +1559,7 @@ __device__ __forceinline__ void nucleus_row(const Params& P, const T* row, float
   // the binade and sub-bucket of a listed logit, from -x exactly as its weight 2^x is formed
   auto hbin = [&](float nx) { return min(kHeadBins - 1, __float2int_rd(nx)); };
   auto sbin = [&](float nx, int hb) { return min(kHeadBins - 1, __float2int_rd((nx - (float)hb) * 16.0f)); };
+  const int cnt = crowded ? kCap + 1 : (int)((wp - col0) / kStride);
   const bool overflow = __syncthreads_or(cnt > kCap);
   bool done = false;
   if (!overflow) {
