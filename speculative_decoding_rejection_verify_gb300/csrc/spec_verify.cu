@@ -22,6 +22,7 @@
 // the final draw L2-resident.  There is no tensor-core work: nothing here is a contraction.
 
 #include <cooperative_groups.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <float.h>
 #include <math.h>
@@ -1531,18 +1532,62 @@ __device__ __forceinline__ void nucleus_row(const Params& P, const T* row, float
       }
     }
   };
+  // bf16 logits are compared in pairs against the largest bf16 value <= zcut (no bf16 value lies
+  // between the two, so z > zcut is z > that value)
+  uint32_t zc2 = 0u;
+  if (sizeof(T) == 2) {
+    const uint32_t zb = __float_as_uint(zcut);
+    uint32_t h = zb >> 16;
+    if ((zb & 0xFFFFu) != 0u && (zb >> 31)) ++h;  // negative: rounding the magnitude up rounds down
+    zc2 = h | (h << 16);
+  }
+  auto scan_raw = [&](const uint4 (&raw)[Cfg<T>::LOADS], int nn) {
+    if (wp >= col_end) {
+      crowded = true;
+      wp = col_end - kStride;
+    }
+#pragma unroll
+    for (int l = 0; l < Cfg<T>::LOADS; ++l) {
+      if ((l * kThreads + t) * Cfg<T>::VW >= nn) continue;  // past the row (tail chunk)
+      const uint32_t w[4] = {raw[l].x, raw[l].y, raw[l].z, raw[l].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t m = __hgt2_mask(*reinterpret_cast<const __nv_bfloat162*>(&w[k]),
+                                       *reinterpret_cast<const __nv_bfloat162*>(&zc2));
+        if (m & 0xFFFFu) {
+          *reinterpret_cast<uint16_t*>(nbuf + wp) = (uint16_t)w[k];
+          wp += kStride;
+        }
+        if (m >> 16) {
+          *reinterpret_cast<uint16_t*>(nbuf + wp) = (uint16_t)(w[k] >> 16);
+          wp += kStride;
+        }
+      }
+    }
+  };
+  auto scan_vec = [&](const uint4 (&raw)[Cfg<T>::LOADS], int nn) {
+    if (sizeof(T) == 2) {
+      scan_raw(raw, nn);
+    } else {
+      float v[Cfg<T>::PER];
+      unpack<T>(raw, nn, v);
+      scan(v);
+    }
+  };
   if (VEC) {  // two chunks' loads in flight ahead of the one being scanned
     uint4 r0[Cfg<T>::LOADS], r1[Cfg<T>::LOADS];
     load_raw<T>(row, min(Cfg<T>::CH, P.V), r0);
     if (P.nchunk > 1) load_raw<T>(row + Cfg<T>::CH, min(Cfg<T>::CH, P.V - Cfg<T>::CH), r1);
     for (int c = 0; c < P.nchunk; ++c) {
       const int v0 = c * Cfg<T>::CH;
-      float v[Cfg<T>::PER];
-      unpack<T>(r0, min(Cfg<T>::CH, P.V - v0), v);
+      uint4 cur[Cfg<T>::LOADS];
 #pragma unroll
-      for (int l = 0; l < Cfg<T>::LOADS; ++l) r0[l] = r1[l];
+      for (int l = 0; l < Cfg<T>::LOADS; ++l) {
+        cur[l] = r0[l];
+        r0[l] = r1[l];
+      }
       if (c + 2 < P.nchunk) load_raw<T>(row + v0 + 2 * Cfg<T>::CH, min(Cfg<T>::CH, P.V - v0 - 2 * Cfg<T>::CH), r1);
-      scan(v);
+      scan_vec(cur, min(Cfg<T>::CH, P.V - v0));
     }
   } else {
     for (int c = 0; c < P.nchunk; ++c) {
