@@ -1446,6 +1446,7 @@ __device__ __forceinline__ void nuc_select(uint32_t* gk, float* gw, int n, float
 // bytes for its bins and gathers.  The common path's buckets are whole binades of the weight:
 // hb = floor(-x) capped at 15 (the tail, w < 2^-15), then 16 sub-buckets of the chosen one.
 constexpr int kHeadBins = 16;
+constexpr int kHeadSpanFirst = 13;  // binades of the weight listed by the first read of a row
 constexpr size_t kNucListBytes = 49152;
 constexpr size_t kNucBinBytes = (size_t)kHeadBins * kThreads * sizeof(float);
 constexpr size_t kNucBufBytes = kNucListBytes + kNucBinBytes;
@@ -1502,10 +1503,6 @@ __device__ __forceinline__ void nucleus_row(const Params& P, const T* row, float
   // ---- common path: one read of the row lists the head logits in per-thread columns ----
   constexpr int kCap = (int)(kNucListBytes / sizeof(T) / kThreads);
   float* bins = reinterpret_cast<float*>(nbuf + kNucListBytes);
-  // Every head logit (hb < 15) lies above zcut: the bound M - 15 / c2, widened by a relative
-  // 1e-4 against rounding, or the top-k threshold if that is higher.  A listed logit whose bucket
-  // turns out to be the tail is ignored below.
-  const float zcut = fmaxf(M - (15.0f / c2) * 1.0001f, thr == -INFINITY ? -FLT_MAX : nextafterf(thr, -INFINITY));
   // Each thread appends to its own column (entry i at byte (i * kThreads + t) * sizeof(T)) through a
   // running offset.  A chunk adds at most PER entries, so a column found full before a chunk is
   // wound back to its last entry and can only run on into the bins behind the list (free until
@@ -1514,6 +1511,11 @@ __device__ __forceinline__ void nucleus_row(const Params& P, const T* row, float
   constexpr uint32_t kStride = kThreads * sizeof(T);
   static_assert((size_t)Cfg<T>::PER * kStride <= kNucBinBytes, "a chunk's overrun stays in the bins");
   const uint32_t col0 = t * (uint32_t)sizeof(T), col_end = col0 + (uint32_t)kCap * kStride;
+  // Every head logit of the current span (binade hb < span) lies above zcut: the bound
+  // M - span / c2, widened by a relative 1e-4 against rounding, or the top-k threshold if that is
+  // higher.  A listed logit whose bucket turns out to be the tail is ignored below.
+  float zcut = 0.0f;
+  uint32_t zc2 = 0u;
   uint32_t wp = col0;
   bool crowded = false;
   auto scan = [&](const float (&v)[Cfg<T>::PER]) {
@@ -1534,13 +1536,6 @@ __device__ __forceinline__ void nucleus_row(const Params& P, const T* row, float
   };
   // bf16 logits are compared in pairs against the largest bf16 value <= zcut (no bf16 value lies
   // between the two, so z > zcut is z > that value)
-  uint32_t zc2 = 0u;
-  if (sizeof(T) == 2) {
-    const uint32_t zb = __float_as_uint(zcut);
-    uint32_t h = zb >> 16;
-    if ((zb & 0xFFFFu) != 0u && (zb >> 31)) ++h;  // negative: rounding the magnitude up rounds down
-    zc2 = h | (h << 16);
-  }
   auto scan_raw = [&](const uint4 (&raw)[Cfg<T>::LOADS], int nn) {
     if (wp >= col_end) {
       crowded = true;
@@ -1574,29 +1569,6 @@ __device__ __forceinline__ void nucleus_row(const Params& P, const T* row, float
       scan(v);
     }
   };
-  if (VEC) {  // two chunks' loads in flight ahead of the one being scanned
-    uint4 r0[Cfg<T>::LOADS], r1[Cfg<T>::LOADS];
-    load_raw<T>(row, min(Cfg<T>::CH, P.V), r0);
-    if (P.nchunk > 1) load_raw<T>(row + Cfg<T>::CH, min(Cfg<T>::CH, P.V - Cfg<T>::CH), r1);
-    for (int c = 0; c < P.nchunk; ++c) {
-      const int v0 = c * Cfg<T>::CH;
-      uint4 cur[Cfg<T>::LOADS];
-#pragma unroll
-      for (int l = 0; l < Cfg<T>::LOADS; ++l) {
-        cur[l] = r0[l];
-        r0[l] = r1[l];
-      }
-      if (c + 2 < P.nchunk) load_raw<T>(row + v0 + 2 * Cfg<T>::CH, min(Cfg<T>::CH, P.V - v0 - 2 * Cfg<T>::CH), r1);
-      scan_vec(cur, min(Cfg<T>::CH, P.V - v0));
-    }
-  } else {
-    for (int c = 0; c < P.nchunk; ++c) {
-      const int v0 = c * Cfg<T>::CH;
-      float v[Cfg<T>::PER];
-      load_chunk<T, VEC>(row + v0, min(Cfg<T>::CH, P.V - v0), v);
-      scan(v);
-    }
-  }
   auto entry = [&](int i) -> float {
     return sizeof(T) == 2 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(nbuf)[i * kThreads + t] << 16)
                           : reinterpret_cast<const float*>(nbuf)[i * kThreads + t];
@@ -1604,63 +1576,102 @@ __device__ __forceinline__ void nucleus_row(const Params& P, const T* row, float
   // the binade and sub-bucket of a listed logit, from -x exactly as its weight 2^x is formed
   auto hbin = [&](float nx) { return min(kHeadBins - 1, __float2int_rd(nx)); };
   auto sbin = [&](float nx, int hb) { return min(kHeadBins - 1, __float2int_rd((nx - (float)hb) * 16.0f)); };
-  const int cnt = crowded ? kCap + 1 : (int)((wp - col0) / kStride);
-  const bool overflow = __syncthreads_or(cnt > kCap);
-  bool done = false;
-  if (!overflow) {
-#pragma unroll
-    for (int b = 0; b < kHeadBins; ++b) bins[b * kThreads + t] = 0.0f;
-    for (int i = 0; i < cnt; ++i) {
-      const float z = entry(i);
-      const float x = (z - M) * c2;
-      const int hb = hbin(-x);
-      if (hb < kHeadBins - 1) bins[hb * kThreads + t] += ex2(x);
+  // The head is listed first down to 2^-kHeadSpanFirst of the max's weight (on rows like these
+  // the cut lies well inside, and a shorter list is searched faster); a cut below that span is
+  // looked for again in a second read down to 2^-15 before the multi-pass search.
+  for (int span = kHeadSpanFirst;; span = kHeadBins - 1) {
+    zcut = fmaxf(M - ((float)span / c2) * 1.0001f, thr == -INFINITY ? -FLT_MAX : nextafterf(thr, -INFINITY));
+    if (sizeof(T) == 2) {  // the largest bf16 value <= zcut, in both halves
+      const uint32_t zb = __float_as_uint(zcut);
+      uint32_t h = zb >> 16;
+      if ((zb & 0xFFFFu) != 0u && (zb >> 31)) ++h;  // negative: rounding the magnitude up rounds down
+      zc2 = h | (h << 16);
     }
-    __syncthreads();
-    nuc_walk_bins(bins, kHeadBins, sm, 0.0f, target, true, S);
-    const int bsel = sm.nuc_digit;
-    if (bsel < kHeadBins - 1) {
-      const float above1 = sm.nuc_above;
+    wp = col0;
+    crowded = false;
+    if (VEC) {  // two chunks' loads in flight ahead of the one being scanned
+      uint4 r0[Cfg<T>::LOADS], r1[Cfg<T>::LOADS];
+      load_raw<T>(row, min(Cfg<T>::CH, P.V), r0);
+      if (P.nchunk > 1) load_raw<T>(row + Cfg<T>::CH, min(Cfg<T>::CH, P.V - Cfg<T>::CH), r1);
+      for (int c = 0; c < P.nchunk; ++c) {
+        const int v0 = c * Cfg<T>::CH;
+        uint4 cur[Cfg<T>::LOADS];
+#pragma unroll
+        for (int l = 0; l < Cfg<T>::LOADS; ++l) {
+          cur[l] = r0[l];
+          r0[l] = r1[l];
+        }
+        if (c + 2 < P.nchunk) load_raw<T>(row + v0 + 2 * Cfg<T>::CH, min(Cfg<T>::CH, P.V - v0 - 2 * Cfg<T>::CH), r1);
+        scan_vec(cur, min(Cfg<T>::CH, P.V - v0));
+      }
+    } else {
+      for (int c = 0; c < P.nchunk; ++c) {
+        const int v0 = c * Cfg<T>::CH;
+        float v[Cfg<T>::PER];
+        load_chunk<T, VEC>(row + v0, min(Cfg<T>::CH, P.V - v0), v);
+        scan(v);
+      }
+    }
+    const int cnt = crowded ? kCap + 1 : (int)((wp - col0) / kStride);
+    const bool overflow = __syncthreads_or(cnt > kCap);
+    bool done = false, deeper = false;
+    if (!overflow) {
 #pragma unroll
       for (int b = 0; b < kHeadBins; ++b) bins[b * kThreads + t] = 0.0f;
       for (int i = 0; i < cnt; ++i) {
         const float z = entry(i);
         const float x = (z - M) * c2;
-        if (hbin(-x) == bsel) bins[sbin(-x, bsel) * kThreads + t] += ex2(x);
+        const int hb = hbin(-x);
+        if (hb < span) bins[hb * kThreads + t] += ex2(x);
       }
       __syncthreads();
-      nuc_walk_bins(bins, kHeadBins, sm, above1, target, false, 0.0f);
-      const int ssel = sm.nuc_digit;
-      const float above2 = sm.nuc_above;
-      // gather the chosen sub-bucket into the sort area (the bins are consumed)
-      uint32_t* sk = reinterpret_cast<uint32_t*>(bins);
-      float* sw = bins + kNucCap;
-      for (int i = 0; i < cnt; ++i) {
-        const float z = entry(i);
-        const float x = (z - M) * c2;
-        if (hbin(-x) == bsel && sbin(-x, bsel) == ssel) {
-          const int idx = atomicAdd(&sm.nuc_n, 1);
-          if (idx < kNucCap) {
-            sk[idx] = fkey(z);
-            sw[idx] = ex2(x);
+      nuc_walk_bins(bins, span + 1, sm, 0.0f, target, true, S);
+      const int bsel = sm.nuc_digit;
+      deeper = bsel >= span;  // uniform: read after the walk's barrier
+      if (!deeper) {
+        const float above1 = sm.nuc_above;
+#pragma unroll
+        for (int b = 0; b < kHeadBins; ++b) bins[b * kThreads + t] = 0.0f;
+        for (int i = 0; i < cnt; ++i) {
+          const float z = entry(i);
+          const float x = (z - M) * c2;
+          if (hbin(-x) == bsel) bins[sbin(-x, bsel) * kThreads + t] += ex2(x);
+        }
+        __syncthreads();
+        nuc_walk_bins(bins, kHeadBins, sm, above1, target, false, 0.0f);
+        const int ssel = sm.nuc_digit;
+        const float above2 = sm.nuc_above;
+        // gather the chosen sub-bucket into the sort area (the bins are consumed)
+        uint32_t* sk = reinterpret_cast<uint32_t*>(bins);
+        float* sw = bins + kNucCap;
+        for (int i = 0; i < cnt; ++i) {
+          const float z = entry(i);
+          const float x = (z - M) * c2;
+          if (hbin(-x) == bsel && sbin(-x, bsel) == ssel) {
+            const int idx = atomicAdd(&sm.nuc_n, 1);
+            if (idx < kNucCap) {
+              sk[idx] = fkey(z);
+              sw[idx] = ex2(x);
+            }
           }
         }
-      }
-      __syncthreads();
-      const int n = sm.nuc_n;
-      if (n <= kNucCap) {
-        nuc_select(sk, sw, n, above2, target, sm);
-        done = true;
+        __syncthreads();
+        const int n = sm.nuc_n;
+        if (n <= kNucCap) {
+          nuc_select(sk, sw, n, above2, target, sm);
+          done = true;
+        }
       }
     }
-  }
-  if (done) {
-    S_kept = sm.nuc_above;
-    cut = keyf(sm.nuc_key);
+    if (done) {
+      S_kept = sm.nuc_above;
+      cut = keyf(sm.nuc_key);
+      __syncthreads();
+      return;
+    }
     __syncthreads();
-    return;
+    if (!deeper || span == kHeadBins - 1) break;
   }
-  __syncthreads();
   // ---- multi-pass path: a crowded head, a cut in the tail, or a large boundary bucket ----
   const uint32_t kthr = thr == -INFINITY ? 0u : fkey(thr);  // keys below it are outside top-k
   NucSel sel{-1, 0u, 0u};
