@@ -151,8 +151,10 @@ typedef struct {
  * spec_verify with the sampling parameters of spec_sampling_t (all other arguments, the
  * workspace size and the results as for spec_verify; `sampling` is a host pointer read before
  * the call returns).  spec_verify(..., T, top_k, ...) is spec_verify_ex with {T, T, top_k, 1}.
- * With top_p < 1 the per-request pass also reads every valid row once or more (two levels for
- * bf16, four for f32, the later ones mostly from L2) to find each row's nucleus.
+ * With top_p < 1 (and top-k off) a nucleus pass between the two reads every valid row once more to
+ * find its nucleus: twice when the cut lies below 2^-13 of the max's weight, and a few times more
+ * (4-bit key digits, mostly from L2) for rows whose head is crowded or whose cut lies below 2^-15.
+ * After top-k the per-request pass finds the nucleus among the kept candidates.
  * Returns SPEC_ERR_INVALID_ARG for sampling == NULL, T_q <= 0 with T > 0, or top_p <= 0 / NaN.
  */
 spec_status_t spec_verify_ex(const void* p_logits, const void* q_logits, const int32_t* draft_tokens,
