@@ -177,11 +177,10 @@ def describe(w: W.Workload) -> str:
 
 def launches_per_step(w: W.Workload) -> int:
     """Kernels of one step: the streaming pass and the per-request pass, plus the ragged row
-    table, the nucleus pass (top-p without top-k) and, for sampling, the q(x) kernel."""
+    table and the nucleus pass (top-p without top-k).  The sampler's q(x) comes from the
+    per-request pass."""
     n = 2 + (w.ragged is not None)
     if w.temperature > 0 and w.top_p < 1.0 and not (0 < w.top_k < w.V):
-        n += 1
-    if w.K == 0 and w.temperature >= 0:
         n += 1
     return n
 

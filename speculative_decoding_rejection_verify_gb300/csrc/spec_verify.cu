@@ -82,6 +82,7 @@ struct Params {
   float* samp_margin;
   float* resid_mass;
   float* lognorm;
+  float* sample_prob;             // draft-token sampling (K = 0): q(x) of each row's drawn token, or null
   int32_t* flags;
   void* pass1_done;               // optional cudaEvent_t recorded after the streaming pass
   int B, K, V, top_k, nchunk, R;  // R = padded rows per request (2K+1, or K+1 in greedy)
@@ -2274,6 +2275,16 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
       P.lognorm[(size_t)b * R + r] = v;
     }
   }
+  if (P.sample_prob && t == 0) {
+    // q(x) of the drawn token under the row's distribution: exp(z_x / T - log-normaliser), 1 for
+    // the greedy draft's one-hot, NaN for a row without a result.  Thread 0 wrote tok[0].
+    const int y = tok[0];
+    float pr = NAN;
+    if (y >= 0 && y < P.V)
+      pr = MODE == kGreedy ? 1.0f
+                           : expf(load1<T>(prow<T>(P, b, 0) + y) * P.invT - (sm.rowM[0] * P.invT + logf(sm.rowS[0])));
+    P.sample_prob[b] = pr;
+  }
   if (MODE == kGreedy && t < K) {
     if (P.p_draft) P.p_draft[(size_t)b * K + t] = NAN;
     if (P.q_draft) P.q_draft[(size_t)b * K + t] = NAN;
@@ -2614,21 +2625,6 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const Params P) {
   }
 }
 
-// Sampling: q(x) of each drawn token, exp(z_x / T - the row's log-normaliser over its kept set);
-// 1 in greedy mode (the draft's one-hot); NaN for a row without a result.
-template <typename T>
-__global__ void __launch_bounds__(256) sample_prob_kernel(const T* __restrict__ logits, const int32_t* __restrict__ tok,
-                                                          const float* __restrict__ lognorm, float invT, int rows,
-                                                          int V, float* __restrict__ out) {
-  pdl_wait();
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= rows) return;
-  const int y = tok[i];
-  float pr = NAN;
-  if (y >= 0 && y < V) pr = invT == 0.0f ? 1.0f : expf(load1<T>(logits + (size_t)i * V + y) * invT - lognorm[i]);
-  out[i] = pr;
-}
-
 // Pass 2 for batches of fewer requests than SMs (sampling mode): a cluster of kCluster blocks per
 // request, which share the full-row residual draw (cluster_draw).
 template <typename T, bool VEC>
@@ -2841,12 +2837,15 @@ size_t spec_verify_workspace_bytes(int32_t B, int32_t K_max, int32_t V, spec_dty
   return a.bytes > b.bytes ? a.bytes : b.bytes;
 }
 
-spec_status_t spec_verify_ex(const void* p_logits, const void* q_logits, const int32_t* draft_tokens,
-                             const int32_t* k_per_row, const float* u_accept, const float* u_resample,
-                             const spec_sampling_t* sampling, int32_t* out_tokens,
-                             int32_t* out_num_accepted, const spec_verify_stats_t* out_stats, int32_t B,
-                             int32_t K_max, int32_t V, spec_dtype_t dtype, void* workspace,
-                             size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+// spec_verify_ex with, for the sampler, q(x) of each request's drawn token written to sample_prob.
+static spec_status_t verify_impl(const void* p_logits, const void* q_logits, const int32_t* draft_tokens,
+                                 const int32_t* k_per_row, const float* u_accept, const float* u_resample,
+                                 const spec_sampling_t* sampling, int32_t* out_tokens, int32_t* out_num_accepted,
+                                 const spec_verify_stats_t* out_stats, int32_t B, int32_t K_max, int32_t V,
+                                 spec_dtype_t dtype, void* workspace, size_t workspace_bytes, void* stream,
+                                 float* sample_prob) {
   if (B < 0 || K_max < 0 || V <= 0 || !sampling) return SPEC_ERR_INVALID_ARG;
   const float temperature = sampling->temperature, tq = sampling->draft_temperature;
   const int32_t top_k = sampling->top_k;
@@ -2889,6 +2888,7 @@ spec_status_t spec_verify_ex(const void* p_logits, const void* q_logits, const i
   P.samp_margin = st.sample_margin;
   P.resid_mass = st.residual_mass;
   P.lognorm = st.row_lognorm;
+  P.sample_prob = sample_prob;
   P.flags = st.flags;
   P.pass1_done = st.pass1_done;
   P.B = B;
@@ -2922,6 +2922,18 @@ spec_status_t spec_verify_ex(const void* p_logits, const void* q_logits, const i
   cudaError_t e = dtype == SPEC_DTYPE_BF16 ? launch_mode<uint16_t>(mode, vec, P, items, s)
                                            : launch_mode<float>(mode, vec, P, items, s);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+extern "C" {
+
+spec_status_t spec_verify_ex(const void* p_logits, const void* q_logits, const int32_t* draft_tokens,
+                             const int32_t* k_per_row, const float* u_accept, const float* u_resample,
+                             const spec_sampling_t* sampling, int32_t* out_tokens,
+                             int32_t* out_num_accepted, const spec_verify_stats_t* out_stats, int32_t B,
+                             int32_t K_max, int32_t V, spec_dtype_t dtype, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  return verify_impl(p_logits, q_logits, draft_tokens, k_per_row, u_accept, u_resample, sampling, out_tokens,
+                     out_num_accepted, out_stats, B, K_max, V, dtype, workspace, workspace_bytes, stream, nullptr);
 }
 
 spec_status_t spec_verify(const void* p_logits, const void* q_logits, const int32_t* draft_tokens,
@@ -3022,7 +3034,7 @@ spec_status_t spec_verify_host(const void* p_logits, const void* q_logits,
 size_t spec_sample_workspace_bytes(int32_t rows, int32_t V, spec_dtype_t dtype, int32_t top_k) {
   const size_t ws = spec_verify_workspace_bytes(rows, 0, V, dtype, top_k);
   if (ws == 0) return 0;
-  return ws + 2 * align256((size_t)rows * sizeof(int32_t));  // + accepted counts and normalisers
+  return ws + align256((size_t)rows * sizeof(int32_t));  // + the accepted counts
 }
 
 spec_status_t spec_sample(const void* logits, const float* u, const spec_sampling_t* sampling, int32_t* out_tokens,
@@ -3039,25 +3051,10 @@ spec_status_t spec_sample(const void* logits, const float* u, const spec_samplin
   char* ws = static_cast<char*>(workspace);
   if (rows > 0 && (!ws || ((uintptr_t)ws & 255u) || workspace_bytes < need)) return SPEC_ERR_WORKSPACE;
   int32_t* nacc = rows > 0 ? reinterpret_cast<int32_t*>(ws + base) : nullptr;
-  float* ln = rows > 0 ? reinterpret_cast<float*>(ws + base + align256((size_t)rows * sizeof(int32_t))) : nullptr;
-  spec_verify_stats_t st = {};
-  st.row_lognorm = out_prob ? ln : nullptr;
-  // a request with no drafts: its one token is the draw from p at position 0 (the bonus draw)
-  spec_status_t r = spec_verify_ex(logits, nullptr, nullptr, nullptr, nullptr, u, &sp, out_tokens, nacc, &st, rows, 0,
-                                   V, dtype, ws, base, stream);
-  if (r != SPEC_OK || rows == 0 || !out_prob) return r;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const float invT = sp.temperature > 0.0f ? (float)(1.0 / (double)sp.temperature) : 0.0f;
-  const unsigned grid = (unsigned)((rows + 255) / 256);
-  cudaError_t e;
-  if (dtype == SPEC_DTYPE_BF16)
-    e = launch_after(sample_prob_kernel<uint16_t>, dim3(grid), dim3(256), 0, s, true,
-                     static_cast<const uint16_t*>(logits), (const int32_t*)out_tokens, (const float*)ln, invT, rows, V,
-                     out_prob);
-  else
-    e = launch_after(sample_prob_kernel<float>, dim3(grid), dim3(256), 0, s, true, static_cast<const float*>(logits),
-                     (const int32_t*)out_tokens, (const float*)ln, invT, rows, V, out_prob);
-  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  // a request with no drafts: its one token is the draw from p at position 0 (the bonus draw); the
+  // per-request pass also writes q(x) of the drawn token
+  return verify_impl(logits, nullptr, nullptr, nullptr, nullptr, u, &sp, out_tokens, nacc, nullptr, rows, 0, V,
+                     dtype, ws, base, stream, rows > 0 ? out_prob : nullptr);
 }
 
 const char* spec_verify_status_string(spec_status_t status) {
