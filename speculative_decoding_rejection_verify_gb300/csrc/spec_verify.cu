@@ -2571,8 +2571,10 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
 // chunk summaries into its (max, sum), exactly as the per-request pass does, finds the row's
 // nucleus and leaves (kept mass, cut) for the per-request pass.  Non-finite rows are left to the
 // per-request pass, which flags them.
+// Three blocks per SM is what its shared memory allows; saying so lets the compiler keep the list
+// pass in 80 registers instead of spilling at 64.
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(kThreads) nucleus_kernel(const Params P) {
+__global__ void __launch_bounds__(kThreads, 3) nucleus_kernel(const Params P) {
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ Smem sm;
   pdl_wait();
