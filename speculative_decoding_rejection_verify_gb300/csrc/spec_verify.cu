@@ -8,18 +8,18 @@
 //   gsyq.cn/news/428210 §3.3                                  temperature / top-k on both sides.
 //
 // Design.  The work is a stream over every logit of every valid row (HBM bound), plus a small
-// per-request tail.  One persistent kernel does all of it:
-//   * the item space is (request, row, 8192-logit chunk) in request-major order; CTAs take items
-//     from an atomic counter (one 16-32 KB chunk per item, read with 128-bit non-allocating loads);
-//   * each item leaves a per-chunk summary in the workspace: (max, sum of exp) for sampling,
-//     (max, lowest argmax) for greedy, the chunk's top-k candidates for top-k;
-//   * the CTA that completes the last item of a request (a counter per request; no block ever
-//     waits for another) combines the summaries into each row's normaliser, runs the ratio test
-//     and the first-rejection scan, and draws the resampled / bonus token by inverse CDF over the
-//     one or two rows it needs, which were streamed microseconds earlier and are still in L2;
-//   * all counters return to zero by the end of the kernel, so the workspace is reusable.
-// A request-major item order keeps only a few requests in flight, which is what keeps the rows of
-// the final draw L2-resident.  There is no tensor-core work: nothing here is a contraction.
+// per-request tail, in two kernels chained by programmatic dependent launch:
+//   * the streaming pass (stats_kernel): a persistent grid whose blocks each own a contiguous range
+//     of (request, row, 16 KB chunk) items; thread 0 moves every chunk into a shared-memory ring
+//     with one bulk copy (the copy engine) completing on an mbarrier, and each warp leaves a
+//     summary of its share: (max, sum of exp) for sampling, (max, lowest argmax) for greedy, a
+//     running candidate set for top-k;
+//   * the per-request pass (finish_kernel; 8-block clusters for small batches): one block per
+//     request merges its rows' summaries into normalisers, runs the ratio test and the
+//     first-rejection scan, and draws the resampled or bonus token by inverse CDF, re-reading only
+//     the rows (or the chunk) the draw needs;
+//   * with top-p and no top-k, a nucleus pass between them finds each row's nucleus.
+// There is no tensor-core work: nothing here is a contraction.
 
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
@@ -37,7 +37,7 @@ namespace sv {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kChunkBytes = 16384;      // bytes of logits per work item (16 B per thread x 4)
-constexpr int kStages = 4;               // work items in flight per CTA (cp.async ring)
+constexpr int kStages = 4;               // work items in flight per CTA (bulk-copy ring)
 constexpr int kCluster = 8;              // blocks sharing one request's draw when requests are few
 constexpr int kStagesTopK = 3;           // top-k: a shallower ring leaves room for 3 blocks per SM
 __host__ __device__ constexpr int stages_of(int mode) { return mode == 1 ? kStagesTopK : kStages; }
@@ -298,6 +298,45 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// Bulk copies (the copy engine, TMA) completing on shared-memory mbarriers: one thread moves a whole
+// 16 KB chunk with one instruction; the stage's barrier counts the arriving bytes.
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count) : "memory");
+}
+// makes the barriers' initialisation visible to the copy engine
+__device__ __forceinline__ void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(smem_addr(b)), "r"(parity)
+      : "memory");
+  return done != 0u;
+}
+// Waits for the phase of the given parity to complete; false if it has not after kWaitLimit tries
+// (each try suspends the thread for a while), which no working copy engine comes near.
+constexpr int kWaitLimit = 1 << 20;
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
+  for (int i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(b, parity)) return true;
+  return false;
+}
+// bytes (a multiple of 16) from global src (16-byte aligned) into shared dst, completing on b
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* b) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(src), "r"(bytes), "r"(smem_addr(b))
+               : "memory");
+}
+
 // ------------------------------------------------------------------------------------------------
 // shared memory
 // ------------------------------------------------------------------------------------------------
@@ -340,6 +379,8 @@ struct Smem {
   int nuc_n;         // logits gathered
   uint32_t nuc_key;  // key of the cut
   uint32_t red_cnt[32];
+  uint64_t ring_full[kStages];   // streaming pass: a stage's bytes have landed
+  uint64_t ring_empty[kStages];  // streaming pass: every warp has read the stage
 };
 
 // ------------------------------------------------------------------------------------------------
@@ -2340,7 +2381,8 @@ __device__ __forceinline__ void cursor_next(const Params& P, Cursor& k) {
   k.row = row_bytes<T>(P, k.b, k.rp);
 }
 
-// Starts the copy of the cursor's chunk into `stage` (16 bytes per thread per vector).
+// Top-k mode's per-thread ring: starts the copy of the cursor's chunk into `stage`, each thread
+// its own 16-byte vectors (which it alone reads back).
 template <typename T>
 __device__ __forceinline__ void issue_at(const Params& P, const Cursor& k, uint4* stage) {
   const int v0 = k.c * Cfg<T>::CH;
@@ -2485,8 +2527,8 @@ __device__ __forceinline__ void greedy_vec(uint4 (&raw)[Cfg<T>::LOADS], int n, i
 
 // Pass 1: stream every valid row once.  Each CTA owns a contiguous range of items
 // (request, row, chunk), so successive items walk memory in order and the cursor needs no
-// divisions; the cp.async ring keeps the next kStages - 1 chunks in flight.  No block waits for
-// another and nothing is counted: pass 2 starts when this grid is done.
+// divisions; for aligned rows the bulk-copy ring keeps the next kStages - 1 chunks in flight.  No
+// block waits for another and nothing is counted: pass 2 starts when this grid is done.
 template <typename T, int MODE, bool VEC>
 __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
   extern __shared__ __align__(128) unsigned char dyn[];
@@ -2514,7 +2556,11 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
     else
       topk_chunk<T, VEC>(P, v, n, k.b, k.rp, k.c, seg_start, seg_end, surv, sm, seg_next, seg_m);
   };
-  if (VEC) {
+  if (VEC && MODE == kTopK) {
+    // Top-k mode keeps a per-thread ring: each thread copies its own vectors of a chunk and refills
+    // its slots as soon as it has read them.  (With the shared ring below, a stage is refilled only
+    // once every warp has read it; between the block barriers of the candidate set that cost the
+    // fp32 top-k pass 6%.)
     Cursor ic = cc;
 #pragma unroll
     for (int s = 0; s < ST; ++s) {
@@ -2538,22 +2584,90 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
       cp_async_commit();
       seg_end = it + 1 == hi || cc.c + 1 == P.nchunk;
       const int n = min(Cfg<T>::CH, P.V - cc.c * Cfg<T>::CH);
-      if (MODE == kSample) {
-        const size_t slot = ((size_t)cc.b * P.R + cc.rp) * P.nchunk + cc.c;
-        sample_vec<T>(cc.rp > P.K ? P.c2q : P.c2, raw, n, P.partial + slot * kWarps);
-      } else if (MODE == kGreedy) {
-        const size_t slot = ((size_t)cc.b * P.R + cc.rp) * P.nchunk + cc.c;
-        greedy_vec<T>(raw, n, cc.c * Cfg<T>::CH, P.partial + slot * kWarps);
-      } else {
-        float v[Cfg<T>::PER];
-        unpack<T>(raw, n, v);
-        summarise_f(cc, v);
-      }
+      float v[Cfg<T>::PER];
+      unpack<T>(raw, n, v);
+      summarise_f(cc, v);
       seg_start = seg_end;
       cursor_next<T>(P, cc);
       s = s + 1 == ST ? 0 : s + 1;
     }
     cp_async_wait<0>();
+  } else if (VEC) {
+    // The ring: thread 0 moves each item (16 KB, or the row's tail) into its stage with one bulk
+    // copy that completes on the stage's `full` barrier; every warp reads its vectors of the stage
+    // into registers and arrives on the stage's `empty` barrier, and thread 0 refills the stage
+    // once all eight warps have.  Every wait is bounded: a thread whose wait gives up waits no more
+    // (thread 0 then copies no more), the loop runs out on whatever the stages hold, and the block
+    // drains its copies in flight and marks all its items NaN, so that their requests come out
+    // flagged non-finite rather than wrong.  (Sampling and greedy modes.)
+    const int t = threadIdx.x;
+    uint64_t* full = sm.ring_full;
+    uint64_t* empty = sm.ring_empty;
+    if (t == 0) {
+      for (int q = 0; q < ST; ++q) {
+        mbar_init(&full[q], 1);
+        mbar_init(&empty[q], kWarps);
+      }
+      mbar_fence_init();
+    }
+    __syncthreads();
+    bool failed = false;
+    uint32_t used = 0u, last_par = 0u;  // thread 0: stages copied into, parity of each one's last copy
+    auto issue = [&](int q, const Cursor& k, uint32_t par) {
+      const uint32_t nb = (uint32_t)(min(Cfg<T>::CH, P.V - k.c * Cfg<T>::CH) * (int)sizeof(T));
+      mbar_arrive_expect_tx(&full[q], nb);
+      bulk_copy(stages + (size_t)q * (kChunkBytes / 16), k.row + (size_t)k.c * Cfg<T>::CH * sizeof(T), nb, &full[q]);
+      used |= 1u << q;
+      last_par = (last_par & ~(1u << q)) | (par << q);
+    };
+    Cursor ic = cc;
+    for (int q = 0; q < ST; ++q) {
+      if (lo + q < hi) {
+        if (t == 0) issue(q, ic, 0u);
+        cursor_next<T>(P, ic);
+      }
+    }
+    int s = 0;
+    uint32_t phase = 0u;  // parity of the stages' current use
+    for (uint32_t it = lo; it < hi; ++it) {
+      uint4* st = stages + (size_t)s * (kChunkBytes / 16);
+      if (!failed) failed = !mbar_wait(&full[s], phase);
+      uint4 raw[Cfg<T>::LOADS];
+#pragma unroll
+      for (int l = 0; l < Cfg<T>::LOADS; ++l) raw[l] = st[l * kThreads + t];
+      __syncwarp();
+      if ((t & 31) == 0) mbar_arrive(&empty[s]);
+      if (it + ST < hi) {  // refill the stage once every warp holds its bytes
+        if (t == 0 && !failed) {
+          failed = !mbar_wait(&empty[s], phase);
+          if (!failed) issue(s, ic, phase ^ 1u);
+        }
+        cursor_next<T>(P, ic);
+      }
+      const int n = min(Cfg<T>::CH, P.V - cc.c * Cfg<T>::CH);
+      const size_t slot = ((size_t)cc.b * P.R + cc.rp) * P.nchunk + cc.c;
+      if (MODE == kSample)
+        sample_vec<T>(cc.rp > P.K ? P.c2q : P.c2, raw, n, P.partial + slot * kWarps);
+      else
+        greedy_vec<T>(raw, n, cc.c * Cfg<T>::CH, P.partial + slot * kWarps);
+      cursor_next<T>(P, cc);
+      if (++s == ST) {
+        s = 0;
+        phase ^= 1u;
+      }
+    }
+    if (__syncthreads_or(failed)) {
+      if (t == 0)
+        for (int q = 0; q < ST; ++q)
+          if ((used >> q) & 1u) mbar_wait(&full[q], (last_par >> q) & 1u);
+      Cursor mc;
+      cursor_at<T>(P, lo, mc);
+      for (uint32_t it = lo; it < hi; ++it) {
+        const size_t slot = ((size_t)mc.b * P.R + mc.rp) * P.nchunk + mc.c;
+        if (t < kWarps) P.partial[slot * kWarps + t] = make_float2(NAN, MODE == kGreedy ? __int_as_float(-1) : NAN);
+        cursor_next<T>(P, mc);
+      }
+    }
   } else {
     for (uint32_t it = lo; it < hi; ++it) {
       const int v0 = cc.c * Cfg<T>::CH;
