@@ -217,6 +217,16 @@ spec_status_t spec_sample(const void* logits, const float* u, const spec_samplin
                           float* out_prob, int32_t rows, int32_t V, spec_dtype_t dtype, void* workspace,
                           size_t workspace_bytes, void* stream);
 
+/*
+ * Test support, not for production use.  With bit 0 of `hooks` set, every later call (from any
+ * host thread) makes each block of the streaming pass withhold its first bulk copy: every wait for
+ * it runs out after a short limit, the block marks all its chunks NaN, and every request of the
+ * batch that uses sampling or greedy mode comes out with SPEC_FLAG_NONFINITE, n_acc 0 and tokens -1
+ * (top-k batches are not affected).  It exercises the bounded-wait failure path of the streaming
+ * pass without any fault.  0 restores normal operation.
+ */
+void spec_verify_set_test_hooks(int32_t hooks);
+
 /* Size of the fixed device array behind spec_verify_static (16 MiB). */
 #define SPEC_STATIC_SCRATCH_BYTES (16u << 20)
 

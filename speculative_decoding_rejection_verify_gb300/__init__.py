@@ -46,7 +46,7 @@ MAX_TOPK = 256
 
 EXPORTS = ("spec_verify_workspace_bytes", "spec_verify", "spec_verify_ex", "spec_verify_host_staging_bytes",
            "spec_verify_host", "spec_verify_host_ex", "spec_verify_static", "spec_verify_status_string",
-           "spec_sample_workspace_bytes", "spec_sample")
+           "spec_sample_workspace_bytes", "spec_sample", "spec_verify_set_test_hooks")
 CONTROL_EXPORTS = ("spec_ctrl_default_config", "spec_ctrl_create", "spec_ctrl_destroy", "spec_ctrl_update",
                    "spec_ctrl_skip", "spec_ctrl_k", "spec_ctrl_window_mean", "spec_ctrl_window_fill",
                    "spec_ctrl_totals")
@@ -127,6 +127,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
             lib.spec_sample_workspace_bytes.restype = Z
             lib.spec_sample.argtypes = [P, P, ctypes.POINTER(SamplingStruct), P, P, I, I, I, P, Z, P]
             lib.spec_sample.restype = I
+            lib.spec_verify_set_test_hooks.argtypes = [I]
+            lib.spec_verify_set_test_hooks.restype = None
             CP = ctypes.POINTER(ControlConfig)
             lib.spec_ctrl_default_config.argtypes = [CP]
             lib.spec_ctrl_default_config.restype = None
@@ -163,6 +165,12 @@ def _dtype_code(t) -> int:
     if t.dtype == torch.bfloat16:
         return DTYPE_BF16
     raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def set_test_hooks(hooks: int) -> None:
+    """spec_verify_set_test_hooks (test support: bit 0 makes the streaming pass's bounded waits
+    run out, so a batch comes out flagged non-finite)."""
+    load().spec_verify_set_test_hooks(int(hooks))
 
 
 def workspace_bytes(B: int, K: int, V: int, dtype: int, top_k: int = 0) -> int:

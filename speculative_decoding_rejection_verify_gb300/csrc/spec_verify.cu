@@ -83,6 +83,7 @@ struct Params {
   float* resid_mass;
   float* lognorm;
   float* sample_prob;             // draft-token sampling (K = 0): q(x) of each row's drawn token, or null
+  int test_hooks;                 // spec_verify_set_test_hooks: 0 in normal operation
   int32_t* flags;
   void* pass1_done;               // optional cudaEvent_t recorded after the streaming pass
   int B, K, V, top_k, nchunk, R;  // R = padded rows per request (2K+1, or K+1 in greedy)
@@ -324,8 +325,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
 // Waits for the phase of the given parity to complete; false if it has not after kWaitLimit tries
 // (each try suspends the thread for a while), which no working copy engine comes near.
 constexpr int kWaitLimit = 1 << 20;
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
-  for (int i = 0; i < kWaitLimit; ++i)
+constexpr int kTestWaitLimit = 1 << 10;  // under the test hook that withholds a copy
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, int limit = kWaitLimit) {
+  for (int i = 0; i < limit; ++i)
     if (mbar_try_wait(b, parity)) return true;
   return false;
 }
@@ -2613,6 +2615,9 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
     __syncthreads();
     bool failed = false;
     uint32_t used = 0u, last_par = 0u;  // thread 0: stages copied into, parity of each one's last copy
+    // test hook 1: the block's first copy is withheld, so every wait for it runs out (soon)
+    const bool withhold = (P.test_hooks & 1) != 0;
+    const int limit = withhold ? kTestWaitLimit : kWaitLimit;
     auto issue = [&](int q, const Cursor& k, uint32_t par) {
       const uint32_t nb = (uint32_t)(min(Cfg<T>::CH, P.V - k.c * Cfg<T>::CH) * (int)sizeof(T));
       mbar_arrive_expect_tx(&full[q], nb);
@@ -2623,7 +2628,7 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
     Cursor ic = cc;
     for (int q = 0; q < ST; ++q) {
       if (lo + q < hi) {
-        if (t == 0) issue(q, ic, 0u);
+        if (t == 0 && !(withhold && q == 0)) issue(q, ic, 0u);
         cursor_next<T>(P, ic);
       }
     }
@@ -2631,7 +2636,7 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
     uint32_t phase = 0u;  // parity of the stages' current use
     for (uint32_t it = lo; it < hi; ++it) {
       uint4* st = stages + (size_t)s * (kChunkBytes / 16);
-      if (!failed) failed = !mbar_wait(&full[s], phase);
+      if (!failed) failed = !mbar_wait(&full[s], phase, limit);
       uint4 raw[Cfg<T>::LOADS];
 #pragma unroll
       for (int l = 0; l < Cfg<T>::LOADS; ++l) raw[l] = st[l * kThreads + t];
@@ -2639,7 +2644,7 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
       if ((t & 31) == 0) mbar_arrive(&empty[s]);
       if (it + ST < hi) {  // refill the stage once every warp holds its bytes
         if (t == 0 && !failed) {
-          failed = !mbar_wait(&empty[s], phase);
+          failed = !mbar_wait(&empty[s], phase, limit);
           if (!failed) issue(s, ic, phase ^ 1u);
         }
         cursor_next<T>(P, ic);
@@ -2659,7 +2664,7 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
     if (__syncthreads_or(failed)) {
       if (t == 0)
         for (int q = 0; q < ST; ++q)
-          if ((used >> q) & 1u) mbar_wait(&full[q], (last_par >> q) & 1u);
+          if ((used >> q) & 1u) mbar_wait(&full[q], (last_par >> q) & 1u, limit);
       Cursor mc;
       cursor_at<T>(P, lo, mc);
       for (uint32_t it = lo; it < hi; ++it) {
@@ -2955,6 +2960,10 @@ size_t spec_verify_workspace_bytes(int32_t B, int32_t K_max, int32_t V, spec_dty
 
 }  // extern "C"
 
+namespace sv {
+std::atomic<int32_t> g_test_hooks{0};  // spec_verify_set_test_hooks
+}  // namespace sv
+
 // spec_verify_ex with, for the sampler, q(x) of each request's drawn token written to sample_prob.
 static spec_status_t verify_impl(const void* p_logits, const void* q_logits, const int32_t* draft_tokens,
                                  const int32_t* k_per_row, const float* u_accept, const float* u_resample,
@@ -3005,6 +3014,7 @@ static spec_status_t verify_impl(const void* p_logits, const void* q_logits, con
   P.resid_mass = st.residual_mass;
   P.lognorm = st.row_lognorm;
   P.sample_prob = sample_prob;
+  P.test_hooks = sv::g_test_hooks.load(std::memory_order_relaxed);
   P.flags = st.flags;
   P.pass1_done = st.pass1_done;
   P.B = B;
@@ -3172,6 +3182,8 @@ spec_status_t spec_sample(const void* logits, const float* u, const spec_samplin
   return verify_impl(logits, nullptr, nullptr, nullptr, nullptr, u, &sp, out_tokens, nacc, nullptr, rows, 0, V,
                      dtype, ws, base, stream, rows > 0 ? out_prob : nullptr);
 }
+
+void spec_verify_set_test_hooks(int32_t hooks) { sv::g_test_hooks.store(hooks, std::memory_order_relaxed); }
 
 const char* spec_verify_status_string(spec_status_t status) {
   switch (status) {
