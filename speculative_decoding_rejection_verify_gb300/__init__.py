@@ -184,12 +184,16 @@ def workspace_bytes(B: int, K: int, V: int, dtype: int, top_k: int = 0) -> int:
 _ws_cache: Dict[Tuple[int, int], object] = {}
 
 
-def workspace(nbytes: int, device, stream_handle: int):
+def workspace(nbytes: int, device, stream):
+    """The cached scratch buffer of ``stream`` (a torch.cuda.Stream), grown to ``nbytes``.  It is
+    allocated on that stream, so when a larger one replaces it the caching allocator hands the old
+    memory out again only in that stream's order, after the calls that used it."""
     torch = _torch()
-    key = (device.index if device.index is not None else torch.cuda.current_device(), stream_handle)
+    key = (device.index if device.index is not None else torch.cuda.current_device(), stream.cuda_stream)
     ws = _ws_cache.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.zeros(nbytes, dtype=torch.uint8, device=device)
+        with torch.cuda.stream(stream):
+            ws = torch.zeros(nbytes, dtype=torch.uint8, device=device)
         _ws_cache[key] = ws
     return ws
 
@@ -261,7 +265,7 @@ def verify(p, q, draft, k_per_row=None, u_accept=None, u_resample=None, temperat
         sp = sp if sp is not None else StatsStruct()
         sp.pass1_done = pass1_event.cuda_event
     nbytes = workspace_bytes(B, K, V, dt, top_k)
-    ws = workspace_tensor if workspace_tensor is not None else workspace(nbytes, dev, handle)
+    ws = workspace_tensor if workspace_tensor is not None else workspace(nbytes, dev, st)
     smp = _sampling(temperature, draft_temperature, top_k, top_p)
     rc = lib.spec_verify_ex(_ptr(p), _ptr(q), _ptr(draft), _ptr(k_per_row), _ptr(u_accept), _ptr(u_resample),
                             ctypes.byref(smp), tokens.data_ptr(), nacc.data_ptr(),
@@ -295,7 +299,7 @@ def sample(logits, u=None, temperature: float = 1.0, top_k: int = 0, top_p: floa
     nbytes = lib.spec_sample_workspace_bytes(rows, V, dt, int(top_k))
     if nbytes == 0:
         raise SpecVerifyError(1, "spec_sample_workspace_bytes")
-    ws = workspace_tensor if workspace_tensor is not None else workspace(nbytes, dev, st.cuda_stream)
+    ws = workspace_tensor if workspace_tensor is not None else workspace(nbytes, dev, st)
     smp = SamplingStruct(float(temperature), float(temperature), int(top_k), float(top_p))
     rc = lib.spec_sample(_ptr(logits), _ptr(u), ctypes.byref(smp), tokens.data_ptr(),
                          None if pr is None else pr.data_ptr(), rows, V, dt, ws.data_ptr(), ws.numel(),
