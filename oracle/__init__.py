@@ -67,6 +67,11 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_verify_ex.argtypes = [_P, _P, _P, _P, _P, _P, f32, f32, i32, f32, _P, _P, _P, _P, _P, _P,
                                      _P, _P, _P, _P, i32, i32, i32, i32, i32]
     lib.oracle_verify_ex.restype = i32
+    lib.oracle_verify_cuts.argtypes = [_P, _P, _P, _P, _P, _P, f32, f32, i32, f32, _P, _P, _P, _P, _P, _P,
+                                       _P, _P, _P, _P, _P, _P, i32, i32, i32, i32, i32]
+    lib.oracle_verify_cuts.restype = i32
+    lib.oracle_row_dist_at.argtypes = [_P, i32, i32, f64, i32, f64, f64, _P, _P]
+    lib.oracle_row_dist_at.restype = i32
     lib.oracle_decide_trials.argtypes = [_P, _P, i32, i32, i32, _P, _P, _P, _P, _P, _P, i32]
     lib.oracle_decide_trials.restype = i32
     return lib
@@ -100,18 +105,20 @@ def _logits(a: np.ndarray):
     raise TypeError(f"logits must be float32 or bf16 bits (uint16), got {a.dtype}")
 
 
-def row_dist(z: np.ndarray, temperature: float, top_k: int = 0, top_p: float = 1.0, lib=None):
+def row_dist(z: np.ndarray, temperature: float, top_k: int = 0, top_p: float = 1.0, lib=None,
+             cut: Optional[float] = None):
     """Normalised distribution of one logit row (temperature, then top-k, then top-p).
 
     Returns (P float64[V], info dict {m, lognorm, threshold, kept, threshold_p, nucleus_margin},
-    flags).  top_p is taken as the float32 value the CUDA library receives."""
+    flags).  top_p is taken as the float32 value the CUDA library receives.  ``cut``: a nucleus
+    cut to take instead of finding one (keep the logits >= cut inside the top-k set)."""
     lib = lib or load()
     z, dt = _logits(z)
     V = z.shape[-1]
     P = np.empty(V, np.float64)
     info = np.empty(6, np.float64)
-    fl = lib.oracle_row_dist_ex(_ptr(z), dt, V, float(temperature), int(top_k), float(np.float32(top_p)),
-                                _ptr(P), _ptr(info))
+    fl = lib.oracle_row_dist_at(_ptr(z), dt, V, float(temperature), int(top_k), float(np.float32(top_p)),
+                                float("nan") if cut is None else float(cut), _ptr(P), _ptr(info))
     return P, dict(m=info[0], lognorm=info[1], threshold=info[2], kept=info[3], threshold_p=info[4],
                    nucleus_margin=info[5]), int(fl)
 
@@ -164,13 +171,15 @@ def decide_trials(P: np.ndarray, Q: np.ndarray, x: np.ndarray, ua: np.ndarray, u
 def verify(p: np.ndarray, q: Optional[np.ndarray], draft: np.ndarray, k_per_row: Optional[np.ndarray],
            ua: Optional[np.ndarray], ur: Optional[np.ndarray], temperature: float, top_k: int = 0,
            nthreads: int = 1, lib=None, draft_temperature: Optional[float] = None,
-           top_p: float = 1.0) -> dict:
+           top_p: float = 1.0, row_cut: Optional[np.ndarray] = None) -> dict:
     """The whole verify step on host arrays, same argument meaning as the CUDA ``spec_verify_ex``.
 
     p: [B, K_max+1, V], q: [B, K_max, V] (float32 or bf16-as-uint16; q may be None when
     temperature == 0), draft: [B, K_max] int32, k_per_row: [B] int32 or None, ua: [B, K_max],
-    ur: [B] float32; draft_temperature None = temperature; top_p 1 = off.  Returns a dict of
-    numpy outputs (tokens, n_acc, stats..., flags, nucleus_margin [B, 2*K_max+1])."""
+    ur: [B] float32; draft_temperature None = temperature; top_p 1 = off.  ``row_cut``
+    [B, 2*K_max+1] (optional): per row, NaN = find the nucleus, a value = take it as the nucleus
+    cut.  Returns a dict of numpy outputs (tokens, n_acc, stats..., flags, nucleus_margin and
+    row_cut [B, 2*K_max+1], the latter each row's smallest kept logit bound)."""
     lib = lib or load()
     p, dt = _logits(p)
     B, K1, V = p.shape
@@ -186,14 +195,17 @@ def verify(p: np.ndarray, q: Optional[np.ndarray], draft: np.ndarray, k_per_row:
         tokens=np.empty((B, K_max + 1), np.int32), n_acc=np.empty(B, np.int32),
         p_draft=np.empty((B, K_max)), q_draft=np.empty((B, K_max)), accept_margin=np.empty((B, K_max)),
         sample_margin=np.empty(B), residual_mass=np.empty(B), row_lognorm=np.empty((B, 2 * K_max + 1)),
-        nucleus_margin=np.empty((B, 2 * K_max + 1)), flags=np.empty(B, np.int32))
+        nucleus_margin=np.empty((B, 2 * K_max + 1)), row_cut=np.empty((B, 2 * K_max + 1)),
+        flags=np.empty(B, np.int32))
     tq = temperature if draft_temperature is None else draft_temperature
-    rc = lib.oracle_verify_ex(_ptr(p), _ptr(q), _ptr(draft), _ptr(kpr), _ptr(ua), _ptr(ur),
-                              float(temperature), float(tq), int(top_k), float(top_p),
-                              _ptr(out["tokens"]), _ptr(out["n_acc"]),
-                              _ptr(out["p_draft"]), _ptr(out["q_draft"]), _ptr(out["accept_margin"]),
-                              _ptr(out["sample_margin"]), _ptr(out["residual_mass"]), _ptr(out["row_lognorm"]),
-                              _ptr(out["nucleus_margin"]), _ptr(out["flags"]), B, K_max, V, dt, int(nthreads))
+    cut_in = None if row_cut is None else np.ascontiguousarray(row_cut, np.float64).reshape(B, 2 * K_max + 1)
+    rc = lib.oracle_verify_cuts(_ptr(p), _ptr(q), _ptr(draft), _ptr(kpr), _ptr(ua), _ptr(ur),
+                                float(temperature), float(tq), int(top_k), float(top_p),
+                                _ptr(out["tokens"]), _ptr(out["n_acc"]),
+                                _ptr(out["p_draft"]), _ptr(out["q_draft"]), _ptr(out["accept_margin"]),
+                                _ptr(out["sample_margin"]), _ptr(out["residual_mass"]), _ptr(out["row_lognorm"]),
+                                _ptr(out["nucleus_margin"]), _ptr(cut_in), _ptr(out["row_cut"]),
+                                _ptr(out["flags"]), B, K_max, V, dt, int(nthreads))
     if rc != 0:
         raise ValueError("oracle_verify rejected its arguments")
     return out

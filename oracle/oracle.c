@@ -92,10 +92,14 @@ static int cmp_zv_desc(const void* a, const void* b) {
  *       threshold t_p (-inf when off), [5] nucleus margin: the distance of top_p to the nearer of
  *       the two cumulative masses around the cut, the mass before the first group (exactly 0)
  *       left out (inf when off).
+ *   cut: NaN = find the nucleus as above.  Otherwise the nucleus cut is given instead of found
+ *       (the parity tests pass the cut the CUDA library chose, once they have checked that it is a
+ *       valid one): the row keeps, inside its top-k set, every logit >= cut and is renormalised,
+ *       which is the nucleus's last step with t_p = cut; info_out[4] = cut, info_out[5] = NaN.
  * Returns OR_FLAG_NONFINITE if the row holds NaN or +inf or keeps nothing finite,
  * OR_FLAG_TOPK_TIE if ties made the top-k set larger than k.
  */
-int oracle_row_dist_ex(const void* z, int dtype, int V, double T, int top_k, double top_p,
+int oracle_row_dist_at(const void* z, int dtype, int V, double T, int top_k, double top_p, double cut,
                        double* P_out, double* info_out) {
   int flags = 0;
   double t = -INFINITY;
@@ -146,7 +150,32 @@ int oracle_row_dist_ex(const void* z, int dtype, int V, double T, int top_k, dou
   for (int v = 0; v < V; ++v) P_out[v] /= sum;
   info[1] = m / T + log(sum);
 
-  if (top_p < 1.0) {
+  if (!isnan(cut)) {
+    /* a given cut: keep the logits >= cut inside the top-k set and renormalise */
+    double wsum = 0.0, mass = 0.0;
+    int nk = 0;
+    for (int v = 0; v < V; ++v) {
+      if (P_out[v] > 0.0 && logit_at(z, dtype, (size_t)v) >= cut) {
+        mass += P_out[v];
+        wsum += exp((logit_at(z, dtype, (size_t)v) - m) / T);
+        ++nk;
+      } else {
+        P_out[v] = 0.0;
+      }
+    }
+    if (!(mass > 0.0)) { /* the cut lies above every kept logit: nothing to sample from */
+      for (int v = 0; v < V; ++v) P_out[v] = NAN;
+      info[4] = cut;
+      info[5] = NAN;
+      if (info_out) memcpy(info_out, info, sizeof info);
+      return flags | OR_FLAG_NONFINITE;
+    }
+    for (int v = 0; v < V; ++v) P_out[v] = P_out[v] / mass;
+    info[1] = m / T + log(wsum);
+    info[3] = nk;
+    info[4] = cut;
+    info[5] = NAN;
+  } else if (top_p < 1.0) {
     /* Nucleus: walk the kept tokens from the most likely down (a library sort as the step),
        one group of equal logits at a time, until the mass taken reaches top_p; the group that
        reaches it is kept whole. */
@@ -194,6 +223,12 @@ int oracle_row_dist_ex(const void* z, int dtype, int V, double T, int top_k, dou
   }
   if (info_out) memcpy(info_out, info, sizeof info);
   return flags;
+}
+
+/* The row's distribution with its nucleus found (oracle_row_dist_at with a NaN cut). */
+int oracle_row_dist_ex(const void* z, int dtype, int V, double T, int top_k, double top_p,
+                       double* P_out, double* info_out) {
+  return oracle_row_dist_at(z, dtype, V, T, top_k, top_p, NAN, P_out, info_out);
 }
 
 /* The same without top-p; info_out (nullable) gets the first four entries. */
@@ -335,14 +370,19 @@ static int32_t argmax_row(const void* z, int dtype, int V, int* flags) {
  * draft rows, > 0 unless greedy, where it is not used), top_k, top_p (in (0, 1]; 1 = off).
  * row_nucleus_margin (nullable) [B, 2*K_max+1]: each row's nucleus margin (inf when top-p is off,
  * NaN where unused).
+ * row_cut_out (nullable) [B, 2*K_max+1]: each row's smallest kept logit bound, the larger of the
+ * top-k threshold and the nucleus cut (-inf when neither is on; NaN where unused and in greedy mode).
+ * row_cut_in (nullable) [B, 2*K_max+1]: per row, NaN = find the nucleus; a value = take it as the
+ * nucleus cut (oracle_row_dist_at).  oracle_verify_ex is this call with both NULL.
  * A request whose rows are non-finite gets n_acc = 0 and tokens -1 (its result is unspecified).
  * nthreads > 1 runs requests in parallel (OpenMP); the result does not depend on it.
  */
-int oracle_verify_ex(const void* p, const void* q, const int32_t* draft, const int32_t* k_per_row,
+int oracle_verify_cuts(const void* p, const void* q, const int32_t* draft, const int32_t* k_per_row,
                      const float* ua, const float* ur, float temperature, float draft_temperature,
                      int top_k, float top_p, int32_t* out_tokens, int32_t* out_n_acc, double* p_draft,
                      double* q_draft, double* accept_margin, double* sample_margin,
                      double* residual_mass, double* row_lognorm, double* row_nucleus_margin,
+                       const double* row_cut_in, double* row_cut_out,
                      int32_t* out_flags, int B, int K_max, int V, int dtype, int nthreads) {
   if (B < 0 || K_max < 0 || K_max > 64 || V <= 0 || !(temperature >= 0.0f) || top_k < 0) return 1;
   if (temperature > 0.0f && !(draft_temperature > 0.0f)) return 1;
@@ -372,9 +412,13 @@ int oracle_verify_ex(const void* p, const void* q, const int32_t* draft, const i
     for (int j = 0; j <= K_max; ++j) tok[j] = -1;
     for (int j = 0; j < K_max; ++j) pd[j] = qd[j] = am[j] = NAN;
     double* nm = row_nucleus_margin ? row_nucleus_margin + (size_t)b * rows_lognorm : NULL;
+    double* co = row_cut_out ? row_cut_out + (size_t)b * rows_lognorm : NULL;
+    const double* ci = row_cut_in ? row_cut_in + (size_t)b * rows_lognorm : NULL;
     for (int r = 0; r < rows_lognorm; ++r) ln[r] = NAN;
     if (nm)
       for (int r = 0; r < rows_lognorm; ++r) nm[r] = NAN;
+    if (co)
+      for (int r = 0; r < rows_lognorm; ++r) co[r] = NAN;
     sample_margin[b] = NAN;
     residual_mass[b] = NAN;
 
@@ -416,14 +460,18 @@ int oracle_verify_ex(const void* p, const void* q, const int32_t* draft, const i
     double* work = (double*)malloc(sizeof(double) * (size_t)V);
     double info[6];
     for (int j = 0; j <= K; ++j) {
-      flags |= oracle_row_dist_ex(pb + (size_t)j * V * es, dtype, V, T, top_k, tp, Pr + (size_t)j * V, info);
+      const double cp = ci ? ci[j] : NAN;
+      flags |= oracle_row_dist_at(pb + (size_t)j * V * es, dtype, V, T, top_k, tp, cp, Pr + (size_t)j * V, info);
       ln[j] = info[1];
       if (nm) nm[j] = info[5];
+      if (co) co[j] = info[4] > info[2] ? info[4] : info[2];
     }
     for (int j = 0; j < K; ++j) {
-      flags |= oracle_row_dist_ex(qb + (size_t)j * V * es, dtype, V, Tq, top_k, tp, Qr + (size_t)j * V, info);
+      const double cq = ci ? ci[K_max + 1 + j] : NAN;
+      flags |= oracle_row_dist_at(qb + (size_t)j * V * es, dtype, V, Tq, top_k, tp, cq, Qr + (size_t)j * V, info);
       ln[K_max + 1 + j] = info[1];
       if (nm) nm[K_max + 1 + j] = info[5];
+      if (co) co[K_max + 1 + j] = info[4] > info[2] ? info[4] : info[2];
     }
     int32_t n = 0;
     if (flags & OR_FLAG_NONFINITE) {
@@ -439,6 +487,19 @@ int oracle_verify_ex(const void* p, const void* q, const int32_t* draft, const i
     free(work);
   }
   return 0;
+}
+
+/* The whole verify step with every nucleus found by the oracle itself. */
+int oracle_verify_ex(const void* p, const void* q, const int32_t* draft, const int32_t* k_per_row,
+                     const float* ua, const float* ur, float temperature, float draft_temperature,
+                     int top_k, float top_p, int32_t* out_tokens, int32_t* out_n_acc, double* p_draft,
+                     double* q_draft, double* accept_margin, double* sample_margin,
+                     double* residual_mass, double* row_lognorm, double* row_nucleus_margin,
+                     int32_t* out_flags, int B, int K_max, int V, int dtype, int nthreads) {
+  return oracle_verify_cuts(p, q, draft, k_per_row, ua, ur, temperature, draft_temperature, top_k, top_p,
+                            out_tokens, out_n_acc, p_draft, q_draft, accept_margin, sample_margin,
+                            residual_mass, row_lognorm, row_nucleus_margin, NULL, NULL, out_flags, B, K_max,
+                            V, dtype, nthreads);
 }
 
 /* The verify step with one temperature for both sides and no top-p. */

@@ -383,6 +383,71 @@ def test_bad_inputs_flagged():
 
 
 # ----------------------------------------------------------------------------------------------
+# the decision margins (a GPU result that differs from the oracle's is excused only where the
+# margin of the decision that differs is below 1e-5, so the margins themselves are pinned)
+# ----------------------------------------------------------------------------------------------
+# Every probability and uniform below is a binary fraction, so each margin is exact in fp64:
+#   accept margin = |u - p(x)/q(x)| (inf when q(x) = 0) at every examined position;
+#   sample margin = min(u - C_{y-1}/R, C_y/R - u), C the cumulative weights of the draw in token
+#   order and R their total.
+HALF = [0.5, 0.25, 0.125, 0.125]
+MARGIN_CASES = [
+    # (P rows, Q rows, drafts, accept uniforms, resample uniform, expected result)
+    # accepted (1/4 / 1/2 = 1/2 against u = 3/8), then the bonus draw from the uniform row at
+    # u = 0.3: token 1, between the cumulative masses 1/4 and 1/2
+    dict(P=[HALF, [0.25] * 4], Q=[[0.25, 0.5, 0.125, 0.125]], x=[1], ua=[0.375], ur=0.3,
+         n_acc=1, tokens=[1, 1], accept_margin=[0.125], sample_margin=0.05, residual_mass=0.0),
+    # rejected (1/8 / 1/2 = 1/4 against u = 5/8); residual (3/8, 1/8, 0, 0), R = 1/2, cumulative
+    # C/R = (3/4, 1, 1, 1); u = 0.8 draws token 1, 0.05 above its lower edge
+    dict(P=[HALF, [0.25] * 4], Q=[[0.125, 0.125, 0.5, 0.25]], x=[2], ua=[0.625], ur=0.8,
+         n_acc=0, tokens=[1, -1], accept_margin=[0.375], sample_margin=0.05, residual_mass=0.5),
+    # the same draw at u = 31/32: token 1, 1/32 below its upper edge
+    dict(P=[HALF, [0.25] * 4], Q=[[0.125, 0.125, 0.5, 0.25]], x=[2], ua=[0.625], ur=31 / 32,
+         n_acc=0, tokens=[1, -1], accept_margin=[0.375], sample_margin=1 / 32, residual_mass=0.5),
+    # the same draw at u = 1/2: token 0, 1/4 below its upper edge (its lower edge is 0, 1/2 away)
+    dict(P=[HALF, [0.25] * 4], Q=[[0.125, 0.125, 0.5, 0.25]], x=[2], ua=[0.625], ur=0.5,
+         n_acc=0, tokens=[0, -1], accept_margin=[0.375], sample_margin=0.25, residual_mass=0.5),
+    # two positions: the first accepted with q(x) = 0 (margin inf, accepted because p(x) > 0), the
+    # second rejected (1/8 / 1/4 = 1/2 against u = 3/4, margin 1/4); the residual at position 1 is
+    # (0, 0, 0, 1/8), so u = 1/4 draws token 3, 1/4 above its lower edge C_2 / R = 0
+    dict(P=[[0.5, 0.5, 0, 0], [0.5, 0.25, 0.125, 0.125], [0.25] * 4], Q=[[1.0, 0, 0, 0], [0.5, 0.25, 0.25, 0]],
+         x=[1, 2], ua=[0.875, 0.75], ur=0.25, n_acc=1, tokens=[1, 3, -1], accept_margin=[np.inf, 0.25],
+         sample_margin=0.25, residual_mass=0.125),
+]
+
+
+def _margin_pin(lib=None):
+    for c in MARGIN_CASES:
+        r = oracle.decide(np.array(c["P"], float), np.array(c["Q"], float), c["x"], c["ua"], c["ur"], lib=lib)
+        assert r["n_acc"] == c["n_acc"], (c, r)
+        np.testing.assert_array_equal(r["tokens"], c["tokens"])
+        np.testing.assert_array_equal(r["accept_margin"][: c["n_acc"] + 1], c["accept_margin"])
+        assert abs(r["sample_margin"] - c["sample_margin"]) < 1e-15, (c, r)
+        assert abs(r["residual_mass"] - c["residual_mass"]) < 1e-15, (c, r)
+
+
+def test_margins_hand_computed():
+    _margin_pin()
+
+
+def test_margins_through_the_batch_entry():
+    """The same cases as logits (ln of the probabilities, -inf for zeros) through oracle.verify:
+    the margins come out as computed by hand, to the rounding of the float32 logits."""
+    for c in MARGIN_CASES:
+        K = len(c["x"])
+        with np.errstate(divide="ignore"):
+            p = np.log(np.array(c["P"], np.float64)).astype(np.float32)[None]
+            q = np.log(np.array(c["Q"], np.float64)).astype(np.float32)[None]
+        out = oracle.verify(p, q, np.array([c["x"]], np.int32), None, np.array([c["ua"]], np.float32),
+                            np.array([c["ur"]], np.float32), 1.0)
+        assert out["n_acc"][0] == c["n_acc"]
+        np.testing.assert_array_equal(out["tokens"][0], c["tokens"])
+        np.testing.assert_allclose(out["accept_margin"][0, : c["n_acc"] + 1], c["accept_margin"], rtol=0, atol=1e-6)
+        assert abs(out["sample_margin"][0] - c["sample_margin"]) < 1e-6
+        assert np.isnan(out["accept_margin"][0, c["n_acc"] + 1:]).all() and K >= c["n_acc"]
+
+
+# ----------------------------------------------------------------------------------------------
 # planted mistakes: every variant must fail at least one pin
 # ----------------------------------------------------------------------------------------------
 MUTANTS = {
@@ -395,6 +460,13 @@ MUTANTS = {
     "residual_sign": ("double d = Pj[v] - Qj[v];", "double d = Qj[v] - Pj[v];"),
     "cdf_from_top": ("for (int v = 0; v < V; ++v) {\n    double prev = C;",
                      "for (int v = V - 1; v >= 0; --v) {\n    double prev = C;"),
+    # the margins the parity tests rely on
+    "accept_margin_unnormalised": ("fabs(u - a / c)", "fabs(u * c - a)"),
+    "accept_margin_swapped": ("fabs(u - a / c)", "fabs(u - c / a)"),
+    "sample_margin_without_R": ("double lo = u - prev / R, hi = C / R - u;", "double lo = u - prev, hi = C - u;"),
+    "sample_margin_lower_edge_off_by_one": ("double lo = u - prev / R, hi = C / R - u;",
+                                            "double lo = u - (prev - (v > 0 ? r[v - 1] : 0.0)) / R, hi = C / R - u;"),
+    "sample_margin_far_edge": ("*margin = lo < hi ? lo : hi;", "*margin = lo < hi ? hi : lo;"),
 }
 
 
@@ -408,6 +480,7 @@ def _pins_fail(lib):
         checks.append(lambda P=P, Q=Q: check_lossless(P, Q, lib))
     checks.append(lambda: _softmax_pin(lib))
     checks.append(lambda: _topk_pin(lib))
+    checks.append(lambda: _margin_pin(lib))
     for c in checks:
         try:
             c()

@@ -154,7 +154,7 @@ MUTANTS = {
     "topp_walks_upwards": ("if (x->z != y->z) return (x->z < y->z) - (x->z > y->z);",
                            "if (x->z != y->z) return (x->z > y->z) - (x->z < y->z);"),
     "topp_stops_one_group_late": ("if (taken + g >= top_p) {", "if (taken >= top_p) {"),
-    "draft_temperature_ignored": ("dtype, V, Tq, top_k, tp, Qr", "dtype, V, T, top_k, tp, Qr"),
+    "draft_temperature_ignored": ("dtype, V, Tq, top_k, tp, cq, Qr", "dtype, V, T, top_k, tp, cq, Qr"),
 }
 
 
