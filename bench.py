@@ -12,6 +12,7 @@ workloads); the per-pass split is then unavailable and the roofline covers the w
 
 value     = verified draft positions per second over all ranks (sum_b K_b / step time)
 roofline  = logits bytes per launch / mean kernel time, against the measured HBM copy peak
+            (and against the nominal 8 TB/s); median_step_ms = median of per-step event times
 e2e       = the same metric through spec_verify_host (pinned host buffers, copies included)
 cpu_baseline = the fp64 oracle on the host cores, on a bounded sample of the same workload
 Multi-GPU (torchrun): every rank verifies its own batch of distinct requests (weak scaling, no
@@ -37,6 +38,7 @@ sys.path.insert(0, ROOT)
 import workloads as W  # noqa: E402
 
 METRIC = "verified draft positions/s and logits GB/s (fraction of GB300 HBM peak)"
+NOMINAL_HBM_GBS = 8000.0  # the nominal GB300 HBM3e bandwidth the fraction is also quoted against
 UNIT = "positions/s"
 KERNEL_SRC = os.path.join(ROOT, "speculative_decoding_rejection_verify_gb300", "csrc", "spec_verify.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
@@ -185,27 +187,40 @@ def launches_per_step(w: W.Workload) -> int:
     return n
 
 
-def cpu_baseline(w: W.Workload, budget_requests: int, seconds: float = 10.0):
-    """The oracle, as it stands, on the host cores over a bounded sample of the workload: the
-    first `budget_requests` requests, verified repeatedly until about `seconds` have passed."""
+def _time_oracle(w: W.Workload, d, nthreads: int, seconds: float):
+    """Repeated oracle calls on the sample `d` for about `seconds`: (positions/s, calls, seconds)."""
     import oracle
-    n = min(budget_requests, w.B)
-    d = W.generate(w, requests=range(n))
-    cores = os.cpu_count() or 1
     kpr = d["k_per_row"] if w.ragged else None
     calls = 0
     t0 = time.perf_counter()
     while True:
         oracle.verify(d["p"], None if w.temperature == 0 else d["q"], d["draft"], kpr, d["ua"], d["ur"],
-                      w.temperature, w.top_k, nthreads=cores, draft_temperature=w.tq, top_p=w.top_p)
+                      w.temperature, w.top_k, nthreads=nthreads, draft_temperature=w.tq, top_p=w.top_p)
         calls += 1
         dt = time.perf_counter() - t0
         if dt >= seconds:
             break
-    pos = int(d["k_per_row"].sum()) * calls
-    return {"value": pos / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+    return int(d["k_per_row"].sum()) * calls / dt, calls, dt
+
+
+def cpu_baseline(w: W.Workload, budget_requests: int, seconds: float = 10.0, single_requests: int = 16,
+                 single_seconds: float = 5.0):
+    """The oracle, as it stands, on the host cores over a bounded sample of the workload: the
+    first `budget_requests` requests with OpenMP over requests on every core, verified repeatedly
+    until about `seconds` have passed; then the first `single_requests` requests on one thread."""
+    n = min(budget_requests, w.B)
+    d = W.generate(w, requests=range(n))
+    cores = os.cpu_count() or 1
+    v, calls, dt = _time_oracle(w, d, cores, seconds)
+    n1 = min(single_requests, n)
+    d1 = {k: (a[:n1] if isinstance(a, np.ndarray) and a.ndim >= 1 and a.shape[0] == n else a) for k, a in d.items()}
+    v1, calls1, dt1 = _time_oracle(w, d1, 1, single_seconds)
+    return {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"first {n} of the {w.B} requests, {calls} oracle calls, OpenMP over requests "
-                      f"({dt:.1f} s)"}, pos, dt
+                      f"({dt:.1f} s)",
+            "single_thread": {"value": v1, "unit": UNIT, "cores": 1,
+                              "sample": f"first {n1} of the {w.B} requests, {calls1} oracle calls on one "
+                                        f"thread ({dt1:.1f} s)"}}, None, dt
 
 
 # ------------------------------------------------------------------------------------------------
@@ -352,8 +367,15 @@ def run_gpu(args, w: W.Workload):
         t_end.record(stream)
         torch.cuda.synchronize()
         barrier(world)
-        # the pass split, on separate steps: an event between the passes serialises them fully
+        # per-step times (events around each step, nothing between its kernels)
         nsplit = min(args.steps, 200)
+        for i in range(nsplit):
+            ev[i][0].record(stream)
+            step(i)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        per_step = [a.elapsed_time(z) for a, _, z in ev[:nsplit]]
+        # the pass split, on separate steps: an event between the passes serialises them fully
         for i in range(nsplit):
             ev[i][0].record(stream)
             step(i, None if (graphs or sampling) else ev[i][1])
@@ -417,8 +439,12 @@ def run_gpu(args, w: W.Workload):
                    "l2": l2_note, "launch": "CUDA graph replay" if graphs else "direct launches",
                    "parallelism": f"{world} independent batches (no collective)"},
         "logits_gbs": logits_bytes / (step_ms * 1e-3) / 1e9,
+        "median_step_ms": statistics.median(per_step), "step_ms_p10_p90": [float(np.percentile(per_step, 10)),
+                                                                        float(np.percentile(per_step, 90))],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "frac_vs_nominal": achieved / NOMINAL_HBM_GBS,
+                     "step_frac_vs_nominal": logits_bytes / (step_ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS,
                      "traffic": traffic_for(w.label),
                      "kernel": ("stats_kernel (streaming pass)" if graphs is None and not sampling else
                                 "whole step" + (" (graph replay)" if graphs else "")),

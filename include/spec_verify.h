@@ -76,7 +76,11 @@ typedef enum {
  *   flags [B] int32: SPEC_FLAG_* bits;
  *   pass1_done: a cudaEvent_t (host handle, cast to void*) recorded on the stream between the
  *       streaming pass and the per-request pass, so a caller can time the two passes apart; NULL
- *       = not recorded.  It is the one field that is not device memory.
+ *       = not recorded.  It is the one field that is not device memory;
+ *   row_cut [B * (2*K_max + 1)] float: per row (same order as row_lognorm), the smallest logit the
+ *       row keeps: the top-k threshold (the k-th largest logit) or the nucleus cut (the logit of the
+ *       last tie group kept), whichever is larger; -inf when neither truncation is on; NaN for rows
+ *       past K_b and in greedy mode.  The kept set of a row is {v : z_v >= row_cut}.
  */
 typedef struct {
   float* p_draft;
@@ -87,6 +91,7 @@ typedef struct {
   float* row_lognorm;
   int32_t* flags;
   void* pass1_done;
+  float* row_cut;
 } spec_verify_stats_t;
 
 /*
@@ -239,8 +244,11 @@ void spec_verify_set_test_hooks(int32_t hooks);
  *     loading this library keeps until the process exits; it needs no initialisation.
  *   - The first call on a device (the current device) looks up the array's device address with
  *     cudaGetSymbolAddress and caches it; make that first call before any stream capture.
- *   - Sizes whose workspace (spec_verify_workspace_bytes) exceeds the array are rejected with
- *     SPEC_ERR_WORKSPACE: B=1024, K_max=4, V=128256 without top-k fits; large top-k batches do not.
+ *   - Arguments are checked as spec_verify checks them, with the same status codes; then a call
+ *     whose own workspace (for its mode -- sampling, top-k or greedy -- and its row layout) exceeds
+ *     the array is rejected with SPEC_ERR_WORKSPACE before anything is launched.  For example
+ *     B=1024, K_max=4, V=128256 fits in bf16 (about 9.5 MB) and in greedy fp32 (about 10.5 MB), but
+ *     not in sampled fp32 (about 19 MB); large top-k batches do not fit.
  *   - Every call on a device shares the one array: calls that may overlap on the GPU (other
  *     streams, other host threads) race and corrupt each other; serialise them.
  *   - Allocates nothing; all other arguments and results are as for spec_verify.

@@ -62,7 +62,7 @@ class SpecVerifyError(RuntimeError):
 class StatsStruct(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("p_draft", "q_draft", "accept_margin", "sample_margin", "residual_mass", "row_lognorm", "flags",
-                 "pass1_done")]
+                 "pass1_done", "row_cut")]
 
 
 class SamplingStruct(ctypes.Structure):
@@ -257,7 +257,8 @@ def verify(p, q, draft, k_per_row=None, u_accept=None, u_resample=None, temperat
         sd = dict(p_draft=torch.empty((B, K), **f32), q_draft=torch.empty((B, K), **f32),
                   accept_margin=torch.empty((B, K), **f32), sample_margin=torch.empty((B,), **f32),
                   residual_mass=torch.empty((B,), **f32), row_lognorm=torch.empty((B, 2 * K + 1), **f32),
-                  flags=torch.empty((B,), dtype=torch.int32, device=dev))
+                  flags=torch.empty((B,), dtype=torch.int32, device=dev),
+                  row_cut=torch.empty((B, 2 * K + 1), **f32))
         sp = StatsStruct(**{k: v.data_ptr() for k, v in sd.items()})
     if pass1_event is not None:
         if pass1_event.cuda_event == 0:  # torch creates the event on its first record

@@ -1,4 +1,5 @@
-// spec_verify.cu — the verify step of speculative sampling as one fused sm_103a kernel.
+// spec_verify.cu — the verify step of speculative sampling as hand-written sm_103a kernels (a streaming
+// pass over every logit row, then a per-request pass; a nucleus pass between them for top-p).
 //
 // What is computed (host + section of the page that defines it):
 //   cf-1.com/news/5155685 §2.2, 2kiu.com/news/5895634 §2.2  accept x ~ q with probability
@@ -82,6 +83,7 @@ struct Params {
   float* samp_margin;
   float* resid_mass;
   float* lognorm;
+  float* rowcut;                  // per row: the smallest kept logit (top-k threshold / nucleus cut)
   float* sample_prob;             // draft-token sampling (K = 0): q(x) of each row's drawn token, or null
   int test_hooks;                 // spec_verify_set_test_hooks: 0 in normal operation
   int32_t* flags;
@@ -2305,17 +2307,21 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
     P.out_nacc[b] = sm.jstar;
     if (P.flags) P.flags[b] = sm.flags;
   }
-  if (P.lognorm) {
+  if (P.lognorm || P.rowcut) {
     const int R = 2 * K + 1;
     for (int r = t; r < R; r += kThreads) {
-      float v = NAN;
+      float v = NAN, cut = NAN;
       if (MODE != kGreedy) {
         int rr = -1;  // compact row index of padded row r
         if (r <= K) rr = r <= Kb ? r : -1;
         else rr = (r - K - 1) < Kb ? Kb + 1 + (r - K - 1) : -1;
-        if (rr >= 0) v = sm.rowM[rr] * (rr > Kb ? P.invTq : P.invT) + logf(sm.rowS[rr]);
+        if (rr >= 0) {
+          v = sm.rowM[rr] * (rr > Kb ? P.invTq : P.invT) + logf(sm.rowS[rr]);
+          cut = sm.rowT[rr];
+        }
       }
-      P.lognorm[(size_t)b * R + r] = v;
+      if (P.lognorm) P.lognorm[(size_t)b * R + r] = v;
+      if (P.rowcut) P.rowcut[(size_t)b * R + r] = cut;
     }
   }
   if (P.sample_prob && t == 0) {
@@ -2964,13 +2970,14 @@ namespace sv {
 std::atomic<int32_t> g_test_hooks{0};  // spec_verify_set_test_hooks
 }  // namespace sv
 
-// spec_verify_ex with, for the sampler, q(x) of each request's drawn token written to sample_prob.
-static spec_status_t verify_impl(const void* p_logits, const void* q_logits, const int32_t* draft_tokens,
-                                 const int32_t* k_per_row, const float* u_accept, const float* u_resample,
-                                 const spec_sampling_t* sampling, int32_t* out_tokens, int32_t* out_num_accepted,
-                                 const spec_verify_stats_t* out_stats, int32_t B, int32_t K_max, int32_t V,
-                                 spec_dtype_t dtype, void* workspace, size_t workspace_bytes, void* stream,
-                                 float* sample_prob) {
+// The host-side checks of a verify call, in order, and the workspace layout of the call's own mode
+// (sampling, top-k or greedy) and row layout.  SPEC_OK with *empty set for B == 0 (nothing to do).
+static spec_status_t check_call(const void* p_logits, const void* q_logits, const int32_t* draft_tokens,
+                                const int32_t* k_per_row, const float* u_accept, const float* u_resample,
+                                const spec_sampling_t* sampling, const int32_t* out_tokens,
+                                const int32_t* out_num_accepted, int32_t B, int32_t K_max, int32_t V,
+                                spec_dtype_t dtype, int* mode_out, Layout* L, bool* empty) {
+  *empty = false;
   if (B < 0 || K_max < 0 || V <= 0 || !sampling) return SPEC_ERR_INVALID_ARG;
   const float temperature = sampling->temperature, tq = sampling->draft_temperature;
   const int32_t top_k = sampling->top_k;
@@ -2982,15 +2989,38 @@ static spec_status_t verify_impl(const void* p_logits, const void* q_logits, con
   if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED;
   const int mode = mode_of(temperature, top_k, V);
   if (mode == kTopK && top_k > SPEC_MAX_TOPK) return SPEC_ERR_UNSUPPORTED;
-  if (B == 0) return SPEC_OK;  // nothing to read or write (empty arrays may have null pointers)
+  *mode_out = mode;
+  if (B == 0) {  // nothing to read or write (empty arrays may have null pointers)
+    *empty = true;
+    return SPEC_OK;
+  }
   if (!p_logits || !out_tokens || !out_num_accepted) return SPEC_ERR_INVALID_ARG;
   if (K_max > 0 && !draft_tokens) return SPEC_ERR_INVALID_ARG;
   if (mode != kGreedy && (!u_resample || (K_max > 0 && (!q_logits || !u_accept))))
     return SPEC_ERR_INVALID_ARG;
-  const bool ragged = k_per_row != nullptr;
+  if (!make_layout(B, K_max, V, dtype == SPEC_DTYPE_BF16 ? 2 : 4, mode, k_per_row != nullptr, L))
+    return SPEC_ERR_UNSUPPORTED;
+  return SPEC_OK;
+}
+
+// spec_verify_ex with, for the sampler, q(x) of each request's drawn token written to sample_prob.
+static spec_status_t verify_impl(const void* p_logits, const void* q_logits, const int32_t* draft_tokens,
+                                 const int32_t* k_per_row, const float* u_accept, const float* u_resample,
+                                 const spec_sampling_t* sampling, int32_t* out_tokens, int32_t* out_num_accepted,
+                                 const spec_verify_stats_t* out_stats, int32_t B, int32_t K_max, int32_t V,
+                                 spec_dtype_t dtype, void* workspace, size_t workspace_bytes, void* stream,
+                                 float* sample_prob) {
+  int mode = kSample;
   Layout L;
-  if (!make_layout(B, K_max, V, dtype == SPEC_DTYPE_BF16 ? 2 : 4, mode, ragged, &L)) return SPEC_ERR_UNSUPPORTED;
+  bool empty = false;
+  const spec_status_t chk = check_call(p_logits, q_logits, draft_tokens, k_per_row, u_accept, u_resample, sampling,
+                                       out_tokens, out_num_accepted, B, K_max, V, dtype, &mode, &L, &empty);
+  if (chk != SPEC_OK || empty) return chk;
   if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
+  const float temperature = sampling->temperature, tq = sampling->draft_temperature;
+  const int32_t top_k = sampling->top_k;
+  const float top_p = sampling->top_p;
+  const bool ragged = k_per_row != nullptr;
 
   const size_t es = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
   const bool vec = ((uintptr_t)p_logits % 16 == 0) && (!q_logits || (uintptr_t)q_logits % 16 == 0) &&
@@ -3013,6 +3043,7 @@ static spec_status_t verify_impl(const void* p_logits, const void* q_logits, con
   P.samp_margin = st.sample_margin;
   P.resid_mass = st.residual_mass;
   P.lognorm = st.row_lognorm;
+  P.rowcut = st.row_cut;
   P.sample_prob = sample_prob;
   P.test_hooks = sv::g_test_hooks.load(std::memory_order_relaxed);
   P.flags = st.flags;
@@ -3224,9 +3255,16 @@ extern "C" spec_status_t spec_verify_static(const void* p_logits, const void* q_
                                             const spec_verify_stats_t* out_stats, int32_t B,
                                             int32_t K_max, int32_t V, spec_dtype_t dtype,
                                             void* stream) {
-  const size_t need = spec_verify_workspace_bytes(B < 0 ? 0 : B, K_max, V, dtype, top_k);
-  if (B < 0 || need == 0) return SPEC_ERR_INVALID_ARG;
-  if (need > sv::kStaticScratchBytes) return SPEC_ERR_WORKSPACE;  // beyond the fixed array
+  // the same host-side checks as spec_verify, in the same order, then the workspace of this call's
+  // own mode and row layout against the fixed array
+  const spec_sampling_t sp = {temperature, temperature, top_k, 1.0f};
+  int mode = 0;
+  sv::Layout L;
+  bool empty = false;
+  const spec_status_t chk = check_call(p_logits, q_logits, draft_tokens, k_per_row, u_accept, u_resample, &sp,
+                                       out_tokens, out_num_accepted, B, K_max, V, dtype, &mode, &L, &empty);
+  if (chk != SPEC_OK || empty) return chk;
+  if (L.bytes > sv::kStaticScratchBytes) return SPEC_ERR_WORKSPACE;  // beyond the fixed array
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= sv::kMaxDevices) return SPEC_ERR_CUDA;
   void* scratch = sv::g_scratch_addr[dev].load(std::memory_order_acquire);

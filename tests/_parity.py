@@ -9,8 +9,14 @@ Acceptance criteria (the tolerances the verify step is held to):
   (= 1e-5 relative on every probability of the row); the residual mass within 1e-5;
 * the data flags (bad token, bad k, non-finite, top-k tie) identical; the rounding flags
   (zero residual, CDF clamp) are free to differ;
-* with top-p, a request any of whose rows has its nucleus cut within 1e-5 of top_p (the
-  oracle's nucleus margin) is counted as low-margin and only its output form is checked.
+* each row's cut (the smallest kept logit, row_cut) identical: the top-k threshold is an exact
+  order statistic;
+* with top-p, the nucleus cut compares a float32 cumulative sum with top_p, so where the row's
+  mass reaches top_p within rounding either neighbouring cut is right.  Every GPU cut that
+  differs from the oracle's is first checked to be a correct one up to 1e-5 of mass (it is a
+  logit of the row inside its top-k set; the mass strictly above it is below top_p + 1e-5 and
+  the mass at or above it reaches top_p - 1e-5), and then the oracle is run again with the
+  GPU's cuts and every request is compared element by element as above.
 """
 from __future__ import annotations
 
@@ -52,7 +58,7 @@ def run_gpu(d, dev="cuda:0", stats=True, k_per_row="auto", **kw):
     return out
 
 
-def run_oracle(d, nthreads=0, k_per_row="auto"):
+def run_oracle(d, nthreads=0, k_per_row="auto", row_cut=None):
     import os
     import oracle
     w = d.get("workload")
@@ -61,7 +67,58 @@ def run_oracle(d, nthreads=0, k_per_row="auto"):
         k_per_row = kpr if (w is None or w.ragged is not None) else None
     return oracle.verify(d["p"], d["q"], d["draft"], k_per_row, d["ua"], d["ur"], d["temperature"],
                          d["top_k"], nthreads=nthreads or (os.cpu_count() or 1),
-                         draft_temperature=d.get("draft_temperature"), top_p=d.get("top_p", 1.0))
+                         draft_temperature=d.get("draft_temperature"), top_p=d.get("top_p", 1.0),
+                         row_cut=row_cut)
+
+
+def nucleus_cuts(d, g, o, kb=None, tol=MARGIN):
+    """Checks that every valid row's nucleus cut on the GPU (g["row_cut"]) is a correct one up to
+    rounding where it differs from the oracle's (o["row_cut"]), and returns the GPU's cuts for an
+    oracle run that takes them (NaN where the oracle has none).  Returns (cuts, rows that differ)."""
+    import oracle
+    top_p = float(np.float32(d.get("top_p", 1.0)))
+    gc, oc = g["row_cut"].astype(np.float64), o["row_cut"]
+    B = gc.shape[0]
+    Kmax = (gc.shape[1] - 1) // 2
+    kb = d["k_per_row"] if kb is None else np.asarray(kb)
+    T, Tq = d["temperature"], d.get("draft_temperature") or d["temperature"]
+    differ = 0
+    for b in range(B):
+        if o["flags"][b] & 16:
+            continue
+        k = int(kb[b])
+        rows = [(d["p"][b, j], T, j) for j in range(k + 1)] + [(d["q"][b, j], Tq, Kmax + 1 + j) for j in range(k)]
+        for z, Tr, r in rows:
+            if gc[b, r] == oc[b, r]:
+                continue
+            differ += 1
+            c = gc[b, r]
+            P, info, _ = oracle.row_dist(z, float(np.float32(Tr)), d["top_k"], 1.0)
+            zf = z.astype(np.float64) if z.dtype == np.float32 else \
+                (z.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            assert (zf == c).any() and c >= info["threshold"], f"b={b} row {r}: cut {c} is not a kept logit"
+            above, incl = P[zf > c].sum(), P[zf >= c].sum()
+            assert above < top_p + tol and incl >= top_p - tol, \
+                f"b={b} row {r}: cut {c} keeps mass {incl} (above it {above}) for top_p {top_p}; oracle cut {oc[b, r]}"
+    return np.where(np.isnan(oc), np.nan, gc), differ
+
+
+def check(d, g, k_per_row="auto", check_stats=True):
+    """The oracle on the same inputs (with top-p: again with the GPU's nucleus cuts, once they
+    are checked to be correct) and the element-by-element comparison; returns the counts and
+    the oracle's result."""
+    o = run_oracle(d, k_per_row=k_per_row)
+    kb = d["k_per_row"]
+    if isinstance(k_per_row, np.ndarray):
+        kb = np.clip(k_per_row, 0, d["workload"].K)
+    differ = 0
+    if d.get("top_p", 1.0) < 1.0 and d["temperature"] > 0:
+        assert "row_cut" in g, "top-p parity needs the GPU's row cuts (stats=True)"
+        cuts, differ = nucleus_cuts(d, g, o, kb)
+        o = run_oracle(d, k_per_row=k_per_row, row_cut=cuts)
+    res = compare(g, o, d["workload"].K, kb, check_stats=check_stats)
+    res["cuts_differ"] = differ
+    return res, o
 
 
 def compare(g, o, K, kb=None, check_stats=True):
@@ -80,24 +137,12 @@ def compare(g, o, K, kb=None, check_stats=True):
         no, ng = int(o["n_acc"][b]), int(g["n_acc"][b])
         to, tg = o["tokens"][b], g["tokens"][b]
         assert 0 <= ng <= kb[b], f"b={b}: n_acc {ng} outside [0, {kb[b]}]"
-        nm = o.get("nucleus_margin")
-        Kmax = (len(o["row_lognorm"][b]) - 1) // 2
-        loose = np.zeros(2 * Kmax + 1, bool)  # rows whose top-p cut is within rounding of top_p
-        if nm is not None:
-            loose = nm[b] < MARGIN
-            used = np.zeros_like(loose)
-            used[: no + 1] = True                     # p rows 0..n_acc
-            used[Kmax + 1: Kmax + 1 + min(no + 1, int(kb[b]))] = True  # q rows 0..n_acc (< K_b)
-            if (loose & used).any():
-                # a row the decision used has its cut within rounding of top_p: either kept set
-                # is correct, so only the form of the result is checked
-                low_margin += 1
-                assert (tg[ng + 1:] == -1).all() and 0 <= tg[ng] < 1 << 30
-                continue
         if no == ng and (to == tg).all():
             exact += 1
         else:
             j = min(no, ng)
+            # the accepted prefix before the first decision that differs is the same draft tokens
+            assert (to[:j] == tg[:j]).all(), f"b={b}: accepted prefix gpu {tg[:j]} oracle {to[:j]}"
             if no != ng:
                 m = o["accept_margin"][b, j]
                 assert m < MARGIN, f"b={b}: accept decision at {j} differs with margin {m} (gpu {ng}, oracle {no})"
@@ -118,8 +163,10 @@ def compare(g, o, K, kb=None, check_stats=True):
         ln_o, ln_g = o["row_lognorm"][b], g["row_lognorm"][b]
         fin = np.isfinite(ln_o)
         assert (np.isfinite(ln_g) == fin).all(), f"b={b}: lognorm validity {ln_g} vs {ln_o}"
-        cmp = fin & ~loose
-        np.testing.assert_allclose(ln_g[cmp], ln_o[cmp], rtol=0, atol=RTOL, err_msg=f"b={b} lognorm")
+        np.testing.assert_allclose(ln_g[fin], ln_o[fin], rtol=0, atol=RTOL, err_msg=f"b={b} lognorm")
+        if "row_cut" in g and "row_cut" in o:
+            np.testing.assert_array_equal(g["row_cut"][b][fin], o["row_cut"][b][fin].astype(np.float32),
+                                          err_msg=f"b={b} row_cut")
         if no == ng:
             np.testing.assert_allclose(g["residual_mass"][b], o["residual_mass"][b], rtol=0, atol=RTOL)
     return dict(exact=exact, low_margin=low_margin, requests=B)

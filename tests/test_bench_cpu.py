@@ -42,3 +42,14 @@ def test_reference_arm_other_ranks_do_no_work():
 def test_fewer_than_three_warmup_steps_refused():
     r = _bench("--impl", "reference", "--steps", "1", "--warmup", "2")
     assert r.returncode != 0 and "warmup" in r.stderr
+
+
+def test_cpu_baseline_reports_all_cores_and_one_thread():
+    """The GPU arm's cpu_baseline: the oracle with OpenMP over requests on every core, and on one
+    thread over a smaller sample, each a positions/s figure with its sample stated."""
+    import bench
+    import workloads as W
+    cb, _, _ = bench.cpu_baseline(W.get("c2", V=2000), 4, seconds=0.2, single_requests=2, single_seconds=0.2)
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0 and cb["unit"] == "positions/s"
+    st = cb["single_thread"]
+    assert st["cores"] == 1 and st["value"] > 0 and "first 2 of the 8 requests" in st["sample"]

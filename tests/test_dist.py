@@ -38,7 +38,7 @@ def _rank(rank, world, port, out):
 
 def test_two_ranks_shard_and_reduce():
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:  # no fork of a process that runs threads
         out = m.dict()
         mp.spawn(_rank, args=(2, port, out), nprocs=2, join=True)
         res = dict(out)

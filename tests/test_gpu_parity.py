@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 
 import workloads as W
-from _parity import compare, run_gpu, run_oracle, to_dev
+from _parity import check, compare, run_gpu, run_oracle, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -20,9 +20,7 @@ torch = pytest.importorskip("torch")
 
 def _check(d, **kw):
     g = run_gpu(d, **kw)
-    o = run_oracle(d)
-    w = d["workload"]
-    res = compare(g, o, w.K, d["k_per_row"])
+    res, o = check(d, g)
     assert res["low_margin"] <= max(2, res["requests"] // 100), res
     return res, g, o
 
@@ -43,7 +41,7 @@ def test_workload_small(name, over):
 # ------------------------------------------------------------------------------------------------
 # full sizes (every request compared)
 # ------------------------------------------------------------------------------------------------
-@pytest.mark.parametrize("name", ["c3", "c4", "c5_a0.8", "c5_greedy"])
+@pytest.mark.parametrize("name", ["c3", "c4", "c5_a0.4", "c5_a0.8", "c5_a0.9", "c5_greedy"])
 def test_workload_full(name):
     d = W.generate(W.get(name))
     res, g, o = _check(d)
@@ -314,7 +312,5 @@ def test_maximum_k_with_topk_and_topp():
     d = W.generate(W.get("c4", B=3, K=sv.MAX_K, ragged=None, V=60000, top_k=sv.MAX_TOPK, tau=0.6))
     _check(d)
     d = W.generate(W.get("c5_topp0.9", B=3, K=sv.MAX_K, V=60000, tau=0.6))
-    g = run_gpu(d)
-    o = run_oracle(d)
-    res = compare(g, o, d["workload"].K, d["k_per_row"])
+    res, _, _ = _check(d)
     assert res["requests"] == 3

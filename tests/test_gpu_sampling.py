@@ -7,51 +7,22 @@ import numpy as np
 import pytest
 
 import workloads as W
-from _parity import compare, run_gpu, run_oracle, to_dev
+from _parity import check, run_gpu, to_dev
 
 pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
 
 
-def _nucleus_valid(d, g, o, tol=1e-5):
-    """Every valid row's kept mass, as the GPU's log-normaliser implies it, is a correct nucleus
-    up to rounding: it reaches top_p, and it passes the oracle's only where the oracle's cut
-    reached top_p by less than the tolerance.  Holds for low-margin rows too."""
-    import oracle
-    w = d["workload"]
-    top_p = float(np.float32(d["top_p"]))
-    if top_p >= 1.0:
-        return
-    K = w.K
-    for b in range(d["p"].shape[0]):
-        if o["flags"][b] & 16:
-            continue
-        kb = int(d["k_per_row"][b])
-        rows = [(d["p"][b, j], d["temperature"], j) for j in range(kb + 1)] + \
-               [(d["q"][b, j], d["draft_temperature"], K + 1 + j) for j in range(kb)]
-        for z, T, r in rows:
-            full = oracle.row_dist(z, T, d["top_k"], 1.0)[1]["lognorm"]
-            fg = np.exp(g["row_lognorm"][b, r] - full)
-            fo = np.exp(o["row_lognorm"][b, r] - full)
-            assert fg >= top_p - tol, (b, r, fg, top_p)
-            assert fg <= fo + tol or fo - top_p < tol, (b, r, fg, fo, top_p)
-
-
-def _check(d, min_exact=0.5, **kw):
-    """Element-by-element parity.  A top-p cut within 1e-5 of top_p on any row a request uses
-    makes it low-margin (either kept set is right; the nucleus of every row is still checked).
-    At least the fraction `min_exact` of the requests must be compared exactly.  (An fp32 row's
-    boundary token carries ~1e-4 of the mass, so about one row in ten has a cut within 1e-5 of
-    top_p, and a request uses up to 2 K + 1 rows.)"""
+def _check(d, **kw):
+    """Element-by-element parity (with top-p, against the oracle run with the GPU's nucleus cuts
+    once each cut that differs from the oracle's is checked to be a correct one up to 1e-5 of
+    mass); at most max(2, B/100) requests may differ, each on a decision whose margin is below
+    1e-5."""
     kw.setdefault("stats", True)
     g = run_gpu(d, **kw)
-    o = run_oracle(d)
-    w = d["workload"]
-    res = compare(g, o, w.K, d["k_per_row"])
-    _nucleus_valid(d, g, o)
-    if d.get("top_p", 1.0) < 0.99:
-        assert res["exact"] >= int(np.ceil(res["requests"] * min_exact)), res
+    res, o = check(d, g)
+    assert res["low_margin"] <= max(2, res["requests"] // 100), res
     return res, g, o
 
 
@@ -121,10 +92,9 @@ def test_greedy_ignores_sampling_parameters():
 def test_variant_full(name):
     """The full batch in the launch configuration the benchmark times; every request compared."""
     d = W.generate(W.get(name))
-    g = run_gpu(d, stats=True)
-    o = run_oracle(d)
-    res = compare(g, o, d["workload"].K, d["k_per_row"])
-    assert res["requests"] == 1024 and res["exact"] >= 512, res
+    res, _, _ = _check(d)
+    print(name, res)
+    assert res["requests"] == 1024, res
 
 
 def test_host_entry_with_sampling():
@@ -142,7 +112,7 @@ def test_host_entry_with_sampling():
 # ---------------------------------------------------------------------------------------------
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_topp_both_dtypes(dtype):
-    _check(W.generate(W.get("c5_topp0.9", B=12, dtype=dtype)), min_exact=0.25)
+    _check(W.generate(W.get("c5_topp0.9", B=12, dtype=dtype)))
 
 
 def test_topp_ragged_sampling_mode():
@@ -177,4 +147,4 @@ def test_topp_rows_off_the_common_path(dtype):
             if key == "q" and j >= w.K:
                 continue
             d[key][b, j] = W.to_bf16_bits(z) if dtype == "bf16" else z
-    _check(d, min_exact=0.25)
+    _check(d)
