@@ -17,8 +17,9 @@ NONFINITE = 16
 
 
 @pytest.mark.parametrize("name,over", [("c5_a0.8", dict(B=16)), ("c5_a0.8", dict(B=200)),
+                                       ("c5_a0.8", dict(B=300, V=40000, ragged=(0, 4))),
                                        ("c5_greedy", dict(B=16)), ("c5_topp0.9", dict(B=8))],
-                         ids=["cluster_tail", "block_tail", "greedy", "top_p"])
+                         ids=["cluster_tail", "block_tail", "block_tail_ragged", "greedy", "top_p"])
 def test_withheld_copy_flags_the_batch(name, over):
     import speculative_decoding_rejection_verify_gb300 as sv
     d = W.generate(W.get(name, **over))
@@ -36,9 +37,10 @@ def test_withheld_copy_flags_the_batch(name, over):
     assert res["exact"] + res["low_margin"] == res["requests"]
 
 
-def test_withheld_copy_in_the_sampler():
+@pytest.mark.parametrize("B", [32, 300])
+def test_withheld_copy_in_the_sampler(B):
     import speculative_decoding_rejection_verify_gb300 as sv
-    d = W.generate(W.get("sample_c5", B=32))
+    d = W.generate(W.get("sample_c5", B=B))
     logits = to_dev(d["p"][:, 0, :].copy(), "cuda:0")
     u = to_dev(d["ur"], "cuda:0")
     sv.set_test_hooks(1)

@@ -297,6 +297,38 @@ def test_cuda_graph_replay_matches_direct_calls(name, over):
         assert torch.equal(tok, ref_tok) and torch.equal(n, ref_n)
 
 
+# ------------------------------------------------------------------------------------------------
+# more requests than SMs (the one-block-per-request tail): just above the SM count, ragged with
+# bonus-only requests, one summary group per row block in fp32, and wide rows of 2^20 logits
+# ------------------------------------------------------------------------------------------------
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("over", [dict(B="sms+1"), dict(B=400, V=40000, ragged=(0, 4)),
+                                  dict(B=300, V=3000, dtype="f32"), dict(B="sms+8", K=2, V=1 << 20)],
+                         ids=["just_above_sms", "ragged_with_bonus_only", "small_rows_f32", "wide_rows"])
+def test_many_requests(over):
+    over = dict(over)
+    if isinstance(over["B"], str):
+        over["B"] = _sms() + int(over["B"].split("+")[1])
+    d = W.generate(W.get("c5_a0.8", **over))
+    if d["workload"].ragged:
+        d["k_per_row"][:7] = 0  # bonus-only requests among the others
+    res, _, _ = _check(d)
+    assert res["requests"] == over["B"]
+
+
+def test_pass_event_between_the_passes_matches():
+    """An event recorded between the passes (the benchmark's pass split) turns the dependent
+    launch into a plain one; the results are the same bit for bit."""
+    d = W.generate(W.get("c5_a0.8", B=300, V=40000))
+    a = run_gpu(d)
+    b = run_gpu(d, pass1_event=torch.cuda.Event(enable_timing=True))
+    for k in a:
+        np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_maximum_sizes(dtype):
     """K_max = 16 drafts over the largest supported vocabulary, 2^21 (SPEC_MAX_K, SPEC_MAX_V):
