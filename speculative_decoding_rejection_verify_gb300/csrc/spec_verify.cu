@@ -45,7 +45,7 @@ __host__ __device__ constexpr int stages_of(int mode) { return mode == 1 ? kStag
 constexpr int kTile = 256;               // inverse-CDF tile: 32 lanes x 8 logits
 constexpr int kCandCap = 256;            // top-k candidates stored per chunk
 constexpr int kSegCap = 1024;            // running top-k candidates of a row segment (per buffer)
-constexpr int kSegCompact = 640;         // compact the running set once it grows past this
+constexpr int kSegCompact = 320;         // compact the running set once it grows past this
 constexpr int kRowCap = 256;             // candidates >= the row's lower bound, per row
 constexpr int kMaxRows = 2 * SPEC_MAX_K + 1;
 constexpr int kUnrollA = 4;              // tiles in flight per warp in the CDF passes (scalar rows)
@@ -500,22 +500,22 @@ __device__ uint32_t chunk_bound(const float (&v)[Cfg<T>::PER], int n, int k, Sme
 }
 
 // Appends the chunk's logits >= theta (key 0: every logit) to the segment buffer.  Once theta is
-// tight almost no logit survives, so each thread first checks its own maximum and a warp only
-// walks its logits one by one when some lane may have a survivor.
+// tight almost no logit survives, so each thread first takes its own maximum (a tree of max.NaN;
+// logits past the row read -inf) and only a thread whose maximum reaches theta walks its logits
+// one by one, reserving its slots with one shared atomic.
 template <typename T, bool VEC>
 __device__ void seg_filter(const float (&v)[Cfg<T>::PER], int n, int v0, uint32_t theta, uint2* buf, Smem& sm) {
   const int t = threadIdx.x, lane = t & 31;
   const float tf = theta == 0u ? -INFINITY : keyf(theta);
   const bool full = n >= Cfg<T>::CH;  // no logit past the row in this chunk
-  float mx = -INFINITY;
-  if (full) {
+  float m[Cfg<T>::PER / 2];
 #pragma unroll
-    for (int i = 0; i < Cfg<T>::PER; ++i) mx = fmax_nan(mx, v[i]);
-  } else {
+  for (int i = 0; i < Cfg<T>::PER / 2; ++i) m[i] = fmax_nan(v[2 * i], v[2 * i + 1]);
 #pragma unroll
-    for (int i = 0; i < Cfg<T>::PER; ++i)
-      if (elem_of<T, VEC>(i, t) < n) mx = fmax_nan(mx, v[i]);
-  }
+  for (int w = Cfg<T>::PER / 4; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) m[i] = fmax_nan(m[i], m[i + w]);
+  const float mx = m[0];
   if (__any_sync(0xFFFFFFFFu, mx != mx) && lane == 0) atomicOr(&sm.seg_flags, (int)kMetaNaN);
   if (!(mx >= tf)) return;
   // a lane with survivors reserves its own slots (survivors are few once the bound is tight)
@@ -535,28 +535,51 @@ __device__ void seg_filter(const float (&v)[Cfg<T>::PER], int n, int v0, uint32_
   }
 }
 
-// The k-th largest key (counted with multiplicity) among src[0..n), n >= k, by radix selection on
-// 8-bit digits with a shared histogram.  Whole block.
-__device__ uint32_t seg_kth(const uint2* src, int n, int k, Smem& sm) {
+// A cut of the segment buffer src[0..n) (n >= k): a key c with at least k keys >= c, found by
+// histograms of the keys over 256 equal bins of a range [lo, hi]: the bin holding the k-th largest
+// key (counting from the top) is taken whole when it holds few keys, and is otherwise made the next
+// range (logits straddling 0 or spanning several binades put most keys in one bin of the full key
+// range; the bin at the next level is 2^8 times narrower).  The returned cut is that bin's lower
+// edge, so every key >= c is a candidate and k of them certify c as a lower bound on the row's
+// k-th largest.  Whole block.
+__device__ uint32_t seg_cut(const uint2* src, int n, int k, Smem& sm) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  uint32_t prefix = 0, mask = 0;
-  int kk = k;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    sm.hist[t] = 0;  // 256 threads, 256 bins
+  constexpr uint32_t kFewKeys = 48;  // a cut bin with at most this many keys is taken whole
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+  for (int i = t; i < n; i += kThreads) {
+    const uint32_t key = src[i].x;
+    lo = min(lo, key);
+    hi = max(hi, key);
+  }
+  lo = __reduce_min_sync(0xFFFFFFFFu, lo);
+  hi = __reduce_max_sync(0xFFFFFFFFu, hi);
+  if (lane == 0) {
+    sm.red_k[warp] = lo;
+    sm.red_c[warp] = (int)hi;
+  }
+  __syncthreads();
+  lo = 0xFFFFFFFFu;
+  hi = 0u;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    lo = min(lo, sm.red_k[w]);
+    hi = max(hi, (uint32_t)sm.red_c[w]);
+  }
+  int above = 0;  // keys above the current range
+  uint32_t cut = lo;
+  for (;;) {  // every thread holds the same lo, hi, above
+    const uint32_t span = hi - lo;
+    const int shift = span < 256u ? 0 : 32 - __clz(span) - 8;  // (hi - lo) >> shift < 256
+    sm.hist[t] = 0u;  // 256 threads, 256 bins
     __syncthreads();
-    for (int i0 = 0; i0 < n; i0 += kThreads) {  // keys of a row share their top digits: one
-      const int i = i0 + t;                          // atomic per distinct digit per warp
-      const uint32_t key = i < n ? src[i].x : 0u;
-      const bool in = i < n && (key & mask) == prefix;
-      const uint32_t dig = in ? (key >> shift) & 255u : 256u;
-      const unsigned peers = __match_any_sync(0xFFFFFFFFu, dig);
-      if (in && (__ffs(peers) - 1) == lane) atomicAdd(&sm.hist[dig], (unsigned)__popc(peers));
+    for (int i = t; i < n; i += kThreads) {
+      const uint32_t key = src[i].x;
+      if (key >= lo && key <= hi) atomicAdd(&sm.hist[(key - lo) >> shift], 1u);
     }
     __syncthreads();
     if (warp == 0) {
-      // lane l owns digits 255-8l .. 248-8l (descending); find the digit where the count of keys
-      // with a larger-or-equal digit first reaches kk
+      // lane l owns bins 255-8l .. 248-8l (descending); the bin where the count of keys in it and
+      // above first reaches k
       int c8[8], s = 0;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
@@ -569,29 +592,38 @@ __device__ uint32_t seg_kth(const uint2* src, int n, int k, Smem& sm) {
         const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
         if (lane >= o) incl += y;
       }
-      const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl >= kk);
-      const int hl = __ffs(hit) - 1;  // hit != 0: n >= kk keys match the prefix
+      const unsigned hit = __ballot_sync(0xFFFFFFFFu, above + incl >= k);
+      const int hl = __ffs(hit) - 1;  // hit != 0: n >= k keys in all, every one in [lo, hi] or above
       if (lane == hl) {
-        int acc = incl - s, q = 0;
-        while (q < 7 && acc + c8[q] < kk) acc += c8[q++];
-        sm.red_c[0] = 255 - 8 * lane - q;
-        sm.red_c[1] = kk - acc;
+        int acc = above + incl - s, q = 0;
+        while (q < 7 && acc + c8[q] < k) acc += c8[q++];
+        const uint32_t bin = (uint32_t)(255 - 8 * lane - q);
+        sm.red_k[0] = lo + (bin << shift);
+        sm.red_c[0] = acc;                       // keys above the bin
+        sm.red_c[1] = c8[q] <= (int)kFewKeys || shift == 0;  // take the bin whole
       }
     }
     __syncthreads();
-    prefix |= (uint32_t)sm.red_c[0] << shift;
-    mask |= 255u << shift;
-    kk = sm.red_c[1];
-    __syncthreads();
+    const uint32_t blo = sm.red_k[0];
+    const int acc = sm.red_c[0], whole = sm.red_c[1];
+    __syncthreads();  // red_k / red_c and the bins are reused
+    if (whole) {
+      cut = blo;
+      break;
+    }
+    above = acc;
+    const uint64_t bhi = (uint64_t)blo + ((1ull << shift) - 1ull);  // the bin's keys become the range
+    hi = bhi < (uint64_t)hi ? (uint32_t)bhi : hi;
+    lo = blo;
   }
-  return prefix;
+  return cut;
 }
 
-// Keeps the segment's entries >= its k-th largest (all of them when fewer than k) in the other
-// buffer; theta becomes that k-th largest.  With `sorted` the kept entries are placed by key
-// descending (buffer index ascending among equal keys).  Whole block.
+// Keeps the segment's entries >= a cut with at least k entries at or above it (all of them when
+// fewer than k) in the other buffer; theta becomes that cut.  With `sorted` the kept entries are
+// placed by key descending (buffer index ascending among equal keys).  Whole block.
 __device__ void seg_compact(int k, bool sorted, uint2* bufs, Smem& sm) {
-  const int t = threadIdx.x;
+  const int t = threadIdx.x, lane = t & 31;
   const int cur = sm.seg_cur;
   const uint2* src = bufs + (size_t)cur * kSegCap;
   uint2* dst = bufs + (size_t)(cur ^ 1) * kSegCap;
@@ -600,11 +632,18 @@ __device__ void seg_compact(int k, bool sorted, uint2* bufs, Smem& sm) {
     if (t == 0) sm.seg_flags |= (int)kMetaOverflow;
     n = kSegCap;
   }
-  const uint32_t kth = n >= k ? seg_kth(src, n, k, sm) : 0u;
+  const uint32_t kth = n >= k ? seg_cut(src, n, k, sm) : 0u;
   if (t == 0) sm.seg_kept = 0;
   __syncthreads();
-  for (int i = t; i < n; i += kThreads)  // keep the entries >= kth (unordered)
-    if (src[i].x >= kth) dst[atomicAdd(&sm.seg_kept, 1)] = src[i];
+  for (int i0 = 0; i0 < n; i0 += kThreads) {  // keep the entries >= kth (unordered), a slot range per warp
+    const int i = i0 + t;
+    const bool keep = i < n && src[i].x >= kth;
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, keep);
+    int base = 0;
+    if (lane == 0 && m) base = atomicAdd(&sm.seg_kept, __popc(m));
+    base = __shfl_sync(0xFFFFFFFFu, base, 0);
+    if (keep) dst[base + __popc(m & ((1u << lane) - 1u))] = src[i];
+  }
   if (sorted) {  // place the kept entries by key descending, then position, back in src
     __syncthreads();
     const int m = sm.seg_kept;
@@ -1065,24 +1104,21 @@ __device__ bool topk_row_fast(const Params& P, int b, int rp, uint2* buf, float&
   if (nan) flags |= SPEC_FLAG_NONFINITE;
   if (ovf) return false;
   const int k = P.top_k;
+  // Only the chunks where a block's row segment starts hold a list (sorted, key descending); the
+  // lists are read by the whole warp, 32 entries per load, one list at a time.
   // Lower bound L on the row's k-th largest: pool the m = ceil(k / nch) largest keys of every
-  // chunk (each list is sorted); the pool's k-th largest has >= k distinct logits at or above it.
+  // chunk's list; the pool's k-th largest has >= k distinct logits at or above it.
   const int m = (k + nch - 1) / nch;
   int np = 0;
   for (int c0 = 0; c0 < nch; c0 += 32) {
-    const int c = c0 + lane;
-    const int cnt = c < nch ? (int)(__ldcg(&meta[c].y) & kMetaCount) : 0;
-    const int take = min(m, cnt);
-    int off = take;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xFFFFFFFFu, off, o);
-      if (lane >= o) off += y;
+    const int cnt = c0 + lane < nch ? (int)(__ldcg(&meta[c0 + lane].y) & kMetaCount) : 0;
+    for (unsigned has = __ballot_sync(0xFFFFFFFFu, cnt > 0); has; has &= has - 1) {
+      const int l = __ffs(has) - 1;
+      const int take = min(m, __shfl_sync(0xFFFFFFFFu, cnt, l));
+      for (int i = lane; i < take; i += 32)
+        if (np + i < kRowCap) buf[np + i] = __ldcg(cand + (size_t)(c0 + l) * kCandCap + i);
+      np += take;
     }
-    const int base = np + off - take;
-    for (int i = 0; i < take; ++i)
-      if (base + i < kRowCap) buf[base + i] = __ldcg(cand + (size_t)c * kCandCap + i);
-    np += __shfl_sync(0xFFFFFFFFu, off, 31);
   }
   if (np > kRowCap) return false;
   __syncwarp();
@@ -1106,27 +1142,22 @@ __device__ bool topk_row_fast(const Params& P, int b, int rp, uint2* buf, float&
   // gather every candidate >= L: a prefix of each chunk's sorted list
   int n = 0;
   for (int c0 = 0; c0 < nch; c0 += 32) {
-    const int c = c0 + lane;
-    const int cnt = c < nch ? (int)(__ldcg(&meta[c].y) & kMetaCount) : 0;
-    const uint2* lst = cand + (size_t)(c < nch ? c : 0) * kCandCap;
-    int take = 0;
-    for (int i = 0; i < cnt; i += 2) {  // two entries per 16-byte load
-      const uint4 v = __ldcg(reinterpret_cast<const uint4*>(lst) + (i >> 1));
-      if (v.x < Lk) break;
-      take = i + 1;
-      if (i + 1 >= cnt || v.z < Lk) break;
-      take = i + 2;
+    const int cnt = c0 + lane < nch ? (int)(__ldcg(&meta[c0 + lane].y) & kMetaCount) : 0;
+    for (unsigned has = __ballot_sync(0xFFFFFFFFu, cnt > 0); has; has &= has - 1) {
+      const int l = __ffs(has) - 1;
+      const int cn = __shfl_sync(0xFFFFFFFFu, cnt, l);
+      const uint2* lst = cand + (size_t)(c0 + l) * kCandCap;
+      for (int i0 = 0; i0 < cn; i0 += 32) {
+        const int i = i0 + lane;
+        const uint2 e = i < cn ? __ldcg(lst + i) : make_uint2(0u, 0u);
+        const bool keep = i < cn && e.x >= Lk;
+        const unsigned mk = __ballot_sync(0xFFFFFFFFu, keep);
+        const int pos = n + __popc(mk & ((1u << lane) - 1u));
+        if (keep && pos < kRowCap) buf[pos] = e;
+        n += __popc(mk);
+        if (mk != 0xFFFFFFFFu) break;  // sorted: the rest lie below L (or past the list)
+      }
     }
-    int off = take;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xFFFFFFFFu, off, o);
-      if (lane >= o) off += y;
-    }
-    const int base = n + off - take;
-    for (int i = 0; i < take; ++i)
-      if (base + i < kRowCap) buf[base + i] = __ldcg(lst + i);
-    n += __shfl_sync(0xFFFFFFFFu, off, 31);
   }
   if (n > kRowCap) return false;
   __syncwarp();
@@ -1772,32 +1803,29 @@ __device__ bool draw_list(const Params& P, int b, int js, const T* qr, const Dra
   const uint2* meta = P.cmeta + ((size_t)b * P.R + js) * nch;
   const uint2* cand = P.cand + ((size_t)b * P.R + js) * nch * (size_t)kCandCap;
   const uint32_t kt = fkey(d.Tp);
-  // the length of a sorted list's prefix at or above the threshold, two entries per 16-byte load
-  auto prefix = [&](int c) {
+  // The prefix of chunk list c at or above the threshold (the lists are sorted, key descending),
+  // read by the whole warp, 32 entries per load; with `out`, copied there.  Warps take the chunks
+  // in turn; a block scan of the warps' totals places their copies.
+  auto take_list = [&](int c, uint2* out) {
     const int cnt = (int)(__ldcg(&meta[c].y) & kMetaCount);
-    const uint4* src = reinterpret_cast<const uint4*>(cand + (size_t)c * kCandCap);
-    int take = 0;
-    for (int i = 0; i < cnt; i += 2) {
-      const uint4 v = __ldcg(src + (i >> 1));
-      if (v.x < kt) break;
-      take = i + 1;
-      if (i + 1 >= cnt || v.z < kt) break;
-      take = i + 2;
+    const uint2* src = cand + (size_t)c * kCandCap;
+    int n = 0;
+    for (int i0 = 0; i0 < cnt; i0 += 32) {
+      const int i = i0 + lane;
+      const uint2 e = i < cnt ? __ldcg(src + i) : make_uint2(0u, 0u);
+      const bool keep = i < cnt && e.x >= kt;
+      const unsigned mk = __ballot_sync(0xFFFFFFFFu, keep);
+      if (out && keep) out[n + __popc(mk & ((1u << lane) - 1u))] = e;
+      n += __popc(mk);
+      if (mk != 0xFFFFFFFFu) break;
     }
-    return take;
+    return n;
   };
-  // gather: every thread takes chunk lists t, t + 256, ...; a block scan of the counts places them
   int mine = 0;
-  for (int c = t; c < nch; c += kThreads) mine += prefix(c);
-  int cincl = mine;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xFFFFFFFFu, cincl, o);
-    if (lane >= o) cincl += y;
-  }
-  if (lane == 31) sm.red_i[warp] = cincl;
+  for (int c = warp; c < nch; c += kWarps) mine += take_list(c, nullptr);
+  if (lane == 0) sm.red_i[warp] = mine;
   __syncthreads();
-  int base = cincl - mine, n = 0;
+  int base = 0, n = 0;
   for (int w = 0; w < kWarps; ++w) {
     if (w < warp) base += sm.red_i[w];
     n += sm.red_i[w];
@@ -1806,12 +1834,7 @@ __device__ bool draw_list(const Params& P, int b, int js, const T* qr, const Dra
     __syncthreads();
     return false;
   }
-  for (int c = t; c < nch; c += kThreads) {
-    const int take = prefix(c);
-    const uint2* src = cand + (size_t)c * kCandCap;
-    for (int i = 0; i < take; ++i) lst[base + i] = __ldcg(src + i);
-    base += take;
-  }
+  for (int c = warp; c < nch; c += kWarps) base += take_list(c, lst + base);
   __syncthreads();
   // weights, as (token, weight bits)
   for (int i = t; i < n; i += kThreads) {
