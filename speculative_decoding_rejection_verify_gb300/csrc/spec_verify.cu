@@ -694,7 +694,7 @@ __device__ void topk_chunk(const Params& P, const float (&v)[Cfg<T>::PER], int n
   seg_filter<T, VEC>(v, n, c * Cfg<T>::CH, theta, bufs + (size_t)sm.seg_cur * kSegCap, sm);
   // The block meets (and maybe compacts) only on its check schedule.  A bound refreshed over m
   // chunks lets about k / m survivors through per chunk; the next check comes when twice that
-  // rate would fill the buffer's free room (after 1..16 chunks).  Every thread derives the same
+  // rate would fill the buffer's free room (after 1..32 chunks).  Every thread derives the same
   // schedule from values it reads between two barriers, so all of them meet at the same chunks.
   const int dc = c - sm.seg_c0;
   if (seg_end || !tight || dc >= seg_next) {
@@ -706,7 +706,7 @@ __device__ void topk_chunk(const Params& P, const float (&v)[Cfg<T>::PER], int n
     const int fill = min(sm.seg_n, kSegCap);
     __syncthreads();  // nobody adds to the set before every thread has read its size
     const int gap = ((kSegCap - fill) * max(seg_m, 1)) / (2 * k);
-    seg_next = dc + min(16, max(1, gap));
+    seg_next = dc + min(32, max(1, gap));
   }
   const size_t row_slot = ((size_t)b * P.R + rp) * P.nchunk;
   if (threadIdx.x == 0 && c != sm.seg_c0) P.cmeta[row_slot + c] = make_uint2(0u, 0u);
