@@ -72,6 +72,11 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_verify_cuts.restype = i32
     lib.oracle_row_dist_at.argtypes = [_P, i32, i32, f64, i32, f64, f64, _P, _P]
     lib.oracle_row_dist_at.restype = i32
+    lib.oracle_decide_multi.argtypes = [_P, _P, i32, i32, i32, _P, _P, f64, _P, _P, _P, _P, _P, _P]
+    lib.oracle_decide_multi.restype = i32
+    lib.oracle_verify_multi.argtypes = [_P, _P, _P, _P, _P, f32, f32, _P, _P, _P, _P, _P, _P, i32, i32, i32, i32,
+                                        i32, i32]
+    lib.oracle_verify_multi.restype = i32
     lib.oracle_decide_trials.argtypes = [_P, _P, i32, i32, i32, _P, _P, _P, _P, _P, _P, i32]
     lib.oracle_decide_trials.restype = i32
     return lib
@@ -208,4 +213,55 @@ def verify(p: np.ndarray, q: Optional[np.ndarray], draft: np.ndarray, k_per_row:
                                 _ptr(out["flags"]), B, K_max, V, dt, int(nthreads))
     if rc != 0:
         raise ValueError("oracle_verify rejected its arguments")
+    return out
+
+
+def decide_multi(P: np.ndarray, Q: np.ndarray, x, ua, ur: float, lib=None):
+    """The multi-draft decision of one request on fp64 distributions: P [N, K+1, V] (row 0 of chain
+    0 is the shared first position), Q [N, K, V], x and ua [N, K] (ua as float64)."""
+    lib = lib or load()
+    P = np.ascontiguousarray(P, np.float64)
+    N, K1, V = P.shape
+    K = K1 - 1
+    Q = np.ascontiguousarray(Q, np.float64).reshape(N, K, V) if K > 0 else np.zeros((N, 1, V))
+    x = np.ascontiguousarray(x, np.int32).reshape(N, K) if K > 0 else np.zeros((N, 1), np.int32)
+    ua = np.ascontiguousarray(ua, np.float64).reshape(N, K) if K > 0 else np.zeros((N, 1))
+    tok = np.empty(K + 1, np.int32)
+    n = np.empty(1, np.int32)
+    ch = np.empty(1, np.int32)
+    am = np.empty(max(N * K, 1))
+    sm = np.empty(1)
+    work = np.empty(2 * V)
+    fl = lib.oracle_decide_multi(_ptr(P), _ptr(Q), V, N, K, _ptr(x), _ptr(ua), float(ur), _ptr(tok), _ptr(n),
+                                 _ptr(ch), _ptr(am), _ptr(sm), _ptr(work))
+    return dict(tokens=tok, n_acc=int(n[0]), chain=int(ch[0]), accept_margin=am[: N * K].reshape(N, K),
+                sample_margin=float(sm[0]), flags=int(fl))
+
+
+def verify_multi(p: np.ndarray, q: Optional[np.ndarray], draft: np.ndarray, ua: Optional[np.ndarray],
+                 ur: Optional[np.ndarray], temperature: float, draft_temperature: Optional[float] = None,
+                 nthreads: int = 1, lib=None) -> dict:
+    """The multi-draft step on host arrays, same argument meaning as the CUDA ``spec_verify_multi``:
+    p [B, N, K+1, V], q [B, N, K, V] (float32 or bf16 bits; None at temperature 0), draft and ua
+    [B, N, K], ur [B].  Returns tokens [B, K+1], n_acc [B], chain [B], accept_margin [B, N, K],
+    sample_margin [B], flags [B]."""
+    lib = lib or load()
+    p, dt = _logits(p)
+    B, N, K1, V = p.shape
+    K = K1 - 1
+    if q is not None:
+        q, dtq = _logits(q)
+        assert dtq == dt and q.shape == (B, N, K, V)
+    draft = np.ascontiguousarray(draft, np.int32).reshape(B, N, K)
+    ua = np.zeros((B, N, K), np.float32) if ua is None else np.ascontiguousarray(ua, np.float32)
+    ur = np.zeros(B, np.float32) if ur is None else np.ascontiguousarray(ur, np.float32)
+    out = dict(tokens=np.empty((B, K + 1), np.int32), n_acc=np.empty(B, np.int32), chain=np.empty(B, np.int32),
+               accept_margin=np.empty((B, N, K)), sample_margin=np.empty(B), flags=np.empty(B, np.int32))
+    tq = temperature if draft_temperature is None else draft_temperature
+    rc = lib.oracle_verify_multi(_ptr(p), _ptr(q), _ptr(draft), _ptr(ua), _ptr(ur), float(temperature), float(tq),
+                                 _ptr(out["tokens"]), _ptr(out["n_acc"]), _ptr(out["chain"]),
+                                 _ptr(out["accept_margin"]), _ptr(out["sample_margin"]), _ptr(out["flags"]),
+                                 B, N, K, V, dt, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_verify_multi rejected its arguments")
     return out

@@ -514,6 +514,195 @@ int oracle_verify(const void* p, const void* q, const int32_t* draft, const int3
 }
 
 /*
+ * Multi-draft verify: several drafts propose at once (2kiu.com §7 and cf-1.com §2.3 name ensembles
+ * of draft models, the target keeping the draft it accepts).  The pages fix the property the step
+ * must keep -- the emitted tokens are distributed as p (cf-1.com §2.2, 2kiu.com §2.2) -- but no rule
+ * for several candidates, so the rule here applies the single-draft rule to the candidates in turn,
+ * each against what the earlier rejections leave of p:
+ *   r_0 = P_0, the target's distribution at the first position (the drafts share the prefix);
+ *   candidate n, the first token x_n of chain n drawn from its draft distribution Q_n, is
+ *     accepted iff u_n * Q_n(x_n) < r_n(x_n); a rejection leaves r_{n+1} = norm(max(0, r_n - Q_n));
+ *   the first accepted candidate's chain is verified on from its second position with the
+ *     single-draft rule (oracle_decide) on its own target and draft distributions;
+ *   if every candidate is rejected, one token is drawn from r_N by the inverse CDF with ur.
+ * Each candidate's step leaves the law of what follows equal to r_n (the single-draft argument), so
+ * the first emitted token is distributed as P_0, and with N = 1 this is oracle_decide.
+ *   P: [N, K+1, V] (row 0 of chain 0 is P_0; rows 1..K of chain n are its target distributions
+ *      along its own prefix); Q: [N, K, V]; x, ua: [N, K]; ur: the resample uniform.
+ *   out_tokens [K+1], *n_acc, *chain (the accepted chain, -1 when every candidate is rejected),
+ *   accept_margin [N, K]: |u - r/q| of every test taken (inf when q = 0), NaN elsewhere;
+ *   *sample_margin as in oracle_decide.  work: 2 V doubles.  Returns the request's flags.
+ */
+int oracle_decide_multi(const double* P, const double* Q, int V, int N, int K, const int32_t* x,
+                        const double* ua, double ur, int32_t* out_tokens, int32_t* n_acc, int32_t* chain,
+                        double* accept_margin, double* sample_margin, double* work) {
+  int flags = 0;
+  for (int j = 0; j <= K; ++j) out_tokens[j] = -1;
+  for (int i = 0; i < N * K; ++i) accept_margin[i] = NAN;
+  *chain = -1;
+  *n_acc = 0;
+  double* r = work;
+  double* rest = work + V;
+  for (int v = 0; v < V; ++v) r[v] = P[v];  /* r_0 = P_0 */
+  if (K == 0) { /* no drafts: the one token is drawn from P_0 */
+    double R = 0.0;
+    for (int v = 0; v < V; ++v) R += r[v];
+    return inverse_cdf(r, V, R, ur, &out_tokens[0], sample_margin);
+  }
+  int acc = -1;
+  for (int n = 0; n < N && acc < 0; ++n) {
+    const double* Qn = Q + (size_t)n * K * V;
+    const int32_t xn = x[(size_t)n * K];
+    double a = 0.0, c = 0.0;
+    if (xn < 0 || xn >= V)
+      flags |= OR_FLAG_BAD_TOKEN;
+    else {
+      a = r[xn];
+      c = Qn[xn];
+    }
+    const double u = ua[(size_t)n * K];
+    accept_margin[(size_t)n * K] = (c > 0.0) ? fabs(u - a / c) : INFINITY;
+    if (u * c < a) {
+      acc = n;
+      break;
+    }
+    /* rejected: what is left of r after candidate n */
+    double R = 0.0;
+    for (int v = 0; v < V; ++v) {
+      const double d = r[v] - Qn[v];
+      rest[v] = d > 0.0 ? d : 0.0;
+      R += rest[v];
+    }
+    if (R > 0.0)
+      for (int v = 0; v < V; ++v) r[v] = rest[v] / R;
+    else /* only reachable through rounding: r is kept */
+      flags |= OR_FLAG_RESIDUAL_ZERO;
+  }
+  if (acc < 0) { /* every candidate rejected: one token from r_N */
+    double R = 0.0;
+    for (int v = 0; v < V; ++v) R += r[v];
+    return flags | inverse_cdf(r, V, R, ur, &out_tokens[0], sample_margin);
+  }
+  *chain = acc;
+  out_tokens[0] = x[(size_t)acc * K];
+  /* the accepted chain from its second position: the single-draft rule on its own rows */
+  const int K1 = K - 1;
+  double pd[64], qd[64], rm;
+  int32_t n1 = 0;
+  flags |= oracle_decide(P + ((size_t)acc * (K + 1) + 1) * V, Q + ((size_t)acc * K + 1) * V, V, K1,
+                         x + (size_t)acc * K + 1, ua + (size_t)acc * K + 1, ur, out_tokens + 1, &n1, pd, qd,
+                         accept_margin + (size_t)acc * K + 1, sample_margin, &rm, rest);
+  *n_acc = 1 + n1;
+  return flags;
+}
+
+/*
+ * The multi-draft step over a batch, with the argument meaning of the CUDA library's
+ * spec_verify_multi, on host arrays: p [B, N, K+1, V], q [B, N, K, V] (dtype), draft, ua [B, N, K],
+ * ur [B]; temperature T of the target rows (0 = greedy), draft_temperature of the q rows.  Row 0 of
+ * chain 0 of every request is the shared first position (row 0 of the other chains is not read).
+ * Outputs: out_tokens [B, K+1], out_n_acc [B], out_chain [B], accept_margin [B, N, K],
+ * sample_margin [B], out_flags [B].  Greedy: the first chain whose first draft is the argmax of
+ * P_0 (lowest index on ties) is followed with the greedy rule; none -> the argmax is emitted.
+ */
+int oracle_verify_multi(const void* p, const void* q, const int32_t* draft, const float* ua, const float* ur,
+                        float temperature, float draft_temperature, int32_t* out_tokens, int32_t* out_n_acc,
+                        int32_t* out_chain, double* accept_margin, double* sample_margin, int32_t* out_flags,
+                        int B, int N, int K, int V, int dtype, int nthreads) {
+  if (B < 0 || N < 1 || N > 16 || K < 0 || K > 64 || V <= 0 || !(temperature >= 0.0f)) return 1;
+  if (temperature > 0.0f && !(draft_temperature > 0.0f)) return 1;
+  if (nthreads < 1) nthreads = 1;
+  const size_t es = dtype == OR_DTYPE_F32 ? 4 : 2;
+  const double T = (double)temperature, Tq = (double)draft_temperature;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+  for (int b = 0; b < B; ++b) {
+    int flags = 0;
+    const char* pb = (const char*)p + (size_t)b * N * (K + 1) * V * es;
+    const char* qb = q ? (const char*)q + (size_t)b * N * K * V * es : NULL;
+    const int32_t* xb = draft + (size_t)b * N * K;
+    int32_t* tok = out_tokens + (size_t)b * (K + 1);
+    double* am = accept_margin + (size_t)b * N * K;
+    for (int j = 0; j <= K; ++j) tok[j] = -1;
+    for (int i = 0; i < N * K; ++i) am[i] = NAN;
+    sample_margin[b] = NAN;
+    out_chain[b] = -1;
+    out_n_acc[b] = 0;
+    if (temperature == 0.0f) {
+      /* every row the step reads is examined, so a NaN anywhere in the request is flagged */
+      int32_t gr[16 * 65];
+      for (int n = 0; n < N; ++n)
+        for (int j = (n == 0 ? 0 : 1); j <= K; ++j)
+          gr[n * (K + 1) + j] = argmax_row(pb + ((size_t)n * (K + 1) + j) * V * es, dtype, V, &flags);
+      const int32_t g = gr[0];
+      int acc = -1;
+      for (int n = 0; n < N && K > 0 && acc < 0; ++n) {
+        if (xb[(size_t)n * K] < 0 || xb[(size_t)n * K] >= V) flags |= OR_FLAG_BAD_TOKEN;
+        if (xb[(size_t)n * K] == g) acc = n;
+      }
+      int nacc = 0;
+      if (acc < 0) {
+        tok[0] = g;
+      } else {
+        tok[0] = g;
+        nacc = 1;
+        for (int j = 1; j <= K; ++j) {
+          const int32_t gj = gr[acc * (K + 1) + j];
+          if (j == K) {
+            tok[j] = gj;
+            break;
+          }
+          const int32_t xj = xb[(size_t)acc * K + j];
+          if (xj < 0 || xj >= V) flags |= OR_FLAG_BAD_TOKEN;
+          tok[j] = gj;
+          if (xj != gj) break;
+          ++nacc;
+        }
+      }
+      if (flags & OR_FLAG_NONFINITE) {
+        for (int j = 0; j <= K; ++j) tok[j] = -1;
+        nacc = 0;
+        acc = -1;
+      }
+      sample_margin[b] = INFINITY;
+      out_chain[b] = acc;
+      out_n_acc[b] = nacc;
+      out_flags[b] = flags;
+      continue;
+    }
+    double* Pr = (double*)malloc(sizeof(double) * (size_t)N * (K + 1) * V);
+    double* Qr = (double*)malloc(sizeof(double) * (size_t)N * (K > 0 ? K : 1) * V);
+    double* work = (double*)malloc(sizeof(double) * 2 * (size_t)V);
+    double* uad = (double*)malloc(sizeof(double) * (size_t)N * (K > 0 ? K : 1));
+    for (int n = 0; n < N; ++n) {
+      for (int j = 0; j <= K; ++j) {
+        double* dst = Pr + ((size_t)n * (K + 1) + j) * V;
+        if (j == 0 && n > 0) { /* the shared first position: chain 0's row */
+          memcpy(dst, Pr, sizeof(double) * (size_t)V);
+          continue;
+        }
+        flags |= oracle_row_dist(pb + ((size_t)n * (K + 1) + j) * V * es, dtype, V, T, 0, dst, NULL);
+      }
+      for (int j = 0; j < K; ++j)
+        flags |= oracle_row_dist(qb + ((size_t)n * K + j) * V * es, dtype, V, Tq, 0, Qr + ((size_t)n * K + j) * V, NULL);
+      for (int j = 0; j < K; ++j) uad[(size_t)n * K + j] = ua ? (double)ua[((size_t)b * N + n) * K + j] : 0.0;
+    }
+    if (!(flags & OR_FLAG_NONFINITE)) {
+      int32_t nacc = 0, ch = -1;
+      flags |= oracle_decide_multi(Pr, Qr, V, N, K, xb, uad, (double)ur[b], tok, &nacc, &ch, am,
+                                   &sample_margin[b], work);
+      out_n_acc[b] = nacc;
+      out_chain[b] = ch;
+    }
+    out_flags[b] = flags;
+    free(Pr);
+    free(Qr);
+    free(work);
+    free(uad);
+  }
+  return 0;
+}
+
+/*
  * Many independent trials of oracle_decide on one shared pair of distributions (the pins'
  * chi-square and Monte-Carlo checks): P [(K+1), V], Q [K, V]; x, ua [N, K]; ur [N].
  * Outputs out_tokens [N, K+1], out_n_acc [N], out_flags [N].

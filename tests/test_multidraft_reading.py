@@ -1,13 +1,14 @@
-"""Why multi-draft verify is not built (CPU only).
+"""Why the literal reading of multi-draft verify is not the one built (CPU only).
 
 2kiu.com §7 suggests running several draft models at once and keeping the one that accepts the
 most; the pages give no verify rule for it.  Read literally -- verify each draft independently
 with the single-draft rule and keep the result with the most accepted drafts -- the selection
 changes the output law: the first emitted token is no longer distributed as p.  The law is
 computed exactly here, by breakpoint enumeration of each draft's verification through the
-oracle's own decisions, then combined over the two independent verifications.  A lossless
-multi-draft rule (a recursive rejection over the candidates) is not on the pages, so neither
-reading is built (the single-draft law is checked beside it as the control)."""
+oracle's own decisions, then combined over the two independent verifications (the single-draft
+law is checked beside it as the control).  The rule built instead tests the candidates in turn,
+each against what the earlier rejections leave of p (oracle_decide_multi, pinned lossless in
+test_oracle_pins_multidraft.py)."""
 import numpy as np
 import pytest
 
