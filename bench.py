@@ -236,18 +236,29 @@ def run_reference(args, w: W.Workload):
     cores = os.cpu_count() or 1
     q_of = lambda d: None if w.temperature == 0 else d["q"]  # noqa: E731
     kpr_of = lambda d: d["k_per_row"] if w.ragged else None  # noqa: E731
-    probe = W.generate(w, requests=range(min(8, w.B)))
+    multi = MULTI_CHAINS.get(w.label)
+
+    def gen(reqs):
+        return W.generate_multi(w, multi, requests=reqs) if multi else W.generate(w, requests=reqs)
+
+    def run(d):
+        if multi:
+            oracle.verify_multi(d["p"], q_of(d), d["draft"], d["ua"], d["ur"], w.temperature,
+                                draft_temperature=w.tq, nthreads=cores)
+        else:
+            oracle.verify(d["p"], q_of(d), d["draft"], kpr_of(d), d["ua"], d["ur"], w.temperature, w.top_k,
+                          nthreads=cores, draft_temperature=w.tq, top_p=w.top_p)
+
+    probe = gen(range(min(8, w.B)))
     t0 = time.perf_counter()
-    oracle.verify(probe["p"], q_of(probe), probe["draft"], kpr_of(probe), probe["ua"], probe["ur"], w.temperature,
-                  w.top_k, nthreads=cores, draft_temperature=w.tq, top_p=w.top_p)
+    run(probe)
     per_req = (time.perf_counter() - t0) / probe["p"].shape[0]
     budget = args.ref_seconds / max(1, args.steps + args.warmup)
     n = int(max(1, min(args.ref_requests, w.B, budget / max(per_req, 1e-9))))
-    d = W.generate(w, requests=range(n))
+    d = gen(range(n))
 
     def one():
-        oracle.verify(d["p"], q_of(d), d["draft"], kpr_of(d), d["ua"], d["ur"], w.temperature, w.top_k,
-                      nthreads=cores, draft_temperature=w.tq, top_p=w.top_p)
+        run(d)
 
     for _ in range(args.warmup):
         one()
@@ -255,7 +266,7 @@ def run_reference(args, w: W.Workload):
     for _ in range(args.steps):
         one()
     dt = (time.perf_counter() - t0) / args.steps
-    pos = int(d["k_per_row"].sum())
+    pos = n * w.K if multi else int(d["k_per_row"].sum())
     v = pos / dt
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -268,10 +279,92 @@ def run_reference(args, w: W.Workload):
     return 0
 
 
+MULTI_CHAINS = {"multi_c5": 4}  # draft chains per request of the multi-draft workloads
+
+
+def run_gpu_multi(args, w: W.Workload):
+    """Multi-draft verify (spec_verify_multi): N chains of K drafts per request; a step is one call
+    over the batch.  value = B K / step time (the positions a request can advance by)."""
+    import torch
+    import speculative_decoding_rejection_verify_gb300 as sv
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sv.load()
+    N = MULTI_CHAINS[w.label]
+    d = W.generate_multi(w, N, requests=shard_requests(w.B, rank))
+    B, K, V = w.B, w.K, w.V
+
+    def up(a):
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == np.uint16 else torch.from_numpy(a)
+        return t.to(dev)
+
+    copies = [dict(p=up(d["p"]), q=up(d["q"]), x=up(d["draft"]), ua=up(d["ua"]), ur=up(d["ur"])) for _ in range(2)]
+    dt_code = sv.DTYPE_BF16 if w.dtype == "bf16" else sv.DTYPE_F32
+    lib = sv.load()
+    ws = torch.zeros(lib.spec_verify_multi_workspace_bytes(B, N, K, V, dt_code), dtype=torch.uint8, device=dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = (torch.empty((B, K + 1), **i32), torch.empty((B,), **i32), torch.empty((B,), **i32), torch.empty((B,), **i32))
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        c = copies[i & 1]
+        sv.verify_multi(c["p"], c["q"], c["x"], c["ua"], c["ur"], w.temperature, draft_temperature=w.tq,
+                        workspace_tensor=ws, stream=stream, out=out)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(min(args.steps, 200))]
+    with ClockSampler(str(local)) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        for i, (a, z) in enumerate(ev):
+            a.record(stream)
+            step(i)
+            z.record(stream)
+        torch.cuda.synchronize()
+    step_ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, world, dev)
+    per_step = [a.elapsed_time(z) for a, z in ev]
+    value = sum_over_ranks(B * K, world, dev) / (step_ms * 1e-3)
+    if rank != 0:
+        return 0
+    nbytes = W.multi_algorithmic_bytes(w, N, B)
+    peak, peak_kind = measured_peak()
+    achieved = nbytes / (step_ms * 1e-3) / 1e9
+    line = {"metric": "verified draft positions/s (multi-draft) and logits GB/s", "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic (seeded generator; no dataset)",
+            "config": {"workload": f"{w.label}: B={B} N={N} chains K={K} V={V} {w.dtype} T={w.temperature:g}",
+                       "logits_bytes_per_step": nbytes, "launch": "direct launches",
+                       "parallelism": f"{world} independent batches (no collective)"},
+            "median_step_ms": statistics.median(per_step),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                         "frac_vs_nominal": achieved / NOMINAL_HBM_GBS, "traffic": None,
+                         "kernel": "whole step (row table, streaming pass, per-request pass)"},
+            "gpu_launches": args.steps * 3, "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_gpu(args, w: W.Workload):
     import torch
     import speculative_decoding_rejection_verify_gb300 as sv
     rank, world, local = dist_env()
+    if w.label in MULTI_CHAINS:
+        return run_gpu_multi(args, w)
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")

@@ -61,6 +61,7 @@ typedef enum {
 #define SPEC_MAX_K 16        /* K_max                                                        */
 #define SPEC_MAX_V 2097152   /* vocabulary size                                              */
 #define SPEC_MAX_TOPK 256    /* top_k values in (0, V) above this take SPEC_ERR_UNSUPPORTED   */
+#define SPEC_MAX_DRAFTS 4    /* draft chains per request of spec_verify_multi                 */
 
 /*
  * Optional diagnostics.  Every pointer is device memory and may be NULL (= not written).
@@ -221,6 +222,42 @@ size_t spec_sample_workspace_bytes(int32_t rows, int32_t V, spec_dtype_t dtype, 
 spec_status_t spec_sample(const void* logits, const float* u, const spec_sampling_t* sampling, int32_t* out_tokens,
                           float* out_prob, int32_t rows, int32_t V, spec_dtype_t dtype, void* workspace,
                           size_t workspace_bytes, void* stream);
+
+/*
+ * Multi-draft verify: N draft chains per request (2kiu.com/news/5895634 §7 and cf-1.com/news/5155685
+ * §2.3 name ensembles of draft models whose accepted draft the target keeps).  The pages fix the
+ * property the step keeps -- the emitted tokens are distributed as p (cf-1.com §2.2, 2kiu.com §2.2) --
+ * but no rule for several candidates; the rule here tests the chains' first drafts in turn, each
+ * against what the earlier rejections leave of p:
+ *   r_0 = P_0; candidate n (first draft x_n of chain n, drawn from its draft distribution Q_n) is
+ *   accepted iff u_n * Q_n(x_n) < r_n(x_n); a rejection leaves r_{n+1} = norm(max(0, r_n - Q_n));
+ *   the first accepted chain is verified on with the single-draft rule (as spec_verify) on its own
+ *   rows; with every candidate rejected one token is drawn from r_N (inverse CDF, ascending token
+ *   id, u_resample).  Temperature 0: the first chain whose first draft is the argmax of P_0 (lowest
+ *   index on ties) is followed with the greedy rule; none: the argmax is emitted.
+ *   p_logits      [B, N, K_max+1, V] dtype: the target's logits along each chain; row 0 of chain 0
+ *                 is the shared first position (row 0 of the other chains is never read);
+ *   q_logits      [B, N, K_max, V] dtype: each chain's draft logits (NULL iff temperature == 0);
+ *   draft_tokens  [B, N, K_max] int32;  u_accept [B, N, K_max] float (NULL iff temperature == 0):
+ *                 u_accept[b, n, 0] tests candidate n, u_accept[b, n, j] position j of chain n;
+ *   u_resample    [B] float (NULL iff temperature == 0);
+ *   sampling      temperature and draft_temperature as for spec_verify_ex; top_k must be off and
+ *                 top_p >= 1 (SPEC_ERR_UNSUPPORTED otherwise);
+ *   out_tokens    [B, K_max+1] int32: the emitted tokens, then -1;  out_num_accepted [B] int32;
+ *   out_chain     [B] int32 or NULL: the accepted chain, -1 when every candidate was rejected;
+ *   out_flags     [B] int32 or NULL: SPEC_FLAG_* bits (a non-finite row anywhere in a request leaves
+ *                 it without a result: n_acc 0, tokens -1, chain -1);
+ *   workspace     spec_verify_multi_workspace_bytes(...) bytes of device memory, 256-B aligned.
+ * Every chain has K_max drafts (no k_per_row).  1 <= N <= SPEC_MAX_DRAFTS.  With N = 1 the results
+ * are spec_verify's.  Launches the row table, the streaming pass over every row read, and one block
+ * per request for the decisions; asynchronous on `stream`.
+ */
+size_t spec_verify_multi_workspace_bytes(int32_t B, int32_t N, int32_t K_max, int32_t V, spec_dtype_t dtype);
+spec_status_t spec_verify_multi(const void* p_logits, const void* q_logits, const int32_t* draft_tokens,
+                                const float* u_accept, const float* u_resample, const spec_sampling_t* sampling,
+                                int32_t* out_tokens, int32_t* out_num_accepted, int32_t* out_chain,
+                                int32_t* out_flags, int32_t B, int32_t N, int32_t K_max, int32_t V,
+                                spec_dtype_t dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Test support, not for production use.  With bit 0 of `hooks` set, every later call (from any

@@ -10,6 +10,9 @@ The C ABI is declared in ``include/spec_verify.h``; the names here mirror it:
   draft_temperature=None, top_p=1.0)`` -> ``(tokens [B, K+1] int32, num_accepted [B] int32,
   stats dict | None)`` on device tensors, through ``spec_verify_ex``;
 * ``verify_host(...)`` the same on host (numpy / CPU torch) arrays through ``spec_verify_host_ex``;
+* ``verify_multi(p, q, draft, u_accept, u_resample, temperature, draft_temperature=None)`` ->
+  ``(tokens, num_accepted, chain, flags)``: several draft chains per request through
+  ``spec_verify_multi``;
 * ``workspace_bytes(B, K, V, dtype, top_k)``;
 * ``Controller(...)``: the host-side draft-length controller of ``include/spec_control.h``
   (2kiu.com/news/5895634 §4.4 and §7), fed with each batch's ``num_accepted``.
@@ -43,10 +46,12 @@ FLAG_TOPK_TIE = 32
 MAX_K = 16
 MAX_V = 2097152
 MAX_TOPK = 256
+MAX_DRAFTS = 4
 
 EXPORTS = ("spec_verify_workspace_bytes", "spec_verify", "spec_verify_ex", "spec_verify_host_staging_bytes",
            "spec_verify_host", "spec_verify_host_ex", "spec_verify_static", "spec_verify_status_string",
-           "spec_sample_workspace_bytes", "spec_sample", "spec_verify_set_test_hooks")
+           "spec_sample_workspace_bytes", "spec_sample", "spec_verify_set_test_hooks",
+           "spec_verify_multi_workspace_bytes", "spec_verify_multi")
 CONTROL_EXPORTS = ("spec_ctrl_default_config", "spec_ctrl_create", "spec_ctrl_destroy", "spec_ctrl_update",
                    "spec_ctrl_skip", "spec_ctrl_k", "spec_ctrl_window_mean", "spec_ctrl_window_fill",
                    "spec_ctrl_totals")
@@ -127,6 +132,11 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
             lib.spec_sample_workspace_bytes.restype = Z
             lib.spec_sample.argtypes = [P, P, ctypes.POINTER(SamplingStruct), P, P, I, I, I, P, Z, P]
             lib.spec_sample.restype = I
+            lib.spec_verify_multi_workspace_bytes.argtypes = [I, I, I, I, I]
+            lib.spec_verify_multi_workspace_bytes.restype = Z
+            lib.spec_verify_multi.argtypes = [P, P, P, P, P, ctypes.POINTER(SamplingStruct), P, P, P, P, I, I, I, I,
+                                              I, P, Z, P]
+            lib.spec_verify_multi.restype = I
             lib.spec_verify_set_test_hooks.argtypes = [I]
             lib.spec_verify_set_test_hooks.restype = None
             CP = ctypes.POINTER(ControlConfig)
@@ -308,6 +318,47 @@ def sample(logits, u=None, temperature: float = 1.0, top_k: int = 0, top_p: floa
     if rc != SPEC_OK:
         raise SpecVerifyError(rc, "spec_sample")
     return tokens, pr
+
+
+def verify_multi(p, q, draft, u_accept=None, u_resample=None, temperature: float = 1.0,
+                 draft_temperature: Optional[float] = None, workspace_tensor=None, stream=None, out=None):
+    """spec_verify_multi on device tensors: p [B, N, K+1, V], q [B, N, K, V] (None at temperature 0),
+    draft and u_accept [B, N, K], u_resample [B].  Returns (tokens [B, K+1], num_accepted [B],
+    chain [B], flags [B]) int32 tensors; the call is asynchronous."""
+    torch = _torch()
+    lib = load()
+    if p.dim() != 4:
+        raise ValueError("p must be [B, N, K+1, V]")
+    B, N, K1, V = p.shape
+    K = K1 - 1
+    dev = p.device
+    dt = _dtype_code(p)
+    _check(p, "p", (B, N, K + 1, V), p.dtype, dev)
+    if q is not None:
+        _check(q, "q", (B, N, K, V), p.dtype, dev)
+    if draft is not None:
+        _check(draft, "draft", (B, N, K), torch.int32, dev)
+    if u_accept is not None:
+        _check(u_accept, "u_accept", (B, N, K), torch.float32, dev)
+    if u_resample is not None:
+        _check(u_resample, "u_resample", (B,), torch.float32, dev)
+    st = stream if stream is not None else torch.cuda.current_stream(dev)
+    if out is None:
+        i32 = dict(dtype=torch.int32, device=dev)
+        out = (torch.empty((B, K + 1), **i32), torch.empty((B,), **i32), torch.empty((B,), **i32),
+               torch.empty((B,), **i32))
+    tokens, nacc, chain, flags = out
+    nbytes = lib.spec_verify_multi_workspace_bytes(B, N, K, V, dt)
+    if nbytes == 0:
+        raise SpecVerifyError(1, "spec_verify_multi_workspace_bytes")
+    ws = workspace_tensor if workspace_tensor is not None else workspace(nbytes, dev, st)
+    smp = _sampling(temperature, draft_temperature, 0, 1.0)
+    rc = lib.spec_verify_multi(_ptr(p), _ptr(q), _ptr(draft), _ptr(u_accept), _ptr(u_resample), ctypes.byref(smp),
+                               tokens.data_ptr(), nacc.data_ptr(), _ptr(chain), _ptr(flags), B, N, K, V, dt,
+                               ws.data_ptr(), ws.numel(), st.cuda_stream)
+    if rc != SPEC_OK:
+        raise SpecVerifyError(rc, "spec_verify_multi")
+    return tokens, nacc, chain, flags
 
 
 _stage_cache: Dict[int, object] = {}

@@ -2786,6 +2786,491 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) fin
   finish_request<T, kSample, VEC, false, kCluster>(P, (int)(blockIdx.x / kCluster), sm, dyn);
 }
 
+// ------------------------------------------------------------------------------------------------
+// multi-draft verify (spec_verify_multi)
+// ------------------------------------------------------------------------------------------------
+// Several draft chains per request (2kiu.com §7 and cf-1.com §2.3 name ensembles of draft models).
+// The first position is shared: the chains' first drafts are tested in turn, each against what the
+// earlier rejections leave of p -- r_0 = P_0; candidate n is accepted iff u_n q_n(x_n) < r_n(x_n);
+// a rejection leaves r_{n+1} = max(0, r_n - q_n) / R_n with R_n = sum_v max(0, r_n(v) - q_n(v)) --
+// so that the first emitted token is distributed as P_0.  The first accepted chain is verified on
+// with the single-draft rule; with every candidate rejected one token is drawn from r_N.  The
+// streaming pass summarises every row the step reads: sub-request b N + n holds chain n of request
+// b, and a row table leaves out row 0 of every chain after the first (the shared position is read
+// once).  The per-request pass below takes the decisions, one block per request.
+
+// The rows of the first position's stage n (weights max(0, r_n - q_n)): P_0 and Q_0..Q_n.
+struct MultiRows {
+  const void* row[SPEC_MAX_DRAFTS + 1];  // P_0, then Q_0, Q_1, ...
+  float L[SPEC_MAX_DRAFTS + 1];          // their log2 normalisers (max * c2 + log2 sum)
+  float Rinv[SPEC_MAX_DRAFTS];           // 1 / R_i, or 0 where R_i vanished (r_{i+1} = r_i then)
+  int n;                                 // the stage
+  bool sub;                              // weights max(0, r_n - q_n); else r_n itself
+};
+
+// The stage's weights for the 8 logits [e0, e0 + 8) (logits past V weigh 0).  r follows the
+// recursion above term by term; every pass computes it with the same instructions.
+template <typename T, bool VEC>
+__device__ __forceinline__ void multi_weights8(const Params& P, const MultiRows& mr, int e0, float (&w)[8]) {
+  float z[8];
+  load8<T, VEC>(static_cast<const T*>(mr.row[0]), e0, P.V, z);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) w[k] = ex2(fmaf(z[k], P.c2, -mr.L[0]));
+  const int last = mr.sub ? mr.n : mr.n - 1;
+  for (int i = 0; i <= last; ++i) {
+    load8<T, VEC>(static_cast<const T*>(mr.row[1 + i]), e0, P.V, z);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float d = w[k] - ex2(fmaf(z[k], P.c2q, -mr.L[1 + i]));
+      if (i < mr.n)
+        w[k] = mr.Rinv[i] > 0.0f ? fmaxf(d, 0.0f) * mr.Rinv[i] : w[k];
+      else
+        w[k] = fmaxf(d, 0.0f);
+    }
+  }
+}
+
+// One block-wide pass over the stage's weights: tile sums (256 logits a warp tile), a block scan of
+// per-thread runs of tiles; returns the total.  With `draw`, also the inverse CDF in ascending token
+// id at target u * total (the tile, then the lane, then the logit), setting sm.y, sm.margin and, when
+// rounding leaves the target past the sums, *clamp with the last logit that has weight.
+template <typename T, bool VEC>
+__device__ float multi_pass(const Params& P, const MultiRows& mr, bool draw, float u, float* wt, Smem& sm,
+                            int* clamp) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int ntile = (P.V + kTile - 1) / kTile;
+  for (int i = warp; i < ntile; i += kWarps) {
+    float w[8];
+    multi_weights8<T, VEC>(P, mr, i * kTile + lane * 8, w);
+    float s = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) s += w[k];
+    s = warp_sum(s);
+    if (lane == 0) wt[i] = s;
+  }
+  __syncthreads();
+  const int L = (ntile + kThreads - 1) / kThreads;
+  const int s0 = t * L, s1 = min(s0 + L, ntile);
+  float seg = 0.0f;
+  for (int i = s0; i < s1; ++i) seg += wt[i];
+  float incl = seg;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sm.red_s[warp] = incl;
+  if (t == 0) {
+    sm.seg_first = kThreads;
+    sm.found = 0;
+  }
+  __syncthreads();
+  float off = 0.0f, total = 0.0f;
+  for (int w = 0; w < kWarps; ++w) {
+    if (w < warp) off += sm.red_s[w];
+    total += sm.red_s[w];
+  }
+  incl += off;
+  if (!draw || !(total > 0.0f)) {
+    __syncthreads();
+    return total;
+  }
+  const float target = u * total;
+  if (target < incl) atomicMin(&sm.seg_first, t);
+  __syncthreads();
+  const int tf = sm.seg_first;
+  if (t == (tf == kThreads ? 0 : tf)) {
+    int found = -1;
+    float run = incl - seg;
+    if (tf < kThreads)
+      for (int i = s0; i < s1; ++i) {
+        if (target < run + wt[i]) {
+          found = i;
+          break;
+        }
+        run += wt[i];
+      }
+    if (found < 0) {  // rounding left the target past the sums: the last tile with weight
+      int i = ntile - 1;
+      while (i > 0 && !(wt[i] > 0.0f)) --i;
+      run = 0.0f;
+      for (int j = 0; j < i; ++j) run += wt[j];
+      found = i;
+      sm.found = 2;
+    } else {
+      sm.found = 1;
+    }
+    sm.tile = found;
+    sm.tile_base = run;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int tile = sm.tile;
+    bool clamped = sm.found == 2;
+    float w[8];
+    multi_weights8<T, VEC>(P, mr, tile * kTile + lane * 8, w);
+    float ls = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) ls += w[k];
+    float li = ls;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xFFFFFFFFu, li, o);
+      if (lane >= o) li += y;
+    }
+    const float tl = target - sm.tile_base;
+    const unsigned hit = clamped ? 0u : __ballot_sync(0xFFFFFFFFu, tl < li);
+    int yl, ye = -1;
+    float margin = 0.0f;
+    if (hit) {
+      yl = __ffs(hit) - 1;
+      if (lane == yl) {
+        float run = li - ls;
+        for (int k = 0; k < 8; ++k) {
+          if (tl < run + w[k]) {
+            ye = k;
+            margin = fminf(tl - run, run + w[k] - tl) / total;
+            break;
+          }
+          run += w[k];
+        }
+        if (ye < 0) {  // sub-ulp disagreement between the levels: the lane's last logit with weight
+          for (int k = 7; k >= 0 && ye < 0; --k)
+            if (w[k] > 0.0f) ye = k;
+          clamped = true;
+        }
+      }
+    } else {
+      const unsigned pos = __ballot_sync(0xFFFFFFFFu, ls > 0.0f);
+      yl = pos ? 31 - __clz(pos) : 0;
+      if (lane == yl)
+        for (int k = 7; k >= 0 && ye < 0; --k)
+          if (w[k] > 0.0f) ye = k;
+      clamped = true;
+    }
+    if (lane == yl) {
+      sm.y = tile * kTile + yl * 8 + (ye < 0 ? 0 : ye);
+      sm.margin = clamped ? 0.0f : margin;
+      if (clamped) *clamp = 1;
+    }
+  }
+  __syncthreads();
+  return total;
+}
+
+// The bonus-style draw of a whole row from p alone (its chunk masses from the stored (max, sum)
+// pairs pick the chunk; only that chunk is read again).  Whole block; result in sm.y, sm.margin.
+template <typename T, bool VEC>
+__device__ void draw_from_summaries(const Params& P, const float2* part, const T* pr, float M, float u, float* wt,
+                                    uint4* ring, Smem& sm, int* clamp) {
+  const int t = threadIdx.x;
+  const int nch = P.nchunk;
+  const float Mp2 = M * P.c2;
+  for (int c = t; c < nch; c += kThreads) {
+    float mass = 0.0f;
+    for (int w = 0; w < kWarps; ++w) {
+      const float2 pc = __ldcg(part + (size_t)c * kWarps + w);
+      if (pc.y != 0.0f) mass += pc.y * ex2(pc.x * P.c2 - Mp2);
+    }
+    wt[c] = mass;
+  }
+  __syncthreads();
+  if (t == 0) {
+    float S = 0.0f;
+    for (int c = 0; c < nch; ++c) S += wt[c];
+    const float target = u * S;
+    float cum = 0.0f;
+    int cs = -1;
+    for (int c = 0; c < nch; ++c) {
+      if (target < cum + wt[c]) {
+        cs = c;
+        break;
+      }
+      cum += wt[c];
+    }
+    if (cs < 0) {  // rounding put u * S past the sum: the last chunk with mass (clamped below)
+      cs = nch - 1;
+      while (cs > 0 && !(wt[cs] > 0.0f)) --cs;
+      cum = 0.0f;
+      for (int c = 0; c < cs; ++c) cum += wt[c];
+    }
+    sm.tile = cs;
+    sm.tile_base = target - cum;
+    sm.total = S;
+  }
+  __syncthreads();
+  const int cs = sm.tile;
+  const float tin = sm.tile_base, S = sm.total;
+  __syncthreads();
+  DrawRows d;
+  d.resid = false;
+  d.Mp2 = Mp2;
+  d.Lp = 0.0f;
+  d.Tp = -INFINITY;
+  d.Lq = 0.0f;
+  d.c2q = P.c2q;
+  d.Tq = 0.0f;
+  const int v0 = cs * Cfg<T>::CH;
+  draw_range<T, VEC, false>(P, pr, pr, d, v0, min(P.V, v0 + Cfg<T>::CH), false, u, tin, S, wt, ring, sm, clamp);
+}
+
+// The per-request pass of spec_verify_multi (MODE kSample or kGreedy; P.B counts sub-requests,
+// P.K is the drafts per chain).  Dynamic shared memory: the CDF ring, the tile / chunk sums, then
+// the rows' (max, sum) or argmax.
+template <typename T, int MODE, bool VEC>
+__global__ void __launch_bounds__(kThreads) finish_multi_kernel(const Params P, int N, int32_t* out_chain) {
+  extern __shared__ __align__(128) unsigned char dyn[];
+  __shared__ Smem sm;
+  pdl_wait();
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int b = blockIdx.x, K = P.K, R = P.R, V = P.V;
+  uint4* ring = reinterpret_cast<uint4*>(dyn);
+  const int ntile = (V + kTile - 1) / kTile;
+  float* wt = reinterpret_cast<float*>(dyn + (VEC ? (size_t)kDrawStages * kDrawStageBytes : 0));
+  float* rM = wt + (ntile > P.nchunk ? ntile : P.nchunk);
+  float* rS = rM + N * R;  // greedy: the argmax, as int bits
+  const int s0 = b * N;    // chain n of request b is sub-request s0 + n
+  auto part = [&](int n, int rp) { return P.partial + ((size_t)(s0 + n) * R + rp) * P.nchunk * kWarps; };
+  auto prow_n = [&](int n, int j) { return static_cast<const T*>(P.p) + ((size_t)(s0 + n) * (K + 1) + j) * (size_t)V; };
+  auto qrow_n = [&](int n, int j) { return static_cast<const T*>(P.q) + ((size_t)(s0 + n) * K + j) * (size_t)V; };
+  // ---- every row the step read: (max, sum) or (max, lowest argmax); a non-finite row anywhere in
+  // the request leaves it without a result ----
+  if (t == 0) {
+    sm.flags = 0;
+    sm.nonfinite = 0;
+  }
+  __syncthreads();
+  for (int r = warp; r < N * R; r += kWarps) {
+    const int n = r / R, rp = r - n * R;
+    if (n > 0 && rp == 0) continue;  // the shared position is chain 0's row
+    const float2* pc0 = part(n, rp);
+    if (MODE == kSample) {
+      const float c2 = rp > K ? P.c2q : P.c2;
+      float m = -INFINITY, s = 0.0f;
+      for (int c = lane; c < P.nchunk * kWarps; c += 32) {
+        const float2 pc = __ldcg(pc0 + c);
+        lse_merge(m, s, pc.x, pc.y, c2);
+      }
+      lse_warp(m, s, c2);
+      if (lane == 0) {
+        rM[r] = m;
+        rS[r] = s;
+        if (!(s > 0.0f) || isinf(m) || isnan(s)) sm.nonfinite = 1;
+      }
+    } else {
+      float best = -INFINITY;
+      int bi = 0x7FFFFFFF;
+      bool nan = false;
+      for (int c = lane; c < P.nchunk * kWarps; c += 32) {
+        const float2 pc = __ldcg(pc0 + c);
+        const int idx = __float_as_int(pc.y);
+        if (idx < 0) nan = true;
+        amax_merge(best, bi, pc.x, idx);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float vo = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+        const int io = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+        amax_merge(best, bi, vo, io);
+      }
+      nan = __any_sync(0xFFFFFFFFu, nan);
+      if (lane == 0) {
+        rS[r] = __int_as_float(bi);
+        if (nan) sm.nonfinite = 1;
+      }
+    }
+  }
+  __syncthreads();
+  int32_t* tok = P.out_tokens + (size_t)b * (K + 1);
+  auto finish = [&](int nacc, int chain) {
+    if (t == 0) {
+      P.out_nacc[b] = nacc;
+      if (out_chain) out_chain[b] = chain;
+      if (P.flags) P.flags[b] = sm.flags;
+    }
+  };
+  if (sm.nonfinite) {
+    if (t <= K) tok[t] = -1;
+    if (t == 0) sm.flags |= SPEC_FLAG_NONFINITE;
+    __syncthreads();
+    finish(0, -1);
+    return;
+  }
+  auto draft = [&](int n, int j) { return __ldg(P.draft + (size_t)(s0 + n) * K + j); };
+  if (MODE == kGreedy) {
+    if (warp == 0) {
+      const int g0 = __float_as_int(rS[0]);
+      int chain = -1;
+      bool bad = false;
+      for (int n = 0; n < N && K > 0 && chain < 0; ++n) {
+        const int x = draft(n, 0);
+        bad |= x < 0 || x >= V;
+        if (x == g0) chain = n;
+      }
+      int nacc = 0;
+      if (chain >= 0) {  // the chain's positions 1..K-1, one per lane, then its argmax at K
+        nacc = 1;
+        const int j = lane + 1;
+        bool acc = true;
+        int x = 0;
+        if (j < K) {
+          x = draft(chain, j);
+          acc = x == __float_as_int(rS[chain * R + j]);
+        }
+        const unsigned rej = __ballot_sync(0xFFFFFFFFu, j < K && !acc);
+        const int js = rej ? __ffs(rej) : K;  // the first position (1..K) that emits the argmax
+        nacc = js;
+        if (rej && lane == js - 1) bad |= x < 0 || x >= V;
+        bad = __any_sync(0xFFFFFFFFu, bad);
+        if (lane <= K) {
+          int v = -1;
+          if (lane == 0) v = g0;
+          else if (lane < js) v = draft(chain, lane);
+          else if (lane == js) v = __float_as_int(rS[chain * R + js]);
+          tok[lane] = v;
+        }
+      } else {
+        if (lane <= K) tok[lane] = lane == 0 ? g0 : -1;
+      }
+      if (lane == 0 && bad) sm.flags |= SPEC_FLAG_BAD_TOKEN;
+      if (lane == 0) sm.jstar = nacc, sm.y = chain;
+    }
+    __syncthreads();
+    finish(sm.jstar, sm.y);
+    return;
+  }
+  // ---- sampling: the first position's candidates in turn ----
+  const float u = __ldg(P.ur + b);
+  auto Lp = [&](int n, int j) { return rM[n * R + j] * P.c2 + log2f(rS[n * R + j]); };
+  auto Lq = [&](int n, int j) { return rM[n * R + K + 1 + j] * P.c2q + log2f(rS[n * R + K + 1 + j]); };
+  int clamp = 0;
+  if (K == 0) {  // no drafts: the one token is drawn from P_0
+    draw_from_summaries<T, VEC>(P, part(0, 0), prow_n(0, 0), rM[0], u, wt, ring, sm, &clamp);
+    if (t == 0) {
+      tok[0] = sm.y;
+      if (clamp) sm.flags |= SPEC_FLAG_CDF_CLAMP;
+    }
+    __syncthreads();
+    finish(0, -1);
+    return;
+  }
+  MultiRows mr;
+  mr.row[0] = prow_n(0, 0);
+  mr.L[0] = Lp(0, 0);
+  for (int n = 0; n < N; ++n) {
+    mr.row[1 + n] = qrow_n(n, 0);
+    mr.L[1 + n] = Lq(n, 0);
+    mr.Rinv[n] = 0.0f;
+  }
+  int chain = -1;
+  for (int n = 0; n < N; ++n) {
+    if (t == 0) {  // candidate n against r_n
+      const int x = draft(n, 0);
+      float a = 0.0f, c = 0.0f;
+      if (x >= 0 && x < V) {
+        a = ex2(fmaf(load1<T>(static_cast<const T*>(mr.row[0]) + x), P.c2, -mr.L[0]));
+        for (int i = 0; i < n; ++i) {
+          const float d = a - ex2(fmaf(load1<T>(static_cast<const T*>(mr.row[1 + i]) + x), P.c2q, -mr.L[1 + i]));
+          a = mr.Rinv[i] > 0.0f ? fmaxf(d, 0.0f) * mr.Rinv[i] : a;
+        }
+        c = ex2(fmaf(load1<T>(static_cast<const T*>(mr.row[1 + n]) + x), P.c2q, -mr.L[1 + n]));
+      } else {
+        sm.flags |= SPEC_FLAG_BAD_TOKEN;
+      }
+      sm.found = __ldg(P.ua + (size_t)(s0 + n) * K) * c < a;
+    }
+    __syncthreads();
+    const bool accepted = sm.found;
+    __syncthreads();
+    if (accepted) {
+      chain = n;
+      break;
+    }
+    // rejected: R_n, the mass of max(0, r_n - q_n); for the last candidate the draw from it
+    mr.n = n;
+    mr.sub = true;
+    const bool last = n == N - 1;
+    const float Rn = multi_pass<T, VEC>(P, mr, last, u, wt, sm, &clamp);
+    mr.Rinv[n] = Rn > 0.0f ? 1.0f / Rn : 0.0f;
+    if (!(Rn > 0.0f)) {
+      if (t == 0) sm.flags |= SPEC_FLAG_RESIDUAL_ZERO;
+      __syncthreads();
+      if (last) {  // nothing of r_n survives q_n (rounding): the draw from r_n itself
+        mr.sub = false;
+        multi_pass<T, VEC>(P, mr, true, u, wt, sm, &clamp);
+      }
+    }
+  }
+  if (chain < 0) {
+    if (t <= K) tok[t] = t == 0 ? sm.y : -1;
+    if (t == 0 && clamp) sm.flags |= SPEC_FLAG_CDF_CLAMP;
+    __syncthreads();
+    finish(0, -1);
+    return;
+  }
+  // ---- the accepted chain from its second position: the single-draft rule on its own rows ----
+  if (warp == 0) {
+    const int j = lane + 1;  // position j, 1..K-1
+    bool acc = true, bad = false;
+    int x = 0;
+    if (j < K) {
+      x = draft(chain, j);
+      bad = x < 0 || x >= V;
+      float a = 0.0f, cq = 0.0f;
+      if (!bad) {
+        a = ex2(fmaf(load1<T>(prow_n(chain, j) + x), P.c2, -Lp(chain, j)));
+        cq = ex2(fmaf(load1<T>(qrow_n(chain, j) + x), P.c2q, -Lq(chain, j)));
+      }
+      acc = __ldg(P.ua + (size_t)(s0 + chain) * K + j) * cq < a;
+    }
+    const unsigned rej = __ballot_sync(0xFFFFFFFFu, j < K && !acc);
+    const int js = rej ? __ffs(rej) : K;  // the position that draws (a rejection, or K: the bonus)
+    if (rej && lane == js - 1 && bad) sm.flags |= SPEC_FLAG_BAD_TOKEN;
+    if (lane <= K) tok[lane] = lane == 0 ? draft(chain, 0) : (lane < js ? draft(chain, lane) : -1);
+    if (lane == 0) sm.jstar = js;
+  }
+  __syncthreads();
+  const int js = sm.jstar;
+  if (js < K) {  // the residual max(0, P - Q) at the rejected position
+    DrawRows d;
+    d.resid = true;
+    d.Mp2 = rM[chain * R + js] * P.c2;
+    d.Lp = Lp(chain, js);
+    d.Tp = -INFINITY;
+    d.Lq = Lq(chain, js);
+    d.c2q = P.c2q;
+    d.Tq = -INFINITY;
+    const float Rr = draw_range<T, VEC, false>(P, prow_n(chain, js), qrow_n(chain, js), d, 0, V, true, u, 0.0f, 0.0f,
+                                               wt, ring, sm, &clamp);
+    if (!(Rr > 0.0f)) {  // max(0, p - q) vanished through rounding: draw from p
+      if (t == 0) sm.flags |= SPEC_FLAG_RESIDUAL_ZERO;
+      d.resid = false;
+      draw_range<T, VEC, false>(P, prow_n(chain, js), prow_n(chain, js), d, 0, V, true, u, 0.0f, 0.0f, wt, ring, sm,
+                                &clamp);
+    }
+  } else {  // every draft of the chain accepted: the extra token from its row K
+    draw_from_summaries<T, VEC>(P, part(chain, K), prow_n(chain, K), rM[chain * R + K], u, wt, ring, sm, &clamp);
+  }
+  if (t == 0) {
+    tok[js] = sm.y;
+    if (clamp) sm.flags |= SPEC_FLAG_CDF_CLAMP;
+  }
+  __syncthreads();
+  finish(js, chain);
+}
+
+// The row table of spec_verify_multi: request b's chains in order, every row of chain 0 and the
+// rows after the first of the other chains (entries (sub-request << 6) | padded row).
+__global__ void __launch_bounds__(256) build_rowmap_multi(int B, int N, int R, uint32_t* rowmap, uint32_t* total_rows) {
+  const uint32_t per_req = (uint32_t)(N * R - (N - 1));
+  for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < B * N; s += gridDim.x * blockDim.x) {
+    const int b = s / N, n = s - b * N;
+    uint32_t off = (uint32_t)b * per_req + (n == 0 ? 0u : (uint32_t)R + (uint32_t)(n - 1) * (uint32_t)(R - 1));
+    for (int rp = n == 0 ? 0 : 1; rp < R; ++rp) rowmap[off++] = ((uint32_t)s << 6) | (uint32_t)rp;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) *total_rows = (uint32_t)B * per_req;
+}
+
 // Ragged batches: a table of valid rows in request-major order, so no item is spent on padding.
 __global__ void __launch_bounds__(1024) build_rowmap(const int32_t* __restrict__ kpr, int B, int K,
                                                      int greedy, uint32_t* rowmap,
@@ -2966,6 +3451,38 @@ static cudaError_t launch_mode(int mode, bool vec, const Params& P, uint32_t ite
     default:
       return vec ? launch_t<T, kGreedy, true>(P, items, st) : launch_t<T, kGreedy, false>(P, items, st);
   }
+}
+
+// spec_verify_multi: the row table, the streaming pass over the table, the per-request pass.
+template <typename T, int MODE, bool VEC>
+static cudaError_t launch_multi(const Params& P, int Breq, int N, int32_t* out_chain, cudaStream_t st) {
+  auto k1 = stats_kernel<T, MODE, VEC>;
+  auto k2 = finish_multi_kernel<T, MODE, VEC>;
+  const size_t d1 = stats_smem(MODE, VEC);
+  const int ntile = (P.V + kTile - 1) / kTile;
+  const size_t d2 = (VEC ? (size_t)kDrawStages * kDrawStageBytes : 0) +
+                    (size_t)(ntile > P.nchunk ? ntile : P.nchunk) * sizeof(float) + (size_t)2 * N * P.R * sizeof(float);
+  cudaError_t e = prepare(k1, d1);
+  if (e == cudaSuccess) e = prepare(k2, d2);
+  int dev = 0, sms = 0, occ = 0;
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k1, kThreads, d1);
+  if (e != cudaSuccess) return e;
+  const uint32_t rows = (uint32_t)Breq * (uint32_t)(N * P.R - (N - 1));
+  const uint64_t items = (uint64_t)rows * (uint64_t)P.nchunk;
+  const unsigned rb = (unsigned)(((uint64_t)Breq * N + 255) / 256);
+  build_rowmap_multi<<<rb < 1024u ? (rb > 0 ? rb : 1u) : 1024u, 256, 0, st>>>(
+      Breq, N, P.R, const_cast<uint32_t*>(P.rowmap), const_cast<uint32_t*>(P.total_rows));
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (occ < 1) occ = 1;
+  uint32_t grid = (uint32_t)sms * (uint32_t)occ;
+  if (items < grid) grid = items > 0 ? (uint32_t)items : 1u;
+  k1<<<grid, kThreads, d1, st>>>(P);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_after(k2, dim3((unsigned)Breq), dim3(kThreads), d2, st, true, P, N, out_chain);
 }
 
 }  // namespace sv
@@ -3235,6 +3752,88 @@ spec_status_t spec_sample(const void* logits, const float* u, const spec_samplin
   // per-request pass also writes q(x) of the drawn token
   return verify_impl(logits, nullptr, nullptr, nullptr, nullptr, u, &sp, out_tokens, nacc, nullptr, rows, 0, V,
                      dtype, ws, base, stream, rows > 0 ? out_prob : nullptr);
+}
+
+size_t spec_verify_multi_workspace_bytes(int32_t B, int32_t N, int32_t K_max, int32_t V, spec_dtype_t dtype) {
+  if (B < 0 || N < 1 || N > SPEC_MAX_DRAFTS || K_max < 0 || K_max > SPEC_MAX_K || V <= 0 || V > SPEC_MAX_V) return 0;
+  if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return 0;
+  if ((int64_t)B * N >= (1ll << 25)) return 0;
+  const int es = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
+  Layout a, g;
+  if (!make_layout(B * N, K_max, V, es, kSample, true, &a) || !make_layout(B * N, K_max, V, es, kGreedy, true, &g))
+    return 0;
+  return a.bytes > g.bytes ? a.bytes : g.bytes;
+}
+
+spec_status_t spec_verify_multi(const void* p_logits, const void* q_logits, const int32_t* draft_tokens,
+                                const float* u_accept, const float* u_resample, const spec_sampling_t* sampling,
+                                int32_t* out_tokens, int32_t* out_num_accepted, int32_t* out_chain,
+                                int32_t* out_flags, int32_t B, int32_t N, int32_t K_max, int32_t V,
+                                spec_dtype_t dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 0 || N < 1 || K_max < 0 || V <= 0 || !sampling) return SPEC_ERR_INVALID_ARG;
+  const float T = sampling->temperature, Tq = sampling->draft_temperature;
+  if (!(T >= 0.0f) || isinf(T) || sampling->top_k < 0) return SPEC_ERR_INVALID_ARG;
+  if (T > 0.0f && (!(Tq > 0.0f) || isinf(Tq))) return SPEC_ERR_INVALID_ARG;
+  if (!(sampling->top_p > 0.0f)) return SPEC_ERR_INVALID_ARG;
+  if (N > SPEC_MAX_DRAFTS || K_max > SPEC_MAX_K || V > SPEC_MAX_V) return SPEC_ERR_UNSUPPORTED;
+  if (dtype != SPEC_DTYPE_F32 && dtype != SPEC_DTYPE_BF16) return SPEC_ERR_UNSUPPORTED;
+  if ((sampling->top_k > 0 && sampling->top_k < V) || sampling->top_p < 1.0f) return SPEC_ERR_UNSUPPORTED;
+  if ((int64_t)B * N >= (1ll << 25)) return SPEC_ERR_UNSUPPORTED;
+  if (B == 0) return SPEC_OK;
+  const bool greedy = T == 0.0f;
+  if (!p_logits || !out_tokens || !out_num_accepted) return SPEC_ERR_INVALID_ARG;
+  if (K_max > 0 && !draft_tokens) return SPEC_ERR_INVALID_ARG;
+  if (!greedy && (!u_resample || (K_max > 0 && (!q_logits || !u_accept)))) return SPEC_ERR_INVALID_ARG;
+  const int mode = greedy ? kGreedy : kSample;
+  const size_t es = dtype == SPEC_DTYPE_BF16 ? 2 : 4;
+  Layout L;
+  if (!make_layout(B * N, K_max, V, (int)es, mode, true, &L)) return SPEC_ERR_UNSUPPORTED;
+  if (!workspace || ((uintptr_t)workspace & 255u) || workspace_bytes < L.bytes) return SPEC_ERR_WORKSPACE;
+  const bool vec = ((uintptr_t)p_logits % 16 == 0) && (!q_logits || (uintptr_t)q_logits % 16 == 0) &&
+                   ((size_t)V * es % 16 == 0);
+  char* ws = static_cast<char*>(workspace);
+  Params P = {};
+  P.p = p_logits;
+  P.q = greedy ? nullptr : q_logits;
+  P.draft = draft_tokens;
+  P.kpr = nullptr;
+  P.ua = u_accept;
+  P.ur = u_resample;
+  P.out_tokens = out_tokens;
+  P.out_nacc = out_num_accepted;
+  P.flags = out_flags;
+  P.test_hooks = sv::g_test_hooks.load(std::memory_order_relaxed);
+  P.B = B * N;
+  P.K = K_max;
+  P.V = V;
+  P.top_k = 0;
+  P.nchunk = L.nchunk;
+  P.R = L.R;
+  P.c2 = greedy ? 0.0f : (float)(1.4426950408889634 / (double)T);
+  P.invT = greedy ? 0.0f : (float)(1.0 / (double)T);
+  P.c2q = greedy ? 0.0f : (float)(1.4426950408889634 / (double)Tq);
+  P.invTq = greedy ? 0.0f : (float)(1.0 / (double)Tq);
+  P.top_p = 1.0f;
+  P.partial = reinterpret_cast<float2*>(ws + L.partial);
+  P.cmeta = reinterpret_cast<uint2*>(ws + L.cmeta);
+  P.cand = reinterpret_cast<uint2*>(ws + L.cand);
+  P.rowstat = reinterpret_cast<float2*>(ws + L.rowstat);
+  P.rowmap = reinterpret_cast<const uint32_t*>(ws + L.rowmap);
+  P.total_rows = reinterpret_cast<const uint32_t*>(ws + L.total_rows);
+  P.uniform_items = (uint32_t)(L.rows_padded * (uint64_t)L.nchunk);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (dtype == SPEC_DTYPE_BF16)
+    e = greedy ? (vec ? launch_multi<uint16_t, kGreedy, true>(P, B, N, out_chain, s)
+                      : launch_multi<uint16_t, kGreedy, false>(P, B, N, out_chain, s))
+               : (vec ? launch_multi<uint16_t, kSample, true>(P, B, N, out_chain, s)
+                      : launch_multi<uint16_t, kSample, false>(P, B, N, out_chain, s));
+  else
+    e = greedy ? (vec ? launch_multi<float, kGreedy, true>(P, B, N, out_chain, s)
+                      : launch_multi<float, kGreedy, false>(P, B, N, out_chain, s))
+               : (vec ? launch_multi<float, kSample, true>(P, B, N, out_chain, s)
+                      : launch_multi<float, kSample, false>(P, B, N, out_chain, s));
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 void spec_verify_set_test_hooks(int32_t hooks) { sv::g_test_hooks.store(hooks, std::memory_order_relaxed); }

@@ -103,6 +103,10 @@ WORKLOADS["c5_topp0.9"] = Workload("c5_topp0.9", B=1024, K=4, V=128256, dtype="b
                                    top_k=0, seed=1061, alpha=0.8, top_p=0.9)
 WORKLOADS["c5_tq0.5"] = Workload("c5_tq0.5", B=1024, K=4, V=128256, dtype="bf16", temperature=1.0,
                                  top_k=0, seed=1062, alpha=0.45, draft_temperature=0.5)
+# Multi-draft verify: 256 requests of 4 draft chains, 4 drafts each, over the largest batch's
+# vocabulary (the target's noise scale 0.5 between each chain's first draft and the target).
+WORKLOADS["multi_c5"] = Workload("multi_c5", B=256, K=4, V=128256, dtype="bf16", temperature=1.0, top_k=0,
+                                 seed=1081, alpha=None, tau=0.5)
 # Draft-token sampling (the step before verification): 1024 rows of 128256 bf16 logits, one draw
 # each; a batch of requests with no drafts, whose one row is the row sampled from.
 WORKLOADS["sample_c5"] = Workload("sample_c5", B=1024, K=0, V=128256, dtype="bf16", temperature=1.0,
@@ -252,6 +256,73 @@ def generate(w: Workload, requests: Optional[Sequence[int]] = None, threads: int
     return dict(p=p, q=q, draft=x, k_per_row=kb.astype(np.int32), ua=ua, ur=ur,
                 temperature=float(w.temperature), draft_temperature=float(w.tq), top_k=int(w.top_k),
                 top_p=float(w.top_p), workload=w)
+
+
+_S_MULTI = 10  # first stream of the multi-draft generator
+
+
+def generate_multi(w: Workload, N: int, requests: Optional[Sequence[int]] = None, tau: Optional[float] = None) -> dict:
+    """N draft chains per request (w.K drafts each), for the multi-draft verify step.
+
+    At the shared first position the target's logits are a base row and each chain's draft logits
+    that base plus tau * N(0, 1) of its own; along chain n (positions 1..K-1) the draft logits are
+    fresh base rows and the target's the same plus noise, and row K is a fresh base row plus noise
+    (the target after the chain's prefix).  Row 0 of chains n > 0 is NaN: the step never reads it.
+    Draft tokens are the chains' own samples (Gumbel-max at T_q; argmax when greedy).
+    Returns dict(p [n, N, K+1, V], q [n, N, K, V], draft [n, N, K], ua [n, N, K], ur [n], temperature,
+    draft_temperature, N, workload)."""
+    tau = (0.5 if w.tau is None else w.tau) if tau is None else tau
+    reqs = np.arange(w.B) if requests is None else np.asarray(requests, np.int64)
+    n_req, K, V = len(reqs), w.K, w.V
+    bf = w.dtype == "bf16"
+    st = np.uint16 if bf else np.float32
+    p = np.empty((n_req, N, K + 1, V), st)
+    q = np.empty((n_req, N, K, V), st)
+    x = np.zeros((n_req, N, K), np.int32)
+    ua = np.empty((n_req, N, K), np.float32)
+    ur = np.empty(n_req, np.float32)
+    bias_v = bias(w)
+    cast = to_bf16_bits if bf else (lambda a: a)
+    nan = BF16_NAN if bf else np.nan
+
+    def one(i):
+        b = int(reqs[i])
+        r = _rng(w.seed, _S_MULTI, b)
+        base0 = SIGMA * r.standard_normal(V, dtype=np.float32) + bias_v
+        for n in range(N):
+            p[i, n, 0] = cast(base0) if n == 0 else nan
+            if K > 0:
+                q[i, n, 0] = cast(base0 + np.float32(tau) * r.standard_normal(V, dtype=np.float32))
+            for j in range(1, K + 1):
+                base = SIGMA * r.standard_normal(V, dtype=np.float32) + bias_v
+                p[i, n, j] = cast(base + np.float32(tau) * r.standard_normal(V, dtype=np.float32))
+                if j < K:
+                    q[i, n, j] = cast(base)
+            g = _rng(w.seed, _S_MULTI + 1 + n, b)
+            for j in range(K):
+                x[i, n, j] = _draft_token(as_f32(q[i, n, j]), w.tq, 0, w.greedy, g)
+        k = _rng(w.seed, _S_MULTI + 1 + N, b).integers(0, 1 << 24, size=N * K + 1)
+        ua[i] = (k[: N * K].astype(np.float32) * np.float32(UGRID)).reshape(N, K)
+        ur[i] = np.float32(k[N * K]) * np.float32(UGRID)
+
+    threads = min(16, os.cpu_count() or 1)
+    if n_req > 1 and threads > 1:
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(one, range(n_req)))
+    else:
+        for i in range(n_req):
+            one(i)
+    return dict(p=p, q=q, draft=x, ua=ua, ur=ur, temperature=float(w.temperature),
+                draft_temperature=float(w.tq), N=N, workload=w)
+
+
+def multi_algorithmic_bytes(w: Workload, N: int, B: int) -> int:
+    """Bytes one multi-draft pass must read at least: the shared first row, every chain's target
+    rows 1..K and (unless greedy) its draft rows, once each, plus tokens, uniforms and outputs."""
+    s = 2 if w.dtype == "bf16" else 4
+    rows = 1 + N * w.K + (0 if w.temperature == 0.0 else N * w.K)
+    per_req = 4 * N * w.K * 2 + 4 + 4 * (w.K + 1) + 4 * 3
+    return B * (rows * w.V * s + per_req)
 
 
 def algorithmic_bytes(w: Workload, kb: np.ndarray) -> int:
