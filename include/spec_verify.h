@@ -261,11 +261,12 @@ spec_status_t spec_verify_multi(const void* p_logits, const void* q_logits, cons
 
 /*
  * Test support, not for production use.  With bit 0 of `hooks` set, every later call (from any
- * host thread) makes each block of the streaming pass withhold its first bulk copy: every wait for
- * it runs out after a short limit, the block marks all its chunks NaN, and every request of the
- * batch that uses sampling or greedy mode comes out with SPEC_FLAG_NONFINITE, n_acc 0 and tokens -1
- * (top-k batches are not affected).  It exercises the bounded-wait failure path of the streaming
- * pass without any fault.  0 restores normal operation.
+ * host thread) makes each block of the streaming pass treat the chunks it was to read as lost:
+ * it leaves their summaries NaN, as a failed load would, instead of reading them, and every
+ * request of a batch in sampling or greedy mode over 16-byte-aligned rows comes out with
+ * SPEC_FLAG_NONFINITE, n_acc 0 and tokens -1 (top-k batches and unaligned rows are not
+ * affected).  It exercises the handling of a lost streaming item without any fault.  0 restores
+ * normal operation.
  */
 void spec_verify_set_test_hooks(int32_t hooks);
 

@@ -178,8 +178,8 @@ def _dtype_code(t) -> int:
 
 
 def set_test_hooks(hooks: int) -> None:
-    """spec_verify_set_test_hooks (test support: bit 0 makes the streaming pass's bounded waits
-    run out, so a batch comes out flagged non-finite)."""
+    """spec_verify_set_test_hooks (test support: bit 0 makes the streaming pass treat every chunk
+    as lost, so a batch comes out flagged non-finite)."""
     load().spec_verify_set_test_hooks(int(hooks))
 
 

@@ -10,11 +10,11 @@
 //
 // Design.  The work is a stream over every logit of every valid row (HBM bound), plus a small
 // per-request tail, in two kernels chained by programmatic dependent launch:
-//   * the streaming pass (stats_kernel): a persistent grid whose blocks each own a contiguous range
-//     of (request, row, 16 KB chunk) items; thread 0 moves every chunk into a shared-memory ring
-//     with one bulk copy (the copy engine) completing on an mbarrier, and each warp leaves a
-//     summary of its share: (max, sum of exp) for sampling, (max, lowest argmax) for greedy, a
-//     running candidate set for top-k;
+//   * the streaming pass: every (request, row, 16 KB chunk) item is read once and each warp leaves
+//     a summary of its share -- (max, sum of exp) for sampling, (max, lowest argmax) for greedy
+//     (stats_item_kernel: short-lived blocks of two items each, loaded straight into registers),
+//     or a running candidate set for top-k (stats_kernel: a persistent grid whose blocks each own
+//     a contiguous range of items, with a cp.async ring);
 //   * the per-request pass (finish_kernel; 8-block clusters for small batches): one block per
 //     request merges its rows' summaries into normalisers, runs the ratio test and the
 //     first-rejection scan, and draws the resampled or bonus token by inverse CDF, re-reading only
@@ -38,10 +38,10 @@ namespace sv {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kChunkBytes = 16384;      // bytes of logits per work item (16 B per thread x 4)
-constexpr int kStages = 4;               // work items in flight per CTA (bulk-copy ring)
 constexpr int kCluster = 8;              // blocks sharing one request's draw when requests are few
-constexpr int kStagesTopK = 3;           // top-k: a shallower ring leaves room for 3 blocks per SM
-__host__ __device__ constexpr int stages_of(int mode) { return mode == 1 ? kStagesTopK : kStages; }
+constexpr int kStagesTopK = 3;           // top-k streaming pass: cp.async ring stages (3 blocks per SM)
+constexpr int kItemBlocksPerSM = 6;      // sampling / greedy streaming pass: resident blocks per SM
+constexpr int kItemsPerBlock = 2;        // items (16 KB each) per block of that pass
 constexpr int kTile = 256;               // inverse-CDF tile: 32 lanes x 8 logits
 constexpr int kCandCap = 256;            // top-k candidates stored per chunk
 constexpr int kSegCap = 1024;            // running top-k candidates of a row segment (per buffer)
@@ -301,46 +301,6 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// Bulk copies (the copy engine, TMA) completing on shared-memory mbarriers: one thread moves a whole
-// 16 KB chunk with one instruction; the stage's barrier counts the arriving bytes.
-__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count) : "memory");
-}
-// makes the barriers' initialisation visible to the copy engine
-__device__ __forceinline__ void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* b, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(done)
-      : "r"(smem_addr(b)), "r"(parity)
-      : "memory");
-  return done != 0u;
-}
-// Waits for the phase of the given parity to complete; false if it has not after kWaitLimit tries
-// (each try suspends the thread for a while), which no working copy engine comes near.
-constexpr int kWaitLimit = 1 << 20;
-constexpr int kTestWaitLimit = 1 << 10;  // under the test hook that withholds a copy
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, int limit = kWaitLimit) {
-  for (int i = 0; i < limit; ++i)
-    if (mbar_try_wait(b, parity)) return true;
-  return false;
-}
-// bytes (a multiple of 16) from global src (16-byte aligned) into shared dst, completing on b
-__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* b) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_addr(dst)),
-               "l"(src), "r"(bytes), "r"(smem_addr(b))
-               : "memory");
-}
-
 // ------------------------------------------------------------------------------------------------
 // shared memory
 // ------------------------------------------------------------------------------------------------
@@ -383,8 +343,6 @@ struct Smem {
   int nuc_n;         // logits gathered
   uint32_t nuc_key;  // key of the cut
   uint32_t red_cnt[32];
-  uint64_t ring_full[kStages];   // streaming pass: a stage's bytes have landed
-  uint64_t ring_empty[kStages];  // streaming pass: every warp has read the stage
 };
 
 // ------------------------------------------------------------------------------------------------
@@ -2556,10 +2514,11 @@ __device__ __forceinline__ void greedy_vec(uint4 (&raw)[Cfg<T>::LOADS], int n, i
   if (lane == 0) out[t >> 5] = make_float2(M, __int_as_float(M == M ? v0 + idx : -1));
 }
 
-// Pass 1: stream every valid row once.  Each CTA owns a contiguous range of items
-// (request, row, chunk), so successive items walk memory in order and the cursor needs no
-// divisions; for aligned rows the bulk-copy ring keeps the next kStages - 1 chunks in flight.  No
-// block waits for another and nothing is counted: pass 2 starts when this grid is done.
+// Pass 1 for top-k (and for rows that are not 16-byte aligned, in every mode): stream every valid
+// row once.  Each CTA owns a contiguous range of items (request, row, chunk), so successive items
+// walk memory in order, the cursor needs no divisions and a row segment's candidate set carries
+// over from chunk to chunk.  No block waits for another and nothing is counted: pass 2 starts
+// when this grid is done.
 template <typename T, int MODE, bool VEC>
 __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
   extern __shared__ __align__(128) unsigned char dyn[];
@@ -2570,7 +2529,7 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
   const uint32_t hi = (uint32_t)(((uint64_t)total * (blockIdx.x + 1)) / gridDim.x);
   if (lo >= hi) return;
   uint4* stages = reinterpret_cast<uint4*>(dyn);
-  constexpr int ST = stages_of(MODE);
+  constexpr int ST = kStagesTopK;
   uint2* surv = reinterpret_cast<uint2*>(dyn + (VEC ? (size_t)ST * kChunkBytes : 0));
   Cursor cc;
   cursor_at<T>(P, lo, cc);
@@ -2588,10 +2547,10 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
       topk_chunk<T, VEC>(P, v, n, k.b, k.rp, k.c, seg_start, seg_end, surv, sm, seg_next, seg_m);
   };
   if (VEC && MODE == kTopK) {
-    // Top-k mode keeps a per-thread ring: each thread copies its own vectors of a chunk and refills
-    // its slots as soon as it has read them.  (With the shared ring below, a stage is refilled only
-    // once every warp has read it; between the block barriers of the candidate set that cost the
-    // fp32 top-k pass 6%.)
+    // A per-thread ring: each thread copies its own vectors of a chunk and refills its slots as
+    // soon as it has read them.  (A ring shared by the block refills a stage only once every warp
+    // has read it; between the block barriers of the candidate set that cost the fp32 top-k pass
+    // 6%.)
     Cursor ic = cc;
 #pragma unroll
     for (int s = 0; s < ST; ++s) {
@@ -2623,85 +2582,6 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
       s = s + 1 == ST ? 0 : s + 1;
     }
     cp_async_wait<0>();
-  } else if (VEC) {
-    // The ring: thread 0 moves each item (16 KB, or the row's tail) into its stage with one bulk
-    // copy that completes on the stage's `full` barrier; every warp reads its vectors of the stage
-    // into registers and arrives on the stage's `empty` barrier, and thread 0 refills the stage
-    // once all eight warps have.  Every wait is bounded: a thread whose wait gives up waits no more
-    // (thread 0 then copies no more), the loop runs out on whatever the stages hold, and the block
-    // drains its copies in flight and marks all its items NaN, so that their requests come out
-    // flagged non-finite rather than wrong.  (Sampling and greedy modes.)
-    const int t = threadIdx.x;
-    uint64_t* full = sm.ring_full;
-    uint64_t* empty = sm.ring_empty;
-    if (t == 0) {
-      for (int q = 0; q < ST; ++q) {
-        mbar_init(&full[q], 1);
-        mbar_init(&empty[q], kWarps);
-      }
-      mbar_fence_init();
-    }
-    __syncthreads();
-    bool failed = false;
-    uint32_t used = 0u, last_par = 0u;  // thread 0: stages copied into, parity of each one's last copy
-    // test hook 1: the block's first copy is withheld, so every wait for it runs out (soon)
-    const bool withhold = (P.test_hooks & 1) != 0;
-    const int limit = withhold ? kTestWaitLimit : kWaitLimit;
-    auto issue = [&](int q, const Cursor& k, uint32_t par) {
-      const uint32_t nb = (uint32_t)(min(Cfg<T>::CH, P.V - k.c * Cfg<T>::CH) * (int)sizeof(T));
-      mbar_arrive_expect_tx(&full[q], nb);
-      bulk_copy(stages + (size_t)q * (kChunkBytes / 16), k.row + (size_t)k.c * Cfg<T>::CH * sizeof(T), nb, &full[q]);
-      used |= 1u << q;
-      last_par = (last_par & ~(1u << q)) | (par << q);
-    };
-    Cursor ic = cc;
-    for (int q = 0; q < ST; ++q) {
-      if (lo + q < hi) {
-        if (t == 0 && !(withhold && q == 0)) issue(q, ic, 0u);
-        cursor_next<T>(P, ic);
-      }
-    }
-    int s = 0;
-    uint32_t phase = 0u;  // parity of the stages' current use
-    for (uint32_t it = lo; it < hi; ++it) {
-      uint4* st = stages + (size_t)s * (kChunkBytes / 16);
-      if (!failed) failed = !mbar_wait(&full[s], phase, limit);
-      uint4 raw[Cfg<T>::LOADS];
-#pragma unroll
-      for (int l = 0; l < Cfg<T>::LOADS; ++l) raw[l] = st[l * kThreads + t];
-      __syncwarp();
-      if ((t & 31) == 0) mbar_arrive(&empty[s]);
-      if (it + ST < hi) {  // refill the stage once every warp holds its bytes
-        if (t == 0 && !failed) {
-          failed = !mbar_wait(&empty[s], phase, limit);
-          if (!failed) issue(s, ic, phase ^ 1u);
-        }
-        cursor_next<T>(P, ic);
-      }
-      const int n = min(Cfg<T>::CH, P.V - cc.c * Cfg<T>::CH);
-      const size_t slot = ((size_t)cc.b * P.R + cc.rp) * P.nchunk + cc.c;
-      if (MODE == kSample)
-        sample_vec<T>(cc.rp > P.K ? P.c2q : P.c2, raw, n, P.partial + slot * kWarps);
-      else
-        greedy_vec<T>(raw, n, cc.c * Cfg<T>::CH, P.partial + slot * kWarps);
-      cursor_next<T>(P, cc);
-      if (++s == ST) {
-        s = 0;
-        phase ^= 1u;
-      }
-    }
-    if (__syncthreads_or(failed)) {
-      if (t == 0)
-        for (int q = 0; q < ST; ++q)
-          if ((used >> q) & 1u) mbar_wait(&full[q], (last_par >> q) & 1u, limit);
-      Cursor mc;
-      cursor_at<T>(P, lo, mc);
-      for (uint32_t it = lo; it < hi; ++it) {
-        const size_t slot = ((size_t)mc.b * P.R + mc.rp) * P.nchunk + mc.c;
-        if (t < kWarps) P.partial[slot * kWarps + t] = make_float2(NAN, MODE == kGreedy ? __int_as_float(-1) : NAN);
-        cursor_next<T>(P, mc);
-      }
-    }
   } else {
     for (uint32_t it = lo; it < hi; ++it) {
       const int v0 = cc.c * Cfg<T>::CH;
@@ -2711,6 +2591,63 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
       summarise_f(cc, v);
       seg_start = seg_end;
       cursor_next<T>(P, cc);
+    }
+  }
+}
+
+// Pass 1 in sampling and greedy modes (aligned rows): one short-lived block per IPB consecutive
+// items.  Each thread loads its 16-byte vectors of the block's items straight into registers (all
+// IPB x 16 KB of the block in flight at once), the block summarises them and exits, and the
+// hardware keeps every SM filled with new blocks: no ring to manage, no barrier, no wait, and no
+// ramp or tail of a persistent grid's static ranges.  Test hook bit 0 makes every block treat
+// its items as lost -- summaries NaN, as a failed load would leave them -- so that the flagging
+// of the requests they touch can be tested without any fault.
+template <typename T, int MODE, int IPB>
+__global__ void __launch_bounds__(kThreads, kItemBlocksPerSM) stats_item_kernel(const Params P) {
+  pdl_launch_next();  // the next pass may launch now; it waits for this grid before reading
+  const uint32_t total = P.rowmap ? __ldg(P.total_rows) * (uint32_t)P.nchunk : P.uniform_items;
+  const uint32_t it0 = blockIdx.x * (uint32_t)IPB;
+  if (it0 >= total) return;
+  const int t = threadIdx.x;
+  Cursor cc;
+  cursor_at<T>(P, it0, cc);
+  if (P.test_hooks & 1) {
+    for (int i = 0; i < IPB && it0 + i < total; ++i) {
+      const size_t slot = ((size_t)cc.b * P.R + cc.rp) * P.nchunk + cc.c;
+      if (t < kWarps) P.partial[slot * kWarps + t] = make_float2(NAN, MODE == kGreedy ? __int_as_float(-1) : NAN);
+      if (i + 1 < IPB) cursor_next<T>(P, cc);
+    }
+    return;
+  }
+  uint4 raw[IPB][Cfg<T>::LOADS];
+  int nn[IPB];
+  {
+    Cursor k = cc;
+#pragma unroll
+    for (int i = 0; i < IPB; ++i) {
+      nn[i] = 0;
+      if (it0 + i < total) {
+        const int v0 = k.c * Cfg<T>::CH;
+        nn[i] = min(Cfg<T>::CH, P.V - v0);
+        const char* base = k.row + (size_t)v0 * sizeof(T);
+#pragma unroll
+        for (int l = 0; l < Cfg<T>::LOADS; ++l) {
+          const int e0 = (l * kThreads + t) * Cfg<T>::VW;
+          raw[i][l] = e0 < nn[i] ? ldg_stream(base + (size_t)e0 * sizeof(T)) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (i + 1 < IPB) cursor_next<T>(P, k);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < IPB; ++i) {
+    if (nn[i] > 0) {
+      const size_t slot = ((size_t)cc.b * P.R + cc.rp) * P.nchunk + cc.c;
+      if (MODE == kSample)
+        sample_vec<T>(cc.rp > P.K ? P.c2q : P.c2, raw[i], nn[i], P.partial + slot * kWarps);
+      else
+        greedy_vec<T>(raw[i], nn[i], cc.c * Cfg<T>::CH, P.partial + slot * kWarps);
+      if (i + 1 < IPB) cursor_next<T>(P, cc);
     }
   }
 }
@@ -3362,7 +3299,7 @@ static int mode_of(float temperature, int top_k, int V) {
 
 // dynamic shared memory of the two passes
 static size_t stats_smem(int mode, bool vec) {
-  return (vec ? (size_t)stages_of(mode) * kChunkBytes : 0) + (mode == kTopK ? (size_t)2 * kSegCap * sizeof(uint2) : 0);
+  return mode == kTopK ? (vec ? (size_t)kStagesTopK * kChunkBytes : 0) + (size_t)2 * kSegCap * sizeof(uint2) : 0;
 }
 static size_t finish_smem(int mode, int V, int es, bool vec, bool nuc) {
   const int ntile = (V + kTile - 1) / kTile;
@@ -3399,25 +3336,47 @@ static cudaError_t launch_after(void (*kern)(A...), dim3 grid, dim3 block, size_
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+static cudaError_t sm_count(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+  return e;
+}
+
+// The streaming pass over `items` (an upper bound when the layout is ragged): short-lived blocks
+// in sampling and greedy modes over aligned rows, else the persistent grid, one resident wave of
+// it with static contiguous ranges.
+template <typename T, int MODE, bool VEC>
+static cudaError_t launch_stream(const Params& P, uint64_t items, cudaStream_t st) {
+  if constexpr (VEC && MODE != kTopK) {
+    const uint64_t g = (items + kItemsPerBlock - 1) / kItemsPerBlock;
+    stats_item_kernel<T, MODE, kItemsPerBlock><<<(unsigned)(g > 0 ? g : 1), kThreads, 0, st>>>(P);
+    return cudaGetLastError();
+  } else {
+    auto k1 = stats_kernel<T, MODE, VEC>;
+    const size_t d1 = stats_smem(MODE, VEC);
+    int sms = 0, occ = 0;
+    cudaError_t e = prepare(k1, d1);
+    if (e == cudaSuccess) e = sm_count(&sms);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k1, kThreads, d1);
+    if (e != cudaSuccess) return e;
+    uint64_t grid = (uint64_t)sms * (uint64_t)(occ > 0 ? occ : 1);
+    if (items < grid) grid = items > 0 ? items : 1;
+    k1<<<(unsigned)grid, kThreads, d1, st>>>(P);
+    return cudaGetLastError();
+  }
+}
+
 template <typename T, int MODE, bool VEC>
 static cudaError_t launch_t(const Params& P, uint32_t items, cudaStream_t st) {
   const int es = (int)sizeof(T);
   const bool nuc = MODE != kGreedy && P.top_p < 1.0f;
-  auto k1 = stats_kernel<T, MODE, VEC>;
   auto k2 = nuc ? finish_kernel<T, MODE, VEC, MODE != kGreedy> : finish_kernel<T, MODE, VEC, false>;
-  const size_t d1 = stats_smem(MODE, VEC), d2 = finish_smem(MODE, P.V, es, VEC, nuc);
-  cudaError_t e = prepare(k1, d1);
-  if (e == cudaSuccess) e = prepare(k2, d2);
-  int dev = 0, sms = 0, occ = 0;
-  if (e == cudaSuccess) e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k1, kThreads, d1);
-  if (e != cudaSuccess) return e;
-  if (occ < 1) occ = 1;
-  uint32_t grid = (uint32_t)sms * (uint32_t)occ;  // one resident wave, static item assignment
-  if (items < grid) grid = items > 0 ? items : 1;
-  k1<<<grid, kThreads, d1, st>>>(P);
-  e = cudaGetLastError();
+  const size_t d2 = finish_smem(MODE, P.V, es, VEC, nuc);
+  int sms = 0;
+  cudaError_t e = prepare(k2, d2);
+  if (e == cudaSuccess) e = sm_count(&sms);
+  if (e == cudaSuccess) e = launch_stream<T, MODE, VEC>(P, items, st);
   if (e == cudaSuccess && P.pass1_done) e = cudaEventRecord(static_cast<cudaEvent_t>(P.pass1_done), st);
   if (e != cudaSuccess) return e;
   // the kernel after the streaming pass overlaps its launch with the pass's tail, unless an event
@@ -3456,18 +3415,11 @@ static cudaError_t launch_mode(int mode, bool vec, const Params& P, uint32_t ite
 // spec_verify_multi: the row table, the streaming pass over the table, the per-request pass.
 template <typename T, int MODE, bool VEC>
 static cudaError_t launch_multi(const Params& P, int Breq, int N, int32_t* out_chain, cudaStream_t st) {
-  auto k1 = stats_kernel<T, MODE, VEC>;
   auto k2 = finish_multi_kernel<T, MODE, VEC>;
-  const size_t d1 = stats_smem(MODE, VEC);
   const int ntile = (P.V + kTile - 1) / kTile;
   const size_t d2 = (VEC ? (size_t)kDrawStages * kDrawStageBytes : 0) +
                     (size_t)(ntile > P.nchunk ? ntile : P.nchunk) * sizeof(float) + (size_t)2 * N * P.R * sizeof(float);
-  cudaError_t e = prepare(k1, d1);
-  if (e == cudaSuccess) e = prepare(k2, d2);
-  int dev = 0, sms = 0, occ = 0;
-  if (e == cudaSuccess) e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k1, kThreads, d1);
+  cudaError_t e = prepare(k2, d2);
   if (e != cudaSuccess) return e;
   const uint32_t rows = (uint32_t)Breq * (uint32_t)(N * P.R - (N - 1));
   const uint64_t items = (uint64_t)rows * (uint64_t)P.nchunk;
@@ -3476,11 +3428,7 @@ static cudaError_t launch_multi(const Params& P, int Breq, int N, int32_t* out_c
       Breq, N, P.R, const_cast<uint32_t*>(P.rowmap), const_cast<uint32_t*>(P.total_rows));
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (occ < 1) occ = 1;
-  uint32_t grid = (uint32_t)sms * (uint32_t)occ;
-  if (items < grid) grid = items > 0 ? (uint32_t)items : 1u;
-  k1<<<grid, kThreads, d1, st>>>(P);
-  e = cudaGetLastError();
+  e = launch_stream<T, MODE, VEC>(P, items, st);
   if (e != cudaSuccess) return e;
   return launch_after(k2, dim3((unsigned)Breq), dim3(kThreads), d2, st, true, P, N, out_chain);
 }

@@ -1,8 +1,8 @@
-"""The streaming pass's bounded waits give up cleanly, tested without any fault: under the test
-hook (spec_verify_set_test_hooks, bit 0) every block withholds its first bulk copy, so every wait
-for it runs out after a short limit; the block drains its other copies, marks all its chunks NaN,
-and every request of the batch comes out flagged non-finite with n_acc 0 and tokens -1.  With the
-hook cleared the next call on the same context is exact again."""
+"""A lost streaming item is flagged, tested without any fault: under the test hook
+(spec_verify_set_test_hooks, bit 0) every block of the streaming pass leaves the summaries of the
+chunks it was to read NaN instead of reading them, and every request of the batch comes out
+flagged non-finite with n_acc 0 and tokens -1.  With the hook cleared the next call on the same
+context is exact again."""
 import numpy as np
 import pytest
 
@@ -20,7 +20,7 @@ NONFINITE = 16
                                        ("c5_a0.8", dict(B=300, V=40000, ragged=(0, 4))),
                                        ("c5_greedy", dict(B=16)), ("c5_topp0.9", dict(B=8))],
                          ids=["cluster_tail", "block_tail", "block_tail_ragged", "greedy", "top_p"])
-def test_withheld_copy_flags_the_batch(name, over):
+def test_lost_items_flag_the_batch(name, over):
     import speculative_decoding_rejection_verify_gb300 as sv
     d = W.generate(W.get(name, **over))
     sv.set_test_hooks(1)
@@ -38,7 +38,7 @@ def test_withheld_copy_flags_the_batch(name, over):
 
 
 @pytest.mark.parametrize("B", [32, 300])
-def test_withheld_copy_in_the_sampler(B):
+def test_lost_items_in_the_sampler(B):
     import speculative_decoding_rejection_verify_gb300 as sv
     d = W.generate(W.get("sample_c5", B=B))
     logits = to_dev(d["p"][:, 0, :].copy(), "cuda:0")

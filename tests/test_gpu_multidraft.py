@@ -130,7 +130,7 @@ def test_multi_bad_tokens_and_nonfinite_rows():
     compare_multi(g, o)
 
 
-def test_multi_withheld_copy_flags_the_batch():
+def test_multi_lost_items_flag_the_batch():
     import speculative_decoding_rejection_verify_gb300 as sv
     d = W.generate_multi(W.get("multi_c5", B=20, K=2, V=30000), 2)
     sv.set_test_hooks(1)
