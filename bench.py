@@ -177,6 +177,12 @@ def describe(w: W.Workload) -> str:
         (f" alpha~{w.alpha:g}" if w.alpha is not None and not w.greedy else "")
 
 
+def stream_kernel(w: W.Workload) -> str:
+    """The streaming pass's kernel for rows of whole 16-byte vectors (every workload here):
+    short-lived blocks in sampling and greedy modes, the persistent candidate-set grid for top-k."""
+    return "stats_kernel" if 0 < w.top_k < w.V and w.temperature > 0 else "stats_item_kernel"
+
+
 def launches_per_step(w: W.Workload) -> int:
     """Kernels of one step: the streaming pass and the per-request pass, plus the ragged row
     table and the nucleus pass (top-p without top-k).  The sampler's q(x) comes from the
@@ -539,7 +545,7 @@ def run_gpu(args, w: W.Workload):
                      "frac_vs_nominal": achieved / NOMINAL_HBM_GBS,
                      "step_frac_vs_nominal": logits_bytes / (step_ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS,
                      "traffic": traffic_for(w.label),
-                     "kernel": ("stats_kernel (streaming pass)" if graphs is None and not sampling else
+                     "kernel": (stream_kernel(w) + " (streaming pass)" if graphs is None and not sampling else
                                 "whole step" + (" (graph replay)" if graphs else "")),
                      "per_launch_ms": pass1_ms,
                      "step_frac": logits_bytes / (step_ms * 1e-3) / 1e9 / peak,
