@@ -42,6 +42,7 @@ constexpr int kCluster = 8;              // blocks sharing one request's draw wh
 constexpr int kStagesTopK = 3;           // top-k streaming pass: cp.async ring stages (3 blocks per SM)
 constexpr int kItemBlocksPerSM = 6;      // sampling / greedy streaming pass: resident blocks per SM
 constexpr int kItemsPerBlock = 2;        // items (16 KB each) per block of that pass
+constexpr int kMultiTiles = 2;           // multi-draft stage passes: tiles in flight per warp
 constexpr int kTile = 256;               // inverse-CDF tile: 32 lanes x 8 logits
 constexpr int kCandCap = 256;            // top-k candidates stored per chunk
 constexpr int kSegCap = 1024;            // running top-k candidates of a row segment (per buffer)
@@ -2745,24 +2746,90 @@ struct MultiRows {
   bool sub;                              // weights max(0, r_n - q_n); else r_n itself
 };
 
-// The stage's weights for the 8 logits [e0, e0 + 8) (logits past V weigh 0).  r follows the
-// recursion above term by term; every pass computes it with the same instructions.
-template <typename T, bool VEC>
-__device__ __forceinline__ void multi_weights8(const Params& P, const MultiRows& mr, int e0, float (&w)[8]) {
+// The stage's weights for 8 logits [e0, e0 + 8) (logits past V weigh 0): r follows the recursion
+// above term by term; every pass computes it with the same instructions.  Over aligned rows the
+// 16-byte vectors of every row the stage reads (P_0, then Q_0 .. Q_last) are loaded first
+// (multi_load8) and used after (multi_weights_raw), so that all of them are in flight at once.
+template <typename T>
+struct MultiRaw {
+  static constexpr int NV = 8 * (int)sizeof(T) / 16;  // vectors per row
+  uint4 v[SPEC_MAX_DRAFTS + 1][NV];
+};
+template <typename T>
+__device__ __forceinline__ void multi_load8(const Params& P, const MultiRows& mr, int e0, MultiRaw<T>& m) {
+  constexpr int NV = MultiRaw<T>::NV, VW = 16 / (int)sizeof(T);
+  const int last = mr.sub ? mr.n : mr.n - 1;
+  const uint4 ninf = sizeof(T) == 2 ? make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u)
+                                    : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
+#pragma unroll
+  for (int r = 0; r <= SPEC_MAX_DRAFTS; ++r)
+#pragma unroll
+    for (int h = 0; h < NV; ++h) {
+      const int e = e0 + h * VW;
+      m.v[r][h] = r <= last + 1 && e < P.V ? ldg_stream(static_cast<const T*>(mr.row[r]) + e) : ninf;
+    }
+}
+template <typename T>
+__device__ __forceinline__ void multi_weights_raw(const Params& P, const MultiRows& mr, const MultiRaw<T>& m,
+                                                  float (&w)[8]) {
+  constexpr int NV = MultiRaw<T>::NV;
+  const int last = mr.sub ? mr.n : mr.n - 1;
+  auto unpack8 = [&](int r, float (&z)[8]) {
+#pragma unroll
+    for (int h = 0; h < NV; ++h) {
+      const uint32_t q[4] = {m.v[r][h].x, m.v[r][h].y, m.v[r][h].z, m.v[r][h].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (sizeof(T) == 2) {
+          z[h * 8 + 2 * k] = bf16_lo(q[k]);
+          z[h * 8 + 2 * k + 1] = bf16_hi(q[k]);
+        } else {
+          z[h * 4 + k] = __uint_as_float(q[k]);
+        }
+      }
+    }
+  };
   float z[8];
-  load8<T, VEC>(static_cast<const T*>(mr.row[0]), e0, P.V, z);
+  unpack8(0, z);
 #pragma unroll
   for (int k = 0; k < 8; ++k) w[k] = ex2(fmaf(z[k], P.c2, -mr.L[0]));
-  const int last = mr.sub ? mr.n : mr.n - 1;
-  for (int i = 0; i <= last; ++i) {
-    load8<T, VEC>(static_cast<const T*>(mr.row[1 + i]), e0, P.V, z);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const float d = w[k] - ex2(fmaf(z[k], P.c2q, -mr.L[1 + i]));
-      if (i < mr.n)
-        w[k] = mr.Rinv[i] > 0.0f ? fmaxf(d, 0.0f) * mr.Rinv[i] : w[k];
-      else
-        w[k] = fmaxf(d, 0.0f);
+  for (int i = 0; i < SPEC_MAX_DRAFTS; ++i) {
+    if (i <= last) {
+      unpack8(1 + i, z);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float d = w[k] - ex2(fmaf(z[k], P.c2q, -mr.L[1 + i]));
+        if (i < mr.n)
+          w[k] = mr.Rinv[i] > 0.0f ? fmaxf(d, 0.0f) * mr.Rinv[i] : w[k];
+        else
+          w[k] = fmaxf(d, 0.0f);
+      }
+    }
+  }
+}
+template <typename T, bool VEC>
+__device__ __forceinline__ void multi_weights8(const Params& P, const MultiRows& mr, int e0, float (&w)[8]) {
+  if constexpr (VEC) {
+    MultiRaw<T> m;
+    multi_load8<T>(P, mr, e0, m);
+    multi_weights_raw<T>(P, mr, m, w);
+  } else {
+    const int last = mr.sub ? mr.n : mr.n - 1;
+    float z[8];
+    load8<T, VEC>(static_cast<const T*>(mr.row[0]), e0, P.V, z);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w[k] = ex2(fmaf(z[k], P.c2, -mr.L[0]));
+    for (int i = 0; i <= last; ++i) {
+      load8<T, VEC>(static_cast<const T*>(mr.row[1 + i]), e0, P.V, z);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float d = w[k] - ex2(fmaf(z[k], P.c2q, -mr.L[1 + i]));
+        if (i < mr.n)
+          w[k] = mr.Rinv[i] > 0.0f ? fmaxf(d, 0.0f) * mr.Rinv[i] : w[k];
+        else
+          w[k] = fmaxf(d, 0.0f);
+      }
     }
   }
 }
@@ -2776,14 +2843,31 @@ __device__ float multi_pass(const Params& P, const MultiRows& mr, bool draw, flo
                             int* clamp) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int ntile = (P.V + kTile - 1) / kTile;
-  for (int i = warp; i < ntile; i += kWarps) {
-    float w[8];
-    multi_weights8<T, VEC>(P, mr, i * kTile + lane * 8, w);
+  auto tile_sum = [&](int i, const float (&w)[8]) {
     float s = 0.0f;
 #pragma unroll
     for (int k = 0; k < 8; ++k) s += w[k];
     s = warp_sum(s);
-    if (lane == 0) wt[i] = s;
+    if (lane == 0 && i < ntile) wt[i] = s;
+  };
+  if constexpr (VEC) {
+    for (int i0 = warp; i0 < ntile; i0 += kMultiTiles * kWarps) {  // kMultiTiles tiles a warp, all loads first
+      MultiRaw<T> m[kMultiTiles];
+#pragma unroll
+      for (int g = 0; g < kMultiTiles; ++g) multi_load8<T>(P, mr, (i0 + g * kWarps) * kTile + lane * 8, m[g]);
+#pragma unroll
+      for (int g = 0; g < kMultiTiles; ++g) {
+        float w[8];
+        multi_weights_raw<T>(P, mr, m[g], w);
+        tile_sum(i0 + g * kWarps, w);
+      }
+    }
+  } else {
+    for (int i = warp; i < ntile; i += kWarps) {
+      float w[8];
+      multi_weights8<T, VEC>(P, mr, i * kTile + lane * 8, w);
+      tile_sum(i, w);
+    }
   }
   __syncthreads();
   const int L = (ntile + kThreads - 1) / kThreads;
