@@ -346,3 +346,22 @@ def test_maximum_k_with_topk_and_topp():
     d = W.generate(W.get("c5_topp0.9", B=3, K=sv.MAX_K, V=60000, tau=0.6))
     res, _, _ = _check(d)
     assert res["requests"] == 3
+
+
+# ------------------------------------------------------------------------------------------------
+# the short-block streaming pass: each block takes two consecutive 16 KB items, so with an odd
+# number of chunks per row blocks straddle rows (the second item in the next row, or the next
+# request), and an odd number of items in all leaves the last block one item
+# ------------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("V,dtype,B,K,greedy", [(16392, "bf16", 5, 3, False), (8196, "f32", 7, 2, False),
+                                                 (16392, "bf16", 3, 4, True), (16392, "bf16", 200, 1, False)],
+                         ids=["bf16_3chunks", "f32_3chunks", "greedy_odd_items", "many_requests"])
+def test_streaming_blocks_straddle_rows(V, dtype, B, K, greedy):
+    w = W.get("c5_greedy" if greedy else "c5_a0.8", B=B, K=K, V=V, dtype=dtype)
+    per = 16384 // (2 if dtype == "bf16" else 4)
+    nchunk = -(-V // per)
+    rows = B * (K + 1 if greedy else 2 * K + 1)
+    assert nchunk % 2 == 1 or (rows * nchunk) % 2 == 1  # the layouts this test is about
+    d = W.generate(w)
+    res, _, _ = _check(d)  # tokens, counts, flags and every row's normaliser against the oracle
+    assert res["requests"] == B
