@@ -39,7 +39,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kChunkBytes = 16384;      // bytes of logits per work item (16 B per thread x 4)
 constexpr int kCluster = 8;              // blocks sharing one request's draw when requests are few
-constexpr int kStagesTopK = 3;           // top-k streaming pass: cp.async ring stages (3 blocks per SM)
+constexpr int kStagesTopK = 2;           // top-k streaming pass: cp.async ring stages (4 blocks per SM)
 constexpr int kItemBlocksPerSM = 6;      // sampling / greedy streaming pass: resident blocks per SM
 constexpr int kItemsPerBlock = 2;        // items (16 KB each) per block of that pass
 constexpr int kMultiTiles = 2;           // multi-draft stage passes: tiles in flight per warp
@@ -2521,7 +2521,7 @@ __device__ __forceinline__ void greedy_vec(uint4 (&raw)[Cfg<T>::LOADS], int n, i
 // over from chunk to chunk.  No block waits for another and nothing is counted: pass 2 starts
 // when this grid is done.
 template <typename T, int MODE, bool VEC>
-__global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
+__global__ void __launch_bounds__(kThreads, 4) stats_kernel(const Params P) {
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ Smem sm;
   pdl_launch_next();  // the next pass may launch now; it waits for this grid before reading
