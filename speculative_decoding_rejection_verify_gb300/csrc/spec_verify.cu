@@ -1996,18 +1996,29 @@ __device__ void finish_request(const Params& P, int b, Smem& sm, unsigned char* 
   const int nrows = MODE == kGreedy ? Kb + 1 : 2 * Kb + 1;
   // ---- row statistics ----
   if (MODE == kSample) {
-    for (int r = warp; r < nrows; r += kWarps) {
-      const int rp = r <= Kb ? r : K + 1 + (r - Kb - 1);
-      const float2* part = P.partial + ((size_t)b * P.R + rp) * P.nchunk * kWarps;
-      const float c2 = r > Kb ? P.c2q : P.c2;
-      float m = -INFINITY, s = 0.0f;
+    // each row's summaries merged by a group of G lanes, so that every row's loads go out in one
+    // round (G divides 32: a group never spans two warps)
+    const int G = nrows <= 8 ? 32 : (nrows <= 16 ? 16 : (nrows <= 32 ? 8 : 4));
+    const int gi = t / G, gl = t % G, per = P.nchunk * kWarps;
+    for (int r0 = 0; r0 < nrows; r0 += kThreads / G) {
+      const int r = r0 + gi;
+      float m = -INFINITY, s = 0.0f, c2 = P.c2;
+      if (r < nrows) {
+        const int rp = r <= Kb ? r : K + 1 + (r - Kb - 1);
+        const float2* part = P.partial + ((size_t)b * P.R + rp) * per;
+        c2 = r > Kb ? P.c2q : P.c2;
 #pragma unroll 4
-      for (int c = lane; c < P.nchunk * kWarps; c += 32) {
-        float2 pc = __ldg(part + c);
-        lse_merge(m, s, pc.x, pc.y, c2);
+        for (int c = gl; c < per; c += G) {
+          float2 pc = __ldg(part + c);
+          lse_merge(m, s, pc.x, pc.y, c2);
+        }
       }
-      lse_warp(m, s, c2);
-      if (lane == 0) {
+      for (int o = G >> 1; o > 0; o >>= 1) {
+        const float mo = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+        const float so = __shfl_xor_sync(0xFFFFFFFFu, s, o);
+        lse_merge(m, s, mo, so, c2);
+      }
+      if (r < nrows && gl == 0) {
         sm.rowM[r] = m;
         sm.rowS[r] = s;
         sm.rowT[r] = -INFINITY;
