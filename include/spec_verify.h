@@ -248,9 +248,10 @@ spec_status_t spec_sample(const void* logits, const float* u, const spec_samplin
  *   out_flags     [B] int32 or NULL: SPEC_FLAG_* bits (a non-finite row anywhere in a request leaves
  *                 it without a result: n_acc 0, tokens -1, chain -1);
  *   workspace     spec_verify_multi_workspace_bytes(...) bytes of device memory, 256-B aligned.
- * Every chain has K_max drafts (no k_per_row).  1 <= N <= SPEC_MAX_DRAFTS.  With N = 1 the results
- * are spec_verify's.  Launches the row table, the streaming pass over every row read, and one block
- * per request for the decisions; asynchronous on `stream`.
+ * Every chain has K_max drafts (no k_per_row).  1 <= N <= SPEC_MAX_DRAFTS.  With N = 1 the rule is
+ * spec_verify's (the draws' sums may round differently).  Launches the row table, the streaming pass
+ * over every row read, and the per-request pass (a cluster of 4 blocks per request when sampling,
+ * one block when greedy); asynchronous on `stream`.
  */
 size_t spec_verify_multi_workspace_bytes(int32_t B, int32_t N, int32_t K_max, int32_t V, spec_dtype_t dtype);
 spec_status_t spec_verify_multi(const void* p_logits, const void* q_logits, const int32_t* draft_tokens,

@@ -43,6 +43,7 @@ constexpr int kStagesTopK = 2;           // top-k streaming pass: cp.async ring 
 constexpr int kItemBlocksPerSM = 6;      // sampling / greedy streaming pass: resident blocks per SM
 constexpr int kItemsPerBlock = 2;        // items (16 KB each) per block of that pass
 constexpr int kMultiTiles = 2;           // multi-draft stage passes: tiles in flight per warp
+constexpr int kMultiCluster = 4;         // multi-draft, sampling: blocks per request (a cluster)
 constexpr int kTile = 256;               // inverse-CDF tile: 32 lanes x 8 logits
 constexpr int kCandCap = 256;            // top-k candidates stored per chunk
 constexpr int kSegCap = 1024;            // running top-k candidates of a row segment (per buffer)
@@ -2746,7 +2747,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads) fin
 // with the single-draft rule; with every candidate rejected one token is drawn from r_N.  The
 // streaming pass summarises every row the step reads: sub-request b N + n holds chain n of request
 // b, and a row table leaves out row 0 of every chain after the first (the shared position is read
-// once).  The per-request pass below takes the decisions, one block per request.
+// once).  The per-request pass below takes the decisions: in sampling mode a cluster of
+// kMultiCluster blocks per request, which share each stage pass and draw; greedy, one block.
 
 // The rows of the first position's stage n (weights max(0, r_n - q_n)): P_0 and Q_0..Q_n.
 struct MultiRows {
@@ -2990,6 +2992,191 @@ __device__ float multi_pass(const Params& P, const MultiRows& mr, bool draw, flo
   return total;
 }
 
+// multi_pass shared by the CL blocks of a cluster: each block sums the stage's weights over its
+// own contiguous share of the tiles; the shares' totals are read from every block's shared memory
+// in rank order, so every block forms the same R; with `draw`, the block whose share holds the
+// target searches its tiles and writes the token into rank 0's shared memory.  Every block takes
+// both cluster barriers on every path.
+template <typename T, bool VEC, int CL>
+__device__ float multi_pass_cluster(const Params& P, const MultiRows& mr, bool draw, float u, float* wt, Smem& sm,
+                                    int* clamp) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
+  const int rank = (int)cl.block_rank();
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int ntile = (P.V + kTile - 1) / kTile;
+  const int per = (ntile + CL - 1) / CL;
+  const int i0 = min(ntile, rank * per), nt = min(ntile, i0 + per) - i0;
+  auto tile_sum = [&](int i, const float (&w)[8]) {
+    float s = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) s += w[k];
+    s = warp_sum(s);
+    if (lane == 0 && i < nt) wt[i] = s;
+  };
+  if constexpr (VEC) {
+    for (int j0 = warp; j0 < nt; j0 += kMultiTiles * kWarps) {
+      MultiRaw<T> m[kMultiTiles];
+#pragma unroll
+      for (int g = 0; g < kMultiTiles; ++g) {
+        const int j = j0 + g * kWarps;
+        multi_load8<T>(P, mr, (j < nt ? i0 + j : ntile) * kTile + lane * 8, m[g]);
+      }
+#pragma unroll
+      for (int g = 0; g < kMultiTiles; ++g) {
+        float w[8];
+        multi_weights_raw<T>(P, mr, m[g], w);
+        tile_sum(j0 + g * kWarps, w);
+      }
+    }
+  } else {
+    for (int j = warp; j < nt; j += kWarps) {
+      float w[8];
+      multi_weights8<T, VEC>(P, mr, (i0 + j) * kTile + lane * 8, w);
+      tile_sum(j, w);
+    }
+  }
+  __syncthreads();
+  // this share's runs of tiles per thread, a block scan, and its total
+  const int L = (nt + kThreads - 1) / kThreads;
+  const int s0 = t * L, s1 = min(s0 + L, nt);
+  float seg = 0.0f;
+  for (int i = s0; i < s1; ++i) seg += wt[i];
+  float incl = seg;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sm.red_s[warp] = incl;
+  __syncthreads();
+  float off = 0.0f, mine = 0.0f;
+  for (int w = 0; w < kWarps; ++w) {
+    if (w < warp) off += sm.red_s[w];
+    mine += sm.red_s[w];
+  }
+  incl += off;
+  if (t == 0) sm.cl_total = mine;
+  cl.sync();
+  float tot[CL], R = 0.0f;
+#pragma unroll
+  for (int r = 0; r < CL; ++r) {
+    tot[r] = *cl.map_shared_rank(&sm.cl_total, r);
+    R += tot[r];
+  }
+  if (draw && R > 0.0f) {
+    const float target = u * R;
+    int owner = -1, last = -1;
+    float cum = 0.0f, base = 0.0f, base_last = 0.0f;
+    for (int r = 0; r < CL; ++r) {
+      if (tot[r] > 0.0f) {
+        if (owner < 0 && target < cum + tot[r]) {
+          owner = r;
+          base = cum;
+        }
+        last = r;
+        base_last = cum;
+      }
+      cum += tot[r];
+    }
+    if (owner < 0) {  // rounding: the last share with mass searches (and clamps)
+      owner = last;
+      base = base_last;
+    }
+    if (rank == owner) {
+      const float tl0 = target - base;  // the mass to pass inside this share
+      if (t == 0) {
+        sm.seg_first = kThreads;
+        sm.found = 0;
+      }
+      __syncthreads();
+      if (tl0 < incl) atomicMin(&sm.seg_first, t);
+      __syncthreads();
+      const int tf = sm.seg_first;
+      if (t == (tf == kThreads ? 0 : tf)) {
+        int found = -1;
+        float run = incl - seg;
+        if (tf < kThreads)
+          for (int i = s0; i < s1; ++i) {
+            if (tl0 < run + wt[i]) {
+              found = i;
+              break;
+            }
+            run += wt[i];
+          }
+        if (found < 0) {  // rounding left the target past the sums: the last tile with weight
+          int i = nt - 1;
+          while (i > 0 && !(wt[i] > 0.0f)) --i;
+          run = 0.0f;
+          for (int j = 0; j < i; ++j) run += wt[j];
+          found = i;
+          sm.found = 2;
+        } else {
+          sm.found = 1;
+        }
+        sm.tile = found;
+        sm.tile_base = run;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        const int tile = i0 + sm.tile;
+        bool clamped = sm.found == 2;
+        float w[8];
+        multi_weights8<T, VEC>(P, mr, tile * kTile + lane * 8, w);
+        float ls = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ls += w[k];
+        float li = ls;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xFFFFFFFFu, li, o);
+          if (lane >= o) li += y;
+        }
+        const float tl = tl0 - sm.tile_base;
+        const unsigned hit = clamped ? 0u : __ballot_sync(0xFFFFFFFFu, tl < li);
+        int yl, ye = -1;
+        float margin = 0.0f;
+        if (hit) {
+          yl = __ffs(hit) - 1;
+          if (lane == yl) {
+            float run = li - ls;
+            for (int k = 0; k < 8; ++k) {
+              if (tl < run + w[k]) {
+                ye = k;
+                margin = fminf(tl - run, run + w[k] - tl) / R;
+                break;
+              }
+              run += w[k];
+            }
+            if (ye < 0) {
+              for (int k = 7; k >= 0 && ye < 0; --k)
+                if (w[k] > 0.0f) ye = k;
+              clamped = true;
+            }
+          }
+        } else {
+          const unsigned pos = __ballot_sync(0xFFFFFFFFu, ls > 0.0f);
+          yl = pos ? 31 - __clz(pos) : 0;
+          if (lane == yl)
+            for (int k = 7; k >= 0 && ye < 0; --k)
+              if (w[k] > 0.0f) ye = k;
+          clamped = true;
+        }
+        if (lane == yl) {
+          Smem* lead = cl.map_shared_rank(&sm, 0);
+          lead->y = tile * kTile + yl * 8 + (ye < 0 ? 0 : ye);
+          lead->margin = clamped ? 0.0f : margin;
+          if (clamped) *clamp = 1;
+        }
+      }
+      if (*clamp) atomicOr(&cl.map_shared_rank(&sm, 0)->flags, SPEC_FLAG_CDF_CLAMP);
+      *clamp = 0;
+    }
+  }
+  cl.sync();  // rank 0 holds the token; no block leaves while another may still read its total
+  return R;
+}
+
 // The bonus-style draw of a whole row from p alone (its chunk masses from the stored (max, sum)
 // pairs pick the chunk; only that chunk is read again).  Whole block; result in sm.y, sm.margin.
 template <typename T, bool VEC>
@@ -3049,13 +3236,16 @@ __device__ void draw_from_summaries(const Params& P, const float2* part, const T
 // The per-request pass of spec_verify_multi (MODE kSample or kGreedy; P.B counts sub-requests,
 // P.K is the drafts per chain).  Dynamic shared memory: the CDF ring, the tile / chunk sums, then
 // the rows' (max, sum) or argmax.
-template <typename T, int MODE, bool VEC>
-__global__ void __launch_bounds__(kThreads) finish_multi_kernel(const Params P, int N, int32_t* out_chain) {
+template <typename T, int MODE, bool VEC, int CL>
+__global__ void __launch_bounds__(kThreads, sizeof(T) == 2 ? 3 : 2) finish_multi_kernel(const Params P, int N, int32_t* out_chain) {
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ Smem sm;
   pdl_wait();
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int b = blockIdx.x, K = P.K, R = P.R, V = P.V;
+  // with CL > 1 the CL blocks of a cluster all take the request's decisions (identically) and
+  // share its stage passes and draws; only rank 0 writes results
+  const bool lead = CL == 1 || cooperative_groups::this_cluster().block_rank() == 0;
+  const int b = (int)(blockIdx.x / CL), K = P.K, R = P.R, V = P.V;
   uint4* ring = reinterpret_cast<uint4*>(dyn);
   const int ntile = (V + kTile - 1) / kTile;
   float* wt = reinterpret_cast<float*>(dyn + (VEC ? (size_t)kDrawStages * kDrawStageBytes : 0));
@@ -3115,14 +3305,14 @@ __global__ void __launch_bounds__(kThreads) finish_multi_kernel(const Params P, 
   __syncthreads();
   int32_t* tok = P.out_tokens + (size_t)b * (K + 1);
   auto finish = [&](int nacc, int chain) {
-    if (t == 0) {
+    if (t == 0 && lead) {
       P.out_nacc[b] = nacc;
       if (out_chain) out_chain[b] = chain;
       if (P.flags) P.flags[b] = sm.flags;
     }
   };
   if (sm.nonfinite) {
-    if (t <= K) tok[t] = -1;
+    if (t <= K && lead) tok[t] = -1;
     if (t == 0) sm.flags |= SPEC_FLAG_NONFINITE;
     __syncthreads();
     finish(0, -1);
@@ -3176,12 +3366,10 @@ __global__ void __launch_bounds__(kThreads) finish_multi_kernel(const Params P, 
   auto Lp = [&](int n, int j) { return rM[n * R + j] * P.c2 + log2f(rS[n * R + j]); };
   auto Lq = [&](int n, int j) { return rM[n * R + K + 1 + j] * P.c2q + log2f(rS[n * R + K + 1 + j]); };
   int clamp = 0;
-  if (K == 0) {  // no drafts: the one token is drawn from P_0
-    draw_from_summaries<T, VEC>(P, part(0, 0), prow_n(0, 0), rM[0], u, wt, ring, sm, &clamp);
-    if (t == 0) {
-      tok[0] = sm.y;
-      if (clamp) sm.flags |= SPEC_FLAG_CDF_CLAMP;
-    }
+  if (K == 0) {  // no drafts: the one token is drawn from P_0 (one chunk: rank 0 alone)
+    if (lead) draw_from_summaries<T, VEC>(P, part(0, 0), prow_n(0, 0), rM[0], u, wt, ring, sm, &clamp);
+    if (t == 0 && lead) tok[0] = sm.y;
+    if (clamp) atomicOr(&sm.flags, SPEC_FLAG_CDF_CLAMP);  // set by the lane that drew
     __syncthreads();
     finish(0, -1);
     return;
@@ -3222,20 +3410,24 @@ __global__ void __launch_bounds__(kThreads) finish_multi_kernel(const Params P, 
     mr.n = n;
     mr.sub = true;
     const bool last = n == N - 1;
-    const float Rn = multi_pass<T, VEC>(P, mr, last, u, wt, sm, &clamp);
+    const float Rn = CL > 1 ? multi_pass_cluster<T, VEC, CL>(P, mr, last, u, wt, sm, &clamp)
+                            : multi_pass<T, VEC>(P, mr, last, u, wt, sm, &clamp);
     mr.Rinv[n] = Rn > 0.0f ? 1.0f / Rn : 0.0f;
     if (!(Rn > 0.0f)) {
       if (t == 0) sm.flags |= SPEC_FLAG_RESIDUAL_ZERO;
       __syncthreads();
       if (last) {  // nothing of r_n survives q_n (rounding): the draw from r_n itself
         mr.sub = false;
-        multi_pass<T, VEC>(P, mr, true, u, wt, sm, &clamp);
+        if (CL > 1)
+          multi_pass_cluster<T, VEC, CL>(P, mr, true, u, wt, sm, &clamp);
+        else
+          multi_pass<T, VEC>(P, mr, true, u, wt, sm, &clamp);
       }
     }
   }
   if (chain < 0) {
-    if (t <= K) tok[t] = t == 0 ? sm.y : -1;
-    if (t == 0 && clamp) sm.flags |= SPEC_FLAG_CDF_CLAMP;
+    if (t <= K && lead) tok[t] = t == 0 ? sm.y : -1;
+    if (clamp) atomicOr(&sm.flags, SPEC_FLAG_CDF_CLAMP);  // set by the lane that drew
     __syncthreads();
     finish(0, -1);
     return;
@@ -3258,7 +3450,7 @@ __global__ void __launch_bounds__(kThreads) finish_multi_kernel(const Params P, 
     const unsigned rej = __ballot_sync(0xFFFFFFFFu, j < K && !acc);
     const int js = rej ? __ffs(rej) : K;  // the position that draws (a rejection, or K: the bonus)
     if (rej && lane == js - 1 && bad) sm.flags |= SPEC_FLAG_BAD_TOKEN;
-    if (lane <= K) tok[lane] = lane == 0 ? draft(chain, 0) : (lane < js ? draft(chain, lane) : -1);
+    if (lane <= K && lead) tok[lane] = lane == 0 ? draft(chain, 0) : (lane < js ? draft(chain, lane) : -1);
     if (lane == 0) sm.jstar = js;
   }
   __syncthreads();
@@ -3272,21 +3464,24 @@ __global__ void __launch_bounds__(kThreads) finish_multi_kernel(const Params P, 
     d.Lq = Lq(chain, js);
     d.c2q = P.c2q;
     d.Tq = -INFINITY;
-    const float Rr = draw_range<T, VEC, false>(P, prow_n(chain, js), qrow_n(chain, js), d, 0, V, true, u, 0.0f, 0.0f,
-                                               wt, ring, sm, &clamp);
-    if (!(Rr > 0.0f)) {  // max(0, p - q) vanished through rounding: draw from p
+    const float Rr =
+        CL > 1 ? cluster_draw<T, VEC, false, CL>(P, prow_n(chain, js), qrow_n(chain, js), d, u, wt, ring, sm, &clamp)
+               : draw_range<T, VEC, false>(P, prow_n(chain, js), qrow_n(chain, js), d, 0, V, true, u, 0.0f, 0.0f, wt,
+                                           ring, sm, &clamp);
+    if (!(Rr > 0.0f)) {  // max(0, p - q) vanished through rounding: draw from p (R is the same in every block)
       if (t == 0) sm.flags |= SPEC_FLAG_RESIDUAL_ZERO;
       d.resid = false;
-      draw_range<T, VEC, false>(P, prow_n(chain, js), prow_n(chain, js), d, 0, V, true, u, 0.0f, 0.0f, wt, ring, sm,
-                                &clamp);
+      if (CL > 1)
+        cluster_draw<T, VEC, false, CL>(P, prow_n(chain, js), prow_n(chain, js), d, u, wt, ring, sm, &clamp);
+      else
+        draw_range<T, VEC, false>(P, prow_n(chain, js), prow_n(chain, js), d, 0, V, true, u, 0.0f, 0.0f, wt, ring, sm,
+                                  &clamp);
     }
-  } else {  // every draft of the chain accepted: the extra token from its row K
+  } else if (lead) {  // every draft of the chain accepted: the extra token from its row K (one chunk)
     draw_from_summaries<T, VEC>(P, part(chain, K), prow_n(chain, K), rM[chain * R + K], u, wt, ring, sm, &clamp);
   }
-  if (t == 0) {
-    tok[js] = sm.y;
-    if (clamp) sm.flags |= SPEC_FLAG_CDF_CLAMP;
-  }
+  if (t == 0 && lead) tok[js] = sm.y;
+  if (clamp) atomicOr(&sm.flags, SPEC_FLAG_CDF_CLAMP);  // set by the lane that drew
   __syncthreads();
   finish(js, chain);
 }
@@ -3462,6 +3657,27 @@ static cudaError_t launch_stream(const Params& P, uint64_t items, cudaStream_t s
   }
 }
 
+// The same with the blocks in clusters of `cl` along x.
+template <typename... A>
+static cudaError_t launch_cluster_after(void (*kern)(A...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                        bool pdl, unsigned cl, A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = cl;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <typename T, int MODE, bool VEC>
 static cudaError_t launch_t(const Params& P, uint32_t items, cudaStream_t st) {
   const int es = (int)sizeof(T);
@@ -3510,11 +3726,13 @@ static cudaError_t launch_mode(int mode, bool vec, const Params& P, uint32_t ite
 // spec_verify_multi: the row table, the streaming pass over the table, the per-request pass.
 template <typename T, int MODE, bool VEC>
 static cudaError_t launch_multi(const Params& P, int Breq, int N, int32_t* out_chain, cudaStream_t st) {
-  auto k2 = finish_multi_kernel<T, MODE, VEC>;
+  auto k2 = finish_multi_kernel<T, MODE, VEC, 1>;
+  auto kc = finish_multi_kernel<T, MODE, VEC, kMultiCluster>;
   const int ntile = (P.V + kTile - 1) / kTile;
   const size_t d2 = (VEC ? (size_t)kDrawStages * kDrawStageBytes : 0) +
                     (size_t)(ntile > P.nchunk ? ntile : P.nchunk) * sizeof(float) + (size_t)2 * N * P.R * sizeof(float);
   cudaError_t e = prepare(k2, d2);
+  if (e == cudaSuccess && MODE == kSample) e = prepare(kc, d2);
   if (e != cudaSuccess) return e;
   const uint32_t rows = (uint32_t)Breq * (uint32_t)(N * P.R - (N - 1));
   const uint64_t items = (uint64_t)rows * (uint64_t)P.nchunk;
@@ -3525,6 +3743,9 @@ static cudaError_t launch_multi(const Params& P, int Breq, int N, int32_t* out_c
   if (e != cudaSuccess) return e;
   e = launch_stream<T, MODE, VEC>(P, items, st);
   if (e != cudaSuccess) return e;
+  if (MODE == kSample)  // a cluster per request shares its stage passes and draws
+    return launch_cluster_after(kc, dim3((unsigned)Breq * kMultiCluster), dim3(kThreads), d2, st, true,
+                                (unsigned)kMultiCluster, P, N, out_chain);
   return launch_after(k2, dim3((unsigned)Breq), dim3(kThreads), d2, st, true, P, N, out_chain);
 }
 

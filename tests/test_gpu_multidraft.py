@@ -5,9 +5,9 @@ rejections leave of p, and the first accepted chain is verified on with the sing
 rule and its losslessness pins are in oracle.c and test_oracle_pins_multidraft.py).  The emitted
 tokens, the accepted count and the chosen chain must equal the oracle's, except where a decision
 that differs has an oracle margin below 1e-5 (at most max(2, B/100) requests).  One chain gives
-spec_verify's results bit for bit; greedy; bad tokens; a NaN in a row the step never reads (row 0 of
-a later chain) changes nothing, a NaN in a row it reads flags the request; the bounded-wait failure
-path; argument checks."""
+spec_verify's tokens on the test's batch; greedy; bad tokens; a NaN in a row the step never reads (row 0 of
+a later chain) changes nothing, a NaN in a row it reads flags the request; lost streaming items
+flag every request; argument checks."""
 import numpy as np
 import pytest
 
