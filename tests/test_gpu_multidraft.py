@@ -74,10 +74,14 @@ CASES = [
     dict(N=3, over=dict(B=40, K=1, V=3001, tau=3.0)),
     dict(N=4, over=dict(B=16, K=2, V=128256, tau=4.0)),
     dict(N=2, over=dict(B=200, K=4, V=40000, tau=0.8)),
+    # rows of one or two 256-logit tiles: most blocks of a request's cluster hold no tile at all
+    dict(N=3, over=dict(B=24, K=2, V=8, tau=3.0)),
+    dict(N=4, over=dict(B=24, K=2, V=264, dtype="f32", tau=3.0)),
 ]
 
 
-@pytest.mark.parametrize("case", CASES, ids=["n2", "n4_f32_tq", "n3_k1_odd_v", "n4_wide_low_alpha", "n2_many"])
+@pytest.mark.parametrize("case", CASES, ids=["n2", "n4_f32_tq", "n3_k1_odd_v", "n4_wide_low_alpha", "n2_many",
+                                             "n3_one_tile", "n4_two_tiles_f32"])
 def test_multi_parity(case):
     d = W.generate_multi(W.get("multi_c5", **case["over"]), case["N"])
     g, o = _gpu(d), _oracle(d)
