@@ -122,8 +122,9 @@ size_t spec_verify_workspace_bytes(int32_t B, int32_t K_max, int32_t V, spec_dty
  *   out_stats     host struct of device pointers, or NULL;
  *   workspace     device memory of at least spec_verify_workspace_bytes(...) bytes, 256-B aligned.
  * Launches two kernels (three with k_per_row): a streaming pass over every valid logit row that
- * leaves per-chunk summaries in the workspace, then one block per request for the decision and
- * the draw.  Returns SPEC_OK once the work is enqueued.
+ * leaves per-chunk summaries in the workspace, then the per-request pass for the decision and the
+ * draw (one block per request; a cluster of 8 blocks per request when the batch has fewer requests
+ * than the GPU has SMs and the rows are long).  Returns SPEC_OK once the work is enqueued.
  */
 spec_status_t spec_verify(const void* p_logits, const void* q_logits, const int32_t* draft_tokens,
                           const int32_t* k_per_row, const float* u_accept, const float* u_resample,
