@@ -284,15 +284,6 @@ __device__ __forceinline__ void load_raw(const T* __restrict__ base, int n, uint
   }
 }
 
-// The thread's vectors of a chunk staged in shared memory by issue_chunk().
-template <typename T>
-__device__ __forceinline__ void load_stage(const uint4* stage, int n, float (&v)[Cfg<T>::PER]) {
-  uint4 raw[Cfg<T>::LOADS];
-#pragma unroll
-  for (int l = 0; l < Cfg<T>::LOADS; ++l) raw[l] = stage[l * kThreads + threadIdx.x];
-  unpack<T>(raw, n, v);
-}
-
 // cp.async ring: each thread copies its own 16-byte vectors of a chunk into a stage and later
 // reads exactly those bytes back, so only its own wait_group orders the copy and the read.
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
@@ -307,17 +298,11 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // shared memory
 // ------------------------------------------------------------------------------------------------
 struct Smem {
-  int item;
-  int last;
-  int req;
   float red_m[kWarps];
   float red_s[kWarps];
   int red_i[kWarps];
   uint32_t red_k[kWarps];
   int red_c[kWarps];
-  int nsurv;
-  int nkept;
-  uint32_t meta;
   // running top-k of the row segment a block streams
   int seg_n, seg_c0, seg_flags, seg_tight, seg_cur, seg_kept;
   uint32_t seg_theta;
