@@ -163,3 +163,12 @@ def test_multi_argument_checks():
     assert call(2, top_k=10) == 2 and call(2, top_p=0.9) == 2
     assert lib.spec_verify_multi(p, p, p, p, p, ctypes.byref(smp), p, p, p, p, 0, 2, 2, 100, 0, None, 0, s) == 0
     torch.cuda.synchronize()
+
+
+def test_multi_full_size():
+    """The benchmarked multi-draft batch (256 requests x 4 chains x 4 drafts over 128256 bf16
+    logits), in the launch configuration bench.py times."""
+    d = W.generate_multi(W.get("multi_c5"), 4)
+    g, o = _gpu(d), _oracle(d)
+    compare_multi(g, o)
+    assert (o["chain"] == 0).any() and (o["chain"] > 0).any()
