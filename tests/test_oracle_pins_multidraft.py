@@ -240,7 +240,33 @@ def test_greedy_multi():
         np.testing.assert_array_equal(out["tokens"][b, 1: n + 1], list(x[b, c, 1:n]) + [g[b, c, n]])
 
 
+def test_multi_margins_hand_computed(lib=None):
+    """Margins of the multi-draft decision on binary-fraction rows (V = 4, N = 2, K = 1): each
+    candidate's |u_n - r_n(x_n) / q_n(x_n)| and the draw's distance to the nearer CDF edge."""
+    nan = np.nan
+    # candidate 0 rejected (r_0(2) / q_0(2) = 0.5 < u_0 = 0.75), r_1 = norm(max(0, P_0 - Q_0)) =
+    # [1, 0, 0, 0], candidate 1 accepted (r_1(0) / q_1(0) = 2), then chain 1's extra token from
+    # its row 1 = [1/2, 1/2, 0, 0] at u = 0.3: token 0, margin min(0.3, 0.5 - 0.3) = 0.2
+    P = np.array([[[0.5, 0.25, 0.125, 0.125], [0.25] * 4],
+                  [[nan] * 4, [0.5, 0.5, 0.0, 0.0]]])
+    Q = np.array([[[0.25] * 4], [[0.5, 0.5, 0.0, 0.0]]])
+    o = oracle.decide_multi(P, Q, [[2], [0]], [[0.75], [0.9]], 0.3, lib=lib)
+    assert o["chain"] == 1 and o["n_acc"] == 1 and list(o["tokens"]) == [0, 0]
+    np.testing.assert_allclose(o["accept_margin"], [[0.25], [1.1]], rtol=0, atol=1e-12)
+    assert abs(o["sample_margin"] - 0.2) < 1e-12
+    # both candidates outside p's support: rejected with margins u_n, r_2 = P_0, the draw at
+    # u = 0.7 over [1/2, 1/2, 0, 0]: token 1, margin min(0.7 - 0.5, 1 - 0.7) = 0.2
+    P = np.array([[[0.5, 0.5, 0.0, 0.0], [0.25] * 4], [[nan] * 4, [0.25] * 4]])
+    Q = np.array([[[0.0, 0.0, 0.5, 0.5]], [[0.0, 0.0, 0.5, 0.5]]])
+    o = oracle.decide_multi(P, Q, [[2], [3]], [[0.3], [0.6]], 0.7, lib=lib)
+    assert o["chain"] == -1 and o["n_acc"] == 0 and list(o["tokens"]) == [1, -1]
+    np.testing.assert_allclose(o["accept_margin"], [[0.3], [0.6]], rtol=0, atol=1e-12)
+    assert abs(o["sample_margin"] - 0.2) < 1e-12
+
+
 MUTANTS = {
+    "multi_accept_margin_unnormalised": ("accept_margin[(size_t)n * K] = (c > 0.0) ? fabs(u - a / c) : INFINITY;",
+                                         "accept_margin[(size_t)n * K] = (c > 0.0) ? fabs(u * c - a) : INFINITY;"),
     "every_candidate_against_p": ("      a = r[xn];\n", "      a = P[xn];\n"),
     "residual_not_renormalised": ("      for (int v = 0; v < V; ++v) r[v] = rest[v] / R;", "      for (int v = 0; v < V; ++v) r[v] = rest[v];"),
     "last_draw_from_p": ("    return flags | inverse_cdf(r, V, R, ur, &out_tokens[0], sample_margin);",
@@ -251,6 +277,10 @@ MUTANTS = {
 
 
 def _pins_fail(lib):
+    try:
+        test_multi_margins_hand_computed(lib)
+    except AssertionError:
+        return True
     cases = [make_case(np.random.default_rng(100 + s), 4, N, K) for s, (N, K) in enumerate([(2, 1), (3, 1), (2, 2)])]
     for c in cases:
         try:
